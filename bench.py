@@ -1,0 +1,432 @@
+"""Benchmark of the KV-cache compression path on GB300.
+
+One step = one full pass of the path over the workload's KV: kvc_encode (fused
+smoothing + Hadamard + quantize + pack, then the lossless chunk stages) followed
+by kvc_decode (lossless decode, then fused reconstruction), all layers.
+
+Metric: KV encode/decode GB/s counted on uncompressed input bytes (K+V of all
+layers), the convention of "Beyond Compression Ratio: High-Throughput KV
+Compression for Disaggregated LLM Serving", Table 1 (GB/s x ms = the raw bytes for
+both directions).  `value` = raw bytes per step / device time per step, i.e. the
+combined encode+decode throughput s_p of "KVServe" §3.1 (1/s_p = 1/s_enc + 1/s_dec);
+encode and decode are also reported apart.
+
+  python bench.py [--workload llama8b] [--steps K] [--warmup W] [--gpus N] [--impl kvc|reference]
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the path
+has no exchange step); the job value is all ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV encode/decode GB/s (input bytes) on 1 GB300 and % of HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha() -> str:
+    csrc = os.path.join(ROOT, "kv_cache_compression_encode_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(workload, {}).get(kernel)
+    if not rec or rec.get("source_sha") != source_sha():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kvc_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------- workload
+def workload_setup(name: str, device):
+    import torch
+
+    from kv_cache_compression_encode_gb300 import kvc, synth
+    from kv_cache_compression_encode_gb300.workloads import PROFILES, WORKLOADS
+
+    w = WORKLOADS[name]
+    prof = PROFILES[name]
+    k, v = [], []
+    for l in range(w.layers):
+        a, b = synth.layer_kv(w.dist, l, w.tokens, w.kv_heads, w.head_dim, w.dtype, w.seed, device)
+        k.append(a.contiguous())
+        v.append(b.contiguous())
+    torch.cuda.synchronize(device)
+    shape = kvc.make_shape(w.layers, w.tokens, w.kv_heads, w.head_dim, kvc.BF16 if w.dtype == "bf16" else kvc.F16)
+    return w, prof, shape, k, v
+
+
+def kernel_bytes(plan, w, name: str, stream_bytes: int) -> int:
+    """Algorithmic bytes one launch of `name` must move (read + write)."""
+    raw_tensor = w.layers * w.tokens * w.kv_heads * w.head_dim * 2
+    sec = [plan.section(i)[1] for i in range(6)]
+    k_out = sec[0] + sec[1] + sec[4] + sec[5]
+    v_out = sec[2] + sec[3]
+    Q = plan.payload_bytes
+    table = 4 * plan.n_chunks
+    return {
+        "kvc_enc_tile": raw_tensor + k_out,
+        "kvc_enc_rows": raw_tensor + v_out,
+        "kvc_dec_tile": raw_tensor + k_out,
+        "kvc_dec_rows": raw_tensor + v_out,
+        "kvc_lossless_enc": Q + stream_bytes,
+        "kvc_lossless_dec": stream_bytes + Q,
+        "kvc_decode_prepare": table + 8 * plan.n_chunks,
+        "kvc_prologue": 64 + 8 * plan.n_chunks,
+    }.get(name, 0)
+
+
+def run_kvc(args):
+    import torch
+    import torch.distributed as dist
+
+    from kv_cache_compression_encode_gb300 import kvc
+    from kv_cache_compression_encode_gb300.codec import Codec
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    w, prof, shape, k, v = workload_setup(args.workload, device)
+    raw = w.raw_bytes
+    codec = Codec(kvc.make_profile(**prof), shape, device)
+    stream_buf = codec.new_stream_buffer()
+    ok = [torch.empty_like(x) for x in k]
+    ov = [torch.empty_like(x) for x in v]
+    cs = torch.cuda.current_stream(device)
+
+    def step():
+        codec.encode(k, v, out=stream_buf)
+        # the decode consumes the bytes the encode produced; its size is the
+        # worst-case bound here (the stream is self-delimiting), so no host sync
+        codec.decode(stream_buf, codec.plan.max_stream_bytes, ok, ov)
+
+    # correctness of the timed configuration: one round trip, checked on the device
+    codec.encode(k, v, out=stream_buf)
+    st, nbytes, flags = codec.query()
+    if st != kvc.KVC_OK:
+        raise RuntimeError(f"encode failed: {kvc.status_str(st)} flags={flags}")
+    codec.decode(stream_buf, nbytes, ok, ov)
+    st, _, flags = codec.query()
+    if st != kvc.KVC_OK:
+        raise RuntimeError(f"decode failed: {kvc.status_str(st)} flags={flags}")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+
+    # encode-only and decode-only timings (untimed by the contract; reported apart)
+    def time_loop(fn, n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cs)
+        for _ in range(n):
+            fn()
+        b.record(cs)
+        b.synchronize()
+        return a.elapsed_time(b) / n
+
+    n_side = max(3, min(50, args.steps // 10))
+    enc_ms = time_loop(lambda: codec.encode(k, v, out=stream_buf), n_side)
+    dec_ms = time_loop(lambda: codec.decode(stream_buf, nbytes, ok, ov), n_side)
+
+    # ---- timed region
+    launches0 = codec.plan.launches
+    kvc.kvc_timing_enable(codec.plan, True, capacity=args.steps * 8 + 64)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(cs)
+        for _ in range(args.steps):
+            step()
+        ev1.record(cs)
+        ev1.synchronize()
+    torch.cuda.synchronize(device)
+    if world > 1:
+        dist.barrier()
+    total_ms = ev0.elapsed_time(ev1)
+    launches = codec.plan.launches - launches0
+    recs = kvc.kvc_timing_read(codec.plan, args.steps * 8 + 64)
+    kvc.kvc_timing_enable(codec.plan, False)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    st, _, flags = codec.query()
+    if st != kvc.KVC_OK:
+        raise RuntimeError(f"timed steps reported {kvc.status_str(st)} flags={flags}")
+
+    if rank == 0:
+        ms_step = total_ms / args.steps
+        value = raw * world * args.steps / (total_ms * 1e-3) / 1e9
+        # per-kernel live timings
+        per = {}
+        for name, ms in recs:
+            d = per.setdefault(name, [0.0, 0])
+            d[0] += ms
+            d[1] += 1
+        step_kernel_ms = sum(d[0] for d in per.values())
+        kernels = {}
+        for name, (ms_sum, n) in sorted(per.items(), key=lambda kv: -kv[1][0]):
+            avg = ms_sum / n
+            b = kernel_bytes(codec.plan, w, name, nbytes)
+            kernels[name] = {"launches": n, "avg_ms": round(avg, 5), "share": round(ms_sum / step_kernel_ms, 4),
+                             "alg_bytes": b, "gbs": round(b / (avg * 1e-3) / 1e9, 1) if avg > 0 else None}
+        top = max(per.items(), key=lambda kv: kv[1][0])[0]
+        peak, peak_src = peaks()
+        top_avg = per[top][0] / per[top][1]
+        achieved = kernel_bytes(codec.plan, w, top, nbytes) / (top_avg * 1e-3) / 1e9
+        e2e = run_e2e(codec, k, v, ok, ov, w, args, device) if args.e2e else None
+        cpu = cpu_baseline(w, prof, args) if not args.no_cpu_baseline else None
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "layers": w.layers, "tokens": w.tokens, "kv_heads": w.kv_heads,
+                       "head_dim": w.head_dim, "elt": w.dtype, "distribution": w.dist,
+                       "profile": {k_: (list(map(list, v_)) if k_ == "stages" else v_) for k_, v_ in prof.items()},
+                       "raw_bytes": raw, "stream_bytes": nbytes, "compression_ratio": round(raw / nbytes, 4),
+                       "step": "kvc_encode + kvc_decode", "l2": "inputs larger than L2 (no flush needed)",
+                       "parallelism": f"replicas x{world}"},
+            "encode_gbs": round(raw / (enc_ms * 1e-3) / 1e9, 2), "decode_gbs": round(raw / (dec_ms * 1e-3) / 1e9, 2),
+            "roofline": {"bound": "hbm", "kernel": top, "achieved": round(achieved, 1), "peak": peak,
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                         else "fallback", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": ncu_traffic(top, w.name)},
+            "kernels": kernels,
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": launches,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(codec, k, v, ok, ov, w, args, device):
+    """Same metric through the public API with host buffers: every step copies the
+    KV from pinned host memory, encodes, reads the size and the stream back, then
+    copies the stream in, decodes and copies the KV out."""
+    import torch
+
+    hk = [x.cpu().pin_memory() for x in k]
+    hv = [x.cpu().pin_memory() for x in v]
+    rk = [torch.empty_like(x, device="cpu").pin_memory() for x in k]
+    rv = [torch.empty_like(x, device="cpu").pin_memory() for x in v]
+    hs = torch.empty(codec.plan.max_stream_bytes, dtype=torch.uint8).pin_memory()
+    dk = [torch.empty_like(x) for x in k]
+    dv = [torch.empty_like(x) for x in v]
+    sbuf = codec.new_stream_buffer()
+    rbuf = codec.new_stream_buffer()
+    counts = {"h2d": 0, "d2h": 0}
+
+    def step():
+        for d, h in zip(dk + dv, hk + hv):
+            d.copy_(h, non_blocking=True)
+        codec.encode(dk, dv, out=sbuf)
+        _, n, _ = codec.query()                     # size scalar to the host (syncs)
+        hs[:n].copy_(sbuf[:n], non_blocking=True)
+        rbuf[:n].copy_(hs[:n], non_blocking=True)   # the receiving side's upload
+        codec.decode(rbuf, n, dk, dv)
+        for h, d in zip(rk + rv, dk + dv):
+            h.copy_(d, non_blocking=True)
+        torch.cuda.current_stream(device).synchronize()
+        counts["h2d"] = w.raw_bytes + n
+        counts["d2h"] = n + w.raw_bytes + 16
+        return n
+
+    for _ in range(2):
+        step()
+    n_steps = max(3, min(20, args.steps // 100))
+    t0 = time.perf_counter()
+    for _ in range(n_steps):
+        step()
+    dt = (time.perf_counter() - t0) / n_steps
+    ok_rt = all(torch.equal(a, b.to(a.device)) for a, b in zip(ok + ov, rk + rv))
+    return {"value": round(w.raw_bytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": counts["h2d"],
+            "d2h_bytes_per_step": counts["d2h"], "ms_per_step": round(dt * 1e3, 3), "steps": n_steps,
+            "roundtrip_matches_device_path": bool(ok_rt)}
+
+
+# ---------------------------------------------------------------------------- oracle
+def oracle_sample(w, prof, layers: int, device=None):
+    """Host bits of the first `layers` layers of the workload (same generator as the GPU run)."""
+    from kv_cache_compression_encode_gb300 import synth
+
+    hk, hv = [], []
+    for l in range(layers):
+        a, b = synth.layer_kv(w.dist, l, w.tokens, w.kv_heads, w.head_dim, w.dtype, w.seed,
+                              device if device is not None else "cpu")
+        hk.append(synth.to_bits_numpy(a))
+        hv.append(synth.to_bits_numpy(b))
+    return hk, hv
+
+
+def time_oracle_step(w, prof, hk, hv, layers):
+    from oracle import oracle as O
+
+    shape = O.make_shape(layers, w.tokens, w.kv_heads, w.head_dim, 2 if w.dtype == "bf16" else 1)
+    oprof = O.make_profile(**prof)
+    t0 = time.perf_counter()
+    s, _ = O.encode(oprof, shape, hk, hv)
+    rk = [np.empty_like(a) for a in hk]
+    rv = [np.empty_like(a) for a in hv]
+    O.decode(oprof, shape, s, rk, rv)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, prof, args):
+    from oracle import oracle as O
+
+    cores = len(os.sched_getaffinity(0))
+    O.set_threads(cores)
+    layers = max(1, min(w.layers, args.oracle_layers))
+    hk, hv = oracle_sample(w, prof, layers, device="cuda" if not args.cpu_inputs else "cpu")
+    dt = time_oracle_step(w, prof, hk, hv, layers)
+    sample_bytes = 2 * layers * w.tokens * w.kv_heads * w.head_dim * 2
+    return {"value": round(sample_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{layers} of {w.layers} layers of {w.name} ({sample_bytes} raw bytes), encode+decode, "
+                      f"{dt:.2f} s"}
+
+
+def run_reference(args):
+    """The reference arm for this build is the oracle itself, on the host cores."""
+    from kv_cache_compression_encode_gb300.workloads import PROFILES, WORKLOADS
+    from oracle import oracle as O
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    prof = PROFILES[args.workload]
+    cores = len(os.sched_getaffinity(0))
+    O.set_threads(cores)
+    layers = max(1, min(w.layers, args.oracle_layers))
+    hk, hv = oracle_sample(w, prof, layers, device="cpu")
+    for _ in range(min(args.warmup, 1)):
+        time_oracle_step(w, prof, hk, hv, layers)
+    steps = max(1, min(args.steps, args.reference_steps))
+    dts = [time_oracle_step(w, prof, hk, hv, layers) for _ in range(steps)]
+    sample_bytes = 2 * layers * w.tokens * w.kv_heads * w.head_dim * 2
+    dt = float(np.mean(dts))
+    value = sample_bytes / dt / 1e9
+    sample = f"{layers} of {w.layers} layers of {w.name} ({sample_bytes} raw bytes) per step, encode+decode"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "layers": w.layers, "tokens": w.tokens, "kv_heads": w.kv_heads,
+                   "head_dim": w.head_dim, "elt": w.dtype, "sample_layers": layers},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--impl", default="kvc", choices=["kvc", "reference"])
+    ap.add_argument("--oracle-layers", type=int, default=4)
+    ap.add_argument("--reference-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-inputs", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_kvc(args)
+
+
+if __name__ == "__main__":
+    main()

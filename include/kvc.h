@@ -1,0 +1,213 @@
+/*
+ * kvc.h -- C ABI of the GB300 KV-cache compression data path.
+ *
+ * The path (encode): per-channel key smoothing -> optional randomized Hadamard
+ * rotation along head_dim -> group-wise asymmetric min-max quantization (2/3/4/8
+ * bit codes, fp16 scale and zero) -> bit-packing into one all-layer payload ->
+ * chunked lossless stage pipeline (tuple shuffle, bit shuffle, delta, zero-word
+ * elimination).  Decode is the exact inverse.  Sources:
+ *   "KVServe: Service-Aware KV Cache Compression for Communication-Efficient
+ *    Disaggregated LLM Serving", §5.1 (pipeline BS = C(Q(T(X))): transformer,
+ *    quantizer, codec; layer-/head-wise precision), §7.3 (KIVI metadata);
+ *   "Beyond Compression Ratio: High-Throughput KV Compression for Disaggregated
+ *    LLM Serving", §4.1 (fused transform + quantization writing a preallocated
+ *    all-layer buffer; fused reconstruction) and §4.2 (LC-style lossless backend
+ *    TUPL8_1 -> BIT_8 -> RZE_2 with device-pointer encode/decode APIs, persistent
+ *    scratch and a compressed-size scalar returned to the host).
+ *
+ * Conventions
+ *  - Every pointer named d_* or documented as "device" is CUDA device memory of
+ *    the current device; host pointers are documented as such.  The caller owns
+ *    every buffer (inputs, outputs, stream, workspace).  A plan owns host memory
+ *    only and never allocates device memory; encode/decode allocate nothing.
+ *  - Work is enqueued asynchronously on the caller's CUDA stream.  Argument and
+ *    profile errors are returned synchronously; errors found by the GPU (corrupt
+ *    stream, non-finite input, fp16 metadata overflow, look-back timeout) set bits
+ *    of a status word in the workspace, which kvc_query() reads after a sync.
+ *  - Device buffers must be 16-byte aligned; token and page strides multiples of 16.
+ *  - A plan is not thread-safe; use one plan per concurrently-issuing host thread.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-identical to cudaStream_t (NULL = the legacy default stream). */
+typedef struct CUstream_st *kvc_stream_t;
+
+typedef enum kvc_status {
+    KVC_OK = 0,
+    KVC_ERR_INVALID_ARG = 1, /* null pointer, bad shape, misaligned buffer, bad block-table entry */
+    KVC_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head_dim != 128) */
+    KVC_ERR_CAPACITY = 3,    /* output or workspace smaller than required */
+    KVC_ERR_CORRUPT = 4,     /* stream header / chunk table / chunk payload inconsistent */
+    KVC_ERR_RANGE = 5,       /* an fp16 zero, scale or smoothing centre overflowed (saturated) */
+    KVC_ERR_NONFINITE = 6,   /* NaN or Inf in the encode input (output bytes unspecified) */
+    KVC_ERR_TIMEOUT = 7,     /* a bounded device wait gave up (chunk offset look-back) */
+    KVC_ERR_CUDA = 8         /* a CUDA runtime call failed */
+} kvc_status;
+
+/* Bits of the device status word (kvc_query's host_flags). */
+#define KVC_FLAG_RANGE 1u
+#define KVC_FLAG_NONFINITE 2u
+#define KVC_FLAG_CORRUPT 4u
+#define KVC_FLAG_CAPACITY 8u
+#define KVC_FLAG_TIMEOUT 16u
+#define KVC_FLAG_BAD_PAGE 32u
+
+enum { KVC_F16 = 1, KVC_BF16 = 2 };
+/* Quantization axis ("Beyond Compression Ratio" §4.1: channel-wise keys, token-wise values). */
+enum { KVC_AXIS_OVER_TOKENS = 0, KVC_AXIS_OVER_CHANNELS = 1 };
+/* Lossless stage kinds ("Beyond Compression Ratio" §4.2). */
+enum { KVC_ST_TUPL = 1, KVC_ST_BIT = 2, KVC_ST_DELTA = 3, KVC_ST_RZE = 4 };
+
+#define KVC_MAX_STAGES 4
+#define KVC_MAX_LAYERS 256
+#define KVC_HEADER_BYTES 64
+
+/* One lossless stage: TUPL param k in {2,4,8} (k-byte tuples -> k byte columns);
+ * BIT param 8 (bit planes of bytes); DELTA param w in {1,2,4} (w-byte words,
+ * differences mod 2^(8w)); RZE param w in {1,2,4} (zero-word elimination with a
+ * two-level bitmap; only as the last stage). */
+typedef struct kvc_stage {
+    uint8_t kind;
+    uint8_t param;
+} kvc_stage;
+
+/* A compression profile, chosen per request and fixed for it ("KVServe" §3.1). */
+typedef struct kvc_profile {
+    uint32_t struct_size;   /* = sizeof(kvc_profile) */
+    uint8_t smooth_keys;    /* per-channel key smoothing (128-token blocks) */
+    uint8_t hadamard;       /* randomized Hadamard rotation along head_dim (K and V) */
+    uint8_t bits_k, bits_v; /* code width: 2, 3, 4 or 8 */
+    uint16_t group_k, group_v; /* group size: 32, 64 or 128 */
+    uint8_t axis_k, axis_v;    /* KVC_AXIS_*; defaults OVER_TOKENS for K, OVER_CHANNELS for V */
+    uint8_t n_stages;          /* 0 = no lossless stage (the stream carries the payload as is) */
+    uint8_t reserved0;
+    kvc_stage stages[KVC_MAX_STAGES];
+    uint32_t chunk_bytes;      /* lossless chunk size: multiple of 256 in [256, 65536] */
+    uint32_t reserved1;
+    uint64_t hadamard_seed;    /* seed of the +-1 sign vector (SplitMix64) */
+} kvc_profile;
+
+/* KV tensor geometry.  Each layer's K (and V) is addressed as rows of
+ * kv_heads*head_dim elements: token t lives at
+ *     base + t*token_stride                                   (no block table)
+ *     base + block_table[t/page_size]*page_stride + (t%page_size)*token_stride
+ * and head h of that row at + h*head_dim*element_size. */
+typedef struct kvc_shape {
+    uint32_t struct_size;  /* = sizeof(kvc_shape) */
+    uint32_t layers;       /* 0 .. KVC_MAX_LAYERS */
+    uint32_t tokens;       /* 0 .. 2^31-1 */
+    uint32_t kv_heads;     /* >= 1 */
+    uint32_t head_dim;     /* 128 */
+    uint32_t dtype;        /* KVC_F16 or KVC_BF16 */
+    uint32_t page_size;    /* tokens per page, power of two (block table only) */
+    uint32_t num_pages;    /* physical pages per layer buffer (block table only; bounds check) */
+    uint64_t token_stride; /* bytes between token rows; 0 = kv_heads*head_dim*element_size */
+    uint64_t page_stride;  /* bytes between physical pages (block table only) */
+} kvc_shape;
+
+/* Where the KV of every layer lives (encode input / decode output). */
+typedef struct kvc_kv {
+    void *const *k_layers;      /* HOST array of `layers` DEVICE pointers to K */
+    void *const *v_layers;      /* HOST array of `layers` DEVICE pointers to V */
+    const int32_t *block_table; /* DEVICE array of ceil(tokens/page_size) physical page
+                                   ids shared by all layers; NULL = contiguous layout */
+} kvc_kv;
+
+typedef struct kvc_plan_s kvc_plan_t;
+
+/* Validate a profile and shape and precompute the payload layout, stream bounds
+ * and the Hadamard sign vector ("Beyond Compression Ratio" §4.1: signs and
+ * workspaces cached and reused across layers and requests).  Host-only object.
+ * Returns KVC_ERR_INVALID_ARG / KVC_ERR_UNSUPPORTED without creating a plan. */
+kvc_status kvc_plan(const kvc_profile *profile, const kvc_shape *shape, kvc_plan_t **out);
+void kvc_plan_destroy(kvc_plan_t *plan);
+
+/* Bytes of the caller-provided device workspace encode/decode need ("persistent
+ * runtime scratch", "Beyond Compression Ratio" §4.2): a 256-byte control block
+ * (status word, stream size, chunk ticket), per-chunk look-back / offset words and,
+ * when lossless stages are on, the quantized payload. */
+size_t kvc_workspace_bytes(const kvc_plan_t *plan);
+/* Worst-case stream size (header + chunk table + every chunk stored raw). */
+size_t kvc_max_stream_bytes(const kvc_plan_t *plan);
+/* Bytes of the quantized payload Q (all sections, each 16-byte aligned). */
+size_t kvc_payload_bytes(const kvc_plan_t *plan);
+/* Offset and size of payload section i: 0 K codes, 1 K scale/zero, 2 V codes,
+ * 3 V scale/zero, 4 K smoothing centres (fp16), 5 K smoothing exponents (int8). */
+kvc_status kvc_section(const kvc_plan_t *plan, int index, uint64_t *offset, uint64_t *size);
+/* Number of lossless chunks (0 without stages). */
+uint64_t kvc_num_chunks(const kvc_plan_t *plan);
+
+/* Full encode: quantize all layers into the payload, then header + lossless
+ * stream into d_stream (capacity stream_cap >= kvc_max_stream_bytes).  The stream
+ * size is written to the device word *d_stream_bytes (may be NULL) and to the
+ * workspace control block; kvc_query() returns it to the host.  No host sync. */
+kvc_status kvc_encode(kvc_plan_t *plan, const kvc_kv *in, void *d_stream, size_t stream_cap,
+                      void *d_workspace, size_t workspace_bytes, uint64_t *d_stream_bytes,
+                      kvc_stream_t stream);
+
+/* Full decode of a stream of stream_bytes bytes into the layers of *out (same
+ * geometry as the plan).  The header is checked against the plan on the device;
+ * a corrupt stream sets KVC_FLAG_CORRUPT and leaves *out untouched. */
+kvc_status kvc_decode(kvc_plan_t *plan, const void *d_stream, size_t stream_bytes, const kvc_kv *out,
+                      void *d_workspace, size_t workspace_bytes, kvc_stream_t stream);
+
+/* The four steps of the path, one call each (encode = quantize + lossless_encode,
+ * decode = lossless_decode + dequantize).  d_payload holds kvc_payload_bytes. */
+/* Smoothing, Hadamard, group statistics, quantization and packing (fused). */
+kvc_status kvc_quantize(kvc_plan_t *plan, const kvc_kv *in, void *d_payload, void *d_workspace,
+                        size_t workspace_bytes, kvc_stream_t stream);
+/* Header + chunk table + lossless chunks of a payload; stream size to *d_stream_bytes. */
+kvc_status kvc_lossless_encode(kvc_plan_t *plan, const void *d_payload, void *d_stream, size_t stream_cap,
+                               void *d_workspace, size_t workspace_bytes, uint64_t *d_stream_bytes,
+                               kvc_stream_t stream);
+/* Validate a stream and restore its payload. */
+kvc_status kvc_lossless_decode(kvc_plan_t *plan, const void *d_stream, size_t stream_bytes, void *d_payload,
+                               void *d_workspace, size_t workspace_bytes, kvc_stream_t stream);
+/* Dequantization, inverse Hadamard, normalization, sign restoration, unsmoothing
+ * and conversion to the element type (fused); skipped when the status word
+ * already carries KVC_FLAG_CORRUPT. */
+kvc_status kvc_dequantize(kvc_plan_t *plan, const void *d_payload, const kvc_kv *out, void *d_workspace,
+                          size_t workspace_bytes, kvc_stream_t stream);
+
+/* Synchronize `stream`, then read the workspace control block: the stream size of
+ * the last encode (host_stream_bytes, may be NULL) and the status bits
+ * (host_flags, may be NULL).  Returns the most severe error the bits encode
+ * (CORRUPT > CAPACITY > TIMEOUT > INVALID_ARG (bad page) > NONFINITE > RANGE) or KVC_OK. */
+kvc_status kvc_query(const void *d_workspace, kvc_stream_t stream, uint64_t *host_stream_bytes,
+                     uint32_t *host_flags);
+
+const char *kvc_status_str(kvc_status status);
+
+/* ---- measurement hooks ---------------------------------------------------- */
+/* Number of kernel launches this plan has enqueued so far. */
+uint64_t kvc_launch_count(const kvc_plan_t *plan);
+/* enable != 0: bracket every kernel launch with CUDA events (up to `capacity`
+ * launches are kept); enable == 0 stops.  Returns KVC_ERR_CUDA if events fail. */
+kvc_status kvc_timing_enable(kvc_plan_t *plan, int enable, int capacity);
+/* After a sync: copy up to `max` records (kernel name, milliseconds) of the
+ * launches recorded since kvc_timing_enable and return how many were written. */
+typedef struct kvc_timing {
+    const char *kernel;
+    float ms;
+} kvc_timing;
+int kvc_timing_read(kvc_plan_t *plan, kvc_timing *out, int max);
+
+/* ---- test hooks -------------------------------------------------------------- */
+/* Fault injection on the host side of the look-back scan: the chunk with ticket
+ * `ticket` (>= 0) does not publish its size, so its successor's bounded wait runs
+ * out after `poll_limit` polls and sets KVC_FLAG_TIMEOUT.  ticket < 0 disables it;
+ * poll_limit = 0 restores the default limit. */
+kvc_status kvc_debug_lookback(kvc_plan_t *plan, int64_t ticket, uint32_t poll_limit);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVC_H */

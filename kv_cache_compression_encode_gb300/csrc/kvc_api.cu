@@ -1,0 +1,581 @@
+// kvc_api.cu -- the C ABI (include/kvc.h): plans, payload layout, launches.
+//
+// Payload layout (the "preallocated all-layer output buffer" of "Beyond
+// Compression Ratio: High-Throughput KV Compression for Disaggregated LLM
+// Serving", §4.1), sections in this order, each starting 16-byte aligned:
+//   0 K codes, 1 K {scale, zero}, 2 V codes, 3 V {scale, zero},
+//   4 K smoothing centres (fp16), 5 K smoothing exponents (int8).
+// Groups over tokens: records [layer][head][token group][channel]; groups over
+// channels: records [layer][token][head][channel group]; smoothing cells
+// [layer][head][128-token block][channel].  A record holds G codes of b bits,
+// least significant bit first.
+#include <cuda_runtime.h>
+
+#include <new>
+#include <stdlib.h>
+#include <string.h>
+#include <vector>
+
+#include "kvc_internal.h"
+
+using namespace kvc;
+
+struct TimingRec {
+  const char *name;
+  cudaEvent_t start, stop;
+};
+
+struct kvc_plan_s {
+  kvc_profile prof;
+  kvc_shape shape;
+  uint64_t off[6], size[6];
+  uint64_t payload_bytes, n_chunks, data_start, max_stream_bytes, workspace_bytes;
+  uint64_t n_tg_k, n_tg_v, n_sb;
+  uint32_t sign[4];
+  uint8_t header[KVC_HEADER_BYTES];
+  int sm_count;
+  uint64_t launches;
+  // timing
+  bool timing;
+  int timing_cap;
+  std::vector<TimingRec> recs;
+  std::vector<cudaEvent_t> pool;
+  // test hooks
+  int64_t skip_ticket;
+  uint32_t poll_limit;
+};
+
+static constexpr uint32_t kDefaultPollLimit = 1u << 22;
+
+static uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+static uint64_t align_up(uint64_t a, uint64_t b) { return (a + b - 1) / b * b; }
+
+// SplitMix64 (S. Vigna), the published 64-bit mixing generator.
+static uint64_t splitmix64(uint64_t &state) {
+  uint64_t z = (state += 0x9E3779B97F4A7C15ull);
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+static bool valid_bits(uint32_t b) { return b == 2 || b == 3 || b == 4 || b == 8; }
+static bool valid_group(uint32_t g) { return g == 32 || g == 64 || g == 128; }
+
+static kvc_status check_profile(const kvc_profile *p) {
+  if (p->struct_size != sizeof(kvc_profile)) return KVC_ERR_INVALID_ARG;
+  if (!valid_bits(p->bits_k) || !valid_bits(p->bits_v)) return KVC_ERR_INVALID_ARG;
+  if (!valid_group(p->group_k) || !valid_group(p->group_v)) return KVC_ERR_INVALID_ARG;
+  if (p->axis_k > 1 || p->axis_v > 1) return KVC_ERR_INVALID_ARG;
+  if (p->smooth_keys > 1 || p->hadamard > 1) return KVC_ERR_INVALID_ARG;
+  if (p->n_stages > KVC_MAX_STAGES) return KVC_ERR_INVALID_ARG;
+  for (uint32_t s = 0; s < p->n_stages; s++) {
+    const uint32_t k = p->stages[s].kind, prm = p->stages[s].param;
+    bool ok = false;
+    if (k == KVC_ST_TUPL) ok = prm == 2 || prm == 4 || prm == 8;
+    else if (k == KVC_ST_BIT) ok = prm == 8;
+    else if (k == KVC_ST_DELTA) ok = prm == 1 || prm == 2 || prm == 4;
+    else if (k == KVC_ST_RZE) ok = (prm == 1 || prm == 2 || prm == 4) && s + 1 == p->n_stages;
+    if (!ok) return KVC_ERR_INVALID_ARG;
+  }
+  if (p->n_stages && (p->chunk_bytes < 256 || p->chunk_bytes > 65536 || p->chunk_bytes % 256))
+    return KVC_ERR_INVALID_ARG;
+  return KVC_OK;
+}
+
+static uint64_t groups(const kvc_shape &s, uint32_t axis, uint32_t G) {
+  const uint64_t L = s.layers, T = s.tokens, H = s.kv_heads, D = s.head_dim;
+  return axis == KVC_AXIS_OVER_TOKENS ? L * H * ceil_div(T, G) * D : L * T * H * (D / G);
+}
+
+static void put16(uint8_t *p, uint32_t v) { p[0] = (uint8_t)v; p[1] = (uint8_t)(v >> 8); }
+static void put32(uint8_t *p, uint32_t v) { for (int i = 0; i < 4; i++) p[i] = (uint8_t)(v >> (8 * i)); }
+static void put64(uint8_t *p, uint64_t v) { for (int i = 0; i < 8; i++) p[i] = (uint8_t)(v >> (8 * i)); }
+
+// Stream header, 64 bytes little-endian: magic "KVC1", version 1, header size,
+// geometry, profile, chunking, seed and payload size.
+static void build_header(kvc_plan_s *P) {
+  uint8_t *h = P->header;
+  memset(h, 0, KVC_HEADER_BYTES);
+  h[0] = 'K'; h[1] = 'V'; h[2] = 'C'; h[3] = '1';
+  put16(h + 4, 1);
+  put16(h + 6, KVC_HEADER_BYTES);
+  put32(h + 8, P->shape.layers);
+  put32(h + 12, P->shape.tokens);
+  put16(h + 16, P->shape.kv_heads);
+  put16(h + 18, P->shape.head_dim);
+  h[20] = (uint8_t)P->shape.dtype;
+  h[21] = (uint8_t)((P->prof.smooth_keys ? 1 : 0) | (P->prof.hadamard ? 2 : 0));
+  h[22] = P->prof.bits_k;
+  h[23] = P->prof.bits_v;
+  put16(h + 24, P->prof.group_k);
+  put16(h + 26, P->prof.group_v);
+  h[28] = P->prof.axis_k;
+  h[29] = P->prof.axis_v;
+  h[30] = P->prof.n_stages;
+  for (uint32_t s = 0; s < P->prof.n_stages; s++) {
+    h[32 + 2 * s] = P->prof.stages[s].kind;
+    h[33 + 2 * s] = P->prof.stages[s].param;
+  }
+  put32(h + 40, P->prof.n_stages ? P->prof.chunk_bytes : 0);
+  put32(h + 44, (uint32_t)P->n_chunks);
+  put64(h + 48, P->prof.hadamard_seed);
+  put64(h + 56, P->payload_bytes);
+}
+
+extern "C" kvc_status kvc_plan(const kvc_profile *profile, const kvc_shape *shape, kvc_plan_t **out) {
+  if (!profile || !shape || !out) return KVC_ERR_INVALID_ARG;
+  *out = nullptr;
+  kvc_status st = check_profile(profile);
+  if (st != KVC_OK) return st;
+  kvc_shape s = *shape;
+  if (s.struct_size != sizeof(kvc_shape)) return KVC_ERR_INVALID_ARG;
+  if (s.dtype != KVC_F16 && s.dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
+  if (s.head_dim != (uint32_t)kHeadDim) return KVC_ERR_UNSUPPORTED;
+  if (s.kv_heads < 1 || s.kv_heads > 65535 || s.layers > KVC_MAX_LAYERS || s.tokens > 0x7fffffffu)
+    return KVC_ERR_INVALID_ARG;
+  if ((uint64_t)s.layers * s.tokens * s.kv_heads >= (1ull << 31)) return KVC_ERR_UNSUPPORTED;
+  const uint64_t row_bytes = (uint64_t)s.kv_heads * s.head_dim * 2;
+  if (s.token_stride == 0) s.token_stride = row_bytes;
+  if (s.token_stride < row_bytes || s.token_stride % 16) return KVC_ERR_INVALID_ARG;
+  if (s.page_size) {
+    if (s.page_size & (s.page_size - 1)) return KVC_ERR_INVALID_ARG;
+    if (s.page_stride % 16 || s.num_pages == 0) return KVC_ERR_INVALID_ARG;
+    if (s.page_stride < (uint64_t)s.page_size * s.token_stride) return KVC_ERR_INVALID_ARG;
+  }
+
+  kvc_plan_s *P = new (std::nothrow) kvc_plan_s();
+  if (!P) return KVC_ERR_INVALID_ARG;
+  P->prof = *profile;
+  P->shape = s;
+  const uint64_t gk = groups(s, profile->axis_k, profile->group_k), gv = groups(s, profile->axis_v, profile->group_v);
+  const uint64_t nsb = (uint64_t)s.layers * s.kv_heads * ceil_div(s.tokens, kSmoothBlock) * s.head_dim;
+  P->size[0] = gk * profile->group_k * profile->bits_k / 8;
+  P->size[1] = gk * 4;
+  P->size[2] = gv * profile->group_v * profile->bits_v / 8;
+  P->size[3] = gv * 4;
+  P->size[4] = profile->smooth_keys ? nsb * 2 : 0;
+  P->size[5] = profile->smooth_keys ? nsb : 0;
+  uint64_t o = 0;
+  for (int i = 0; i < 6; i++) {
+    P->off[i] = o;
+    o += align_up(P->size[i], 16);
+  }
+  P->payload_bytes = o;
+  if (profile->n_stages) {
+    P->n_chunks = ceil_div(o, profile->chunk_bytes);
+    if (P->n_chunks >= (1ull << 31)) {
+      delete P;
+      return KVC_ERR_UNSUPPORTED;
+    }
+    P->data_start = align_up(KVC_HEADER_BYTES + 4 * P->n_chunks, 16);
+  } else {
+    P->n_chunks = 0;
+    P->data_start = KVC_HEADER_BYTES;
+  }
+  P->max_stream_bytes = P->data_start + o;
+  P->workspace_bytes = kCtrlBytes + align_up(8 * P->n_chunks, 256) + (profile->n_stages ? o : 0);
+  P->n_tg_k = ceil_div(s.tokens, profile->group_k);
+  P->n_tg_v = ceil_div(s.tokens, profile->group_v);
+  P->n_sb = ceil_div(s.tokens, kSmoothBlock);
+  if (profile->hadamard) {
+    uint64_t state = profile->hadamard_seed;
+    for (int j = 0; j < kHeadDim; j++)
+      if (splitmix64(state) >> 63) P->sign[j >> 5] |= 1u << (j & 31);
+  }
+  build_header(P);
+  int dev = 0;
+  P->sm_count = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&P->sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (P->sm_count <= 0) P->sm_count = 1;
+  P->skip_ticket = -1;
+  P->poll_limit = kDefaultPollLimit;
+  *out = P;
+  return KVC_OK;
+}
+
+static void timing_clear(kvc_plan_s *P) {
+  for (auto &r : P->recs) {
+    P->pool.push_back(r.start);
+    P->pool.push_back(r.stop);
+  }
+  P->recs.clear();
+}
+
+extern "C" void kvc_plan_destroy(kvc_plan_t *plan) {
+  if (!plan) return;
+  timing_clear(plan);
+  for (cudaEvent_t e : plan->pool) cudaEventDestroy(e);
+  delete plan;
+}
+
+extern "C" size_t kvc_workspace_bytes(const kvc_plan_t *p) { return p ? (size_t)p->workspace_bytes : 0; }
+extern "C" size_t kvc_max_stream_bytes(const kvc_plan_t *p) { return p ? (size_t)p->max_stream_bytes : 0; }
+extern "C" size_t kvc_payload_bytes(const kvc_plan_t *p) { return p ? (size_t)p->payload_bytes : 0; }
+extern "C" uint64_t kvc_num_chunks(const kvc_plan_t *p) { return p ? p->n_chunks : 0; }
+extern "C" uint64_t kvc_launch_count(const kvc_plan_t *p) { return p ? p->launches : 0; }
+
+extern "C" kvc_status kvc_section(const kvc_plan_t *p, int index, uint64_t *offset, uint64_t *size) {
+  if (!p || index < 0 || index > 5) return KVC_ERR_INVALID_ARG;
+  if (offset) *offset = p->off[index];
+  if (size) *size = p->size[index];
+  return KVC_OK;
+}
+
+// ---------------------------------------------------------------------------
+// launch bracketing for kvc_timing_*
+// ---------------------------------------------------------------------------
+static cudaEvent_t take_event(kvc_plan_s *P) {
+  if (!P->pool.empty()) {
+    cudaEvent_t e = P->pool.back();
+    P->pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+struct Bracket {
+  kvc_plan_s *P;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr, b = nullptr;
+  Bracket(kvc_plan_s *p, cudaStream_t s) : P(p), st(s) {
+    if (P->timing && (int)P->recs.size() < P->timing_cap) {
+      a = take_event(P);
+      b = take_event(P);
+      if (a && b) cudaEventRecord(a, st);
+    }
+  }
+  void done(const char *name) {
+    if (a && b) {
+      cudaEventRecord(b, st);
+      P->recs.push_back({name, a, b});
+    }
+  }
+};
+
+static kvc_status cuda_status(int rc) { return rc == 0 ? KVC_OK : KVC_ERR_CUDA; }
+
+extern "C" kvc_status kvc_timing_enable(kvc_plan_t *plan, int enable, int capacity) {
+  if (!plan) return KVC_ERR_INVALID_ARG;
+  timing_clear(plan);
+  plan->timing = enable != 0;
+  plan->timing_cap = capacity > 0 ? capacity : 4096;
+  return KVC_OK;
+}
+
+extern "C" int kvc_timing_read(kvc_plan_t *plan, kvc_timing *out, int max) {
+  if (!plan || !out) return 0;
+  int n = 0;
+  for (auto &r : plan->recs) {
+    if (n >= max) break;
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+      ms = -1.f;
+    out[n].kernel = r.name;
+    out[n].ms = ms;
+    n++;
+  }
+  return n;
+}
+
+extern "C" kvc_status kvc_debug_lookback(kvc_plan_t *plan, int64_t ticket, uint32_t poll_limit) {
+  if (!plan) return KVC_ERR_INVALID_ARG;
+  plan->skip_ticket = ticket < 0 ? -1 : ticket;
+  plan->poll_limit = poll_limit ? poll_limit : kDefaultPollLimit;
+  return KVC_OK;
+}
+
+// ---------------------------------------------------------------------------
+// argument checks shared by the entry points
+// ---------------------------------------------------------------------------
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+static kvc_status check_kv(const kvc_plan_s *P, const kvc_kv *kv) {
+  if (!kv) return KVC_ERR_INVALID_ARG;
+  if (P->shape.layers == 0 || P->shape.tokens == 0) return KVC_OK;
+  if (!kv->k_layers || !kv->v_layers) return KVC_ERR_INVALID_ARG;
+  for (uint32_t l = 0; l < P->shape.layers; l++)
+    if (!kv->k_layers[l] || !kv->v_layers[l] || !aligned16(kv->k_layers[l]) || !aligned16(kv->v_layers[l]))
+      return KVC_ERR_INVALID_ARG;
+  if (kv->block_table && P->shape.page_size == 0) return KVC_ERR_INVALID_ARG;
+  return KVC_OK;
+}
+
+static kvc_status check_ws(const kvc_plan_s *P, const void *ws, size_t bytes) {
+  if (!ws || !aligned16(ws)) return KVC_ERR_INVALID_ARG;
+  if (bytes < P->workspace_bytes) return KVC_ERR_CAPACITY;
+  return KVC_OK;
+}
+
+static uint32_t *ctrl_of(void *ws) { return static_cast<uint32_t *>(ws); }
+static uint64_t *state_of(void *ws) { return reinterpret_cast<uint64_t *>(static_cast<uint8_t *>(ws) + kCtrlBytes); }
+static uint8_t *ws_payload(const kvc_plan_s *P, void *ws) {
+  return static_cast<uint8_t *>(ws) + kCtrlBytes + align_up(8 * P->n_chunks, 256);
+}
+
+static void fill_geom(const kvc_plan_s *P, const kvc_kv *kv, KvGeom &g) {
+  const kvc_shape &s = P->shape;
+  g.L = s.layers;
+  g.T = s.tokens;
+  g.H = s.kv_heads;
+  g.bf16 = s.dtype == KVC_BF16;
+  g.token_stride = s.token_stride;
+  g.page_stride = s.page_stride;
+  g.block_table = kv->block_table;
+  g.page_shift = 0;
+  if (s.page_size)
+    while ((1u << g.page_shift) < s.page_size) g.page_shift++;
+  g.page_mask = s.page_size ? s.page_size - 1 : 0;
+  g.num_pages = s.num_pages;
+  g.pad_ = 0;
+}
+
+// One quantize / dequantize launch per tensor.
+static kvc_status run_quant(kvc_plan_s *P, const kvc_kv *kv, uint8_t *Q, void *ws, bool enc, bool check_corrupt,
+                            cudaStream_t st) {
+  if (P->shape.layers == 0 || P->shape.tokens == 0) return KVC_OK;
+  for (int tensor = 0; tensor < 2; tensor++) {
+    QuantParams q;
+    memset(&q, 0, sizeof q);
+    fill_geom(P, kv, q.g);
+    void *const *src = tensor ? kv->v_layers : kv->k_layers;
+    for (uint32_t l = 0; l < P->shape.layers; l++) q.layers[l] = src[l];
+    q.bits = tensor ? P->prof.bits_v : P->prof.bits_k;
+    q.group = tensor ? P->prof.group_v : P->prof.group_k;
+    q.axis = tensor ? P->prof.axis_v : P->prof.axis_k;
+    q.smooth = tensor == 0 && P->prof.smooth_keys;
+    q.n_tg = (uint32_t)(tensor ? P->n_tg_v : P->n_tg_k);
+    q.n_sb = (uint32_t)P->n_sb;
+    q.hadamard = P->prof.hadamard;
+    memcpy(q.sign, P->sign, sizeof q.sign);
+    q.codes = Q + P->off[tensor ? 2 : 0];
+    q.meta = Q + P->off[tensor ? 3 : 1];
+    q.mu = Q + P->off[4];
+    q.ex = reinterpret_cast<int8_t *>(Q + P->off[5]);
+    q.status = ctrl_of(ws) + kCtrlFlags;
+    q.check_corrupt = check_corrupt;
+    Bracket br(P, st);
+    const char *name = "";
+    const int rc = enc ? launch_quantize(q, P->sm_count, st, &P->launches, &name)
+                       : launch_dequantize(q, P->sm_count, st, &P->launches, &name);
+    br.done(name);
+    if (rc) return KVC_ERR_CUDA;
+  }
+  return KVC_OK;
+}
+
+static kvc_status run_prologue(kvc_plan_s *P, void *ws, bool zero_flags, bool zero_state, uint8_t *stream,
+                               uint64_t *d_stream_bytes, uint8_t *payload, cudaStream_t st) {
+  PrologueParams pp;
+  memset(&pp, 0, sizeof pp);
+  pp.ctrl = ctrl_of(ws);
+  pp.state = state_of(ws);
+  pp.n_state = zero_state ? P->n_chunks : 0;
+  pp.zero_flags = zero_flags;
+  pp.write_header = stream != nullptr;
+  pp.stream = stream;
+  memcpy(pp.header, P->header, KVC_HEADER_BYTES);
+  if (stream) {
+    if (P->prof.n_stages == 0 || P->n_chunks == 0) pp.static_size = P->data_start + (P->prof.n_stages ? 0 : P->payload_bytes);
+    pp.d_stream_bytes = d_stream_bytes;
+    if (P->prof.n_stages) {
+      pp.gap_off = KVC_HEADER_BYTES + 4 * P->n_chunks;
+      pp.gap_len = (uint32_t)(P->data_start - pp.gap_off);
+    }
+  }
+  pp.payload = payload;
+  if (payload)
+    for (int i = 0; i < 6; i++) {
+      pp.pad_off[i] = P->off[i] + P->size[i];
+      pp.pad_len[i] = (uint32_t)(align_up(P->size[i], 16) - P->size[i]);
+    }
+  Bracket br(P, st);
+  const int rc = launch_prologue(pp, st);
+  br.done("kvc_prologue");
+  P->launches++;
+  return cuda_status(rc);
+}
+
+static void fill_lossless(kvc_plan_s *P, LosslessParams &lp, void *ws) {
+  memset(&lp, 0, sizeof lp);
+  lp.payload_bytes = P->payload_bytes;
+  lp.data_start = P->data_start;
+  lp.chunk_bytes = P->prof.chunk_bytes;
+  lp.n_chunks = (uint32_t)P->n_chunks;
+  lp.n_stages = P->prof.n_stages;
+  for (uint32_t s = 0; s < P->prof.n_stages; s++) {
+    lp.kind[s] = P->prof.stages[s].kind;
+    lp.param[s] = P->prof.stages[s].param;
+  }
+  lp.state = state_of(ws);
+  lp.ctrl = ctrl_of(ws);
+  lp.skip_ticket = P->skip_ticket;
+  lp.poll_limit = P->poll_limit;
+  memcpy(lp.header, P->header, KVC_HEADER_BYTES);
+}
+
+static kvc_status lossless_encode_impl(kvc_plan_s *P, const uint8_t *Q, void *d_stream, size_t cap, void *ws,
+                                       uint64_t *d_stream_bytes, cudaStream_t st) {
+  if (P->prof.n_stages == 0) {
+    if (P->payload_bytes &&
+        cudaMemcpyAsync(static_cast<uint8_t *>(d_stream) + KVC_HEADER_BYTES, Q, P->payload_bytes,
+                        cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+      return KVC_ERR_CUDA;
+    return KVC_OK;
+  }
+  LosslessParams lp;
+  fill_lossless(P, lp, ws);
+  lp.payload = Q;
+  lp.stream = static_cast<uint8_t *>(d_stream);
+  lp.stream_cap = cap;
+  lp.d_stream_bytes = d_stream_bytes;
+  Bracket br(P, st);
+  const int rc = launch_lossless_encode(lp, P->sm_count, st);
+  br.done("kvc_lossless_enc");
+  if (P->n_chunks) P->launches++;
+  return cuda_status(rc);
+}
+
+extern "C" kvc_status kvc_quantize(kvc_plan_t *plan, const kvc_kv *in, void *d_payload, void *d_workspace,
+                                   size_t workspace_bytes, kvc_stream_t stream) {
+  if (!plan || !d_payload || !aligned16(d_payload)) return KVC_ERR_INVALID_ARG;
+  kvc_status s = check_kv(plan, in);
+  if (s != KVC_OK) return s;
+  if ((s = check_ws(plan, d_workspace, workspace_bytes)) != KVC_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t *Q = static_cast<uint8_t *>(d_payload);
+  if ((s = run_prologue(plan, d_workspace, true, false, nullptr, nullptr, Q, st)) != KVC_OK) return s;
+  return run_quant(plan, in, Q, d_workspace, true, false, st);
+}
+
+extern "C" kvc_status kvc_lossless_encode(kvc_plan_t *plan, const void *d_payload, void *d_stream, size_t stream_cap,
+                                          void *d_workspace, size_t workspace_bytes, uint64_t *d_stream_bytes,
+                                          kvc_stream_t stream) {
+  if (!plan || !d_stream || !aligned16(d_stream) || (!d_payload && plan->payload_bytes) ||
+      (d_payload && !aligned16(d_payload)))
+    return KVC_ERR_INVALID_ARG;
+  if (stream_cap < plan->max_stream_bytes) return KVC_ERR_CAPACITY;
+  kvc_status s = check_ws(plan, d_workspace, workspace_bytes);
+  if (s != KVC_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((s = run_prologue(plan, d_workspace, false, true, static_cast<uint8_t *>(d_stream), d_stream_bytes, nullptr, st)) !=
+      KVC_OK)
+    return s;
+  return lossless_encode_impl(plan, static_cast<const uint8_t *>(d_payload), d_stream, stream_cap, d_workspace,
+                              d_stream_bytes, st);
+}
+
+extern "C" kvc_status kvc_encode(kvc_plan_t *plan, const kvc_kv *in, void *d_stream, size_t stream_cap,
+                                 void *d_workspace, size_t workspace_bytes, uint64_t *d_stream_bytes,
+                                 kvc_stream_t stream) {
+  if (!plan || !d_stream || !aligned16(d_stream)) return KVC_ERR_INVALID_ARG;
+  kvc_status s = check_kv(plan, in);
+  if (s != KVC_OK) return s;
+  if (stream_cap < plan->max_stream_bytes) return KVC_ERR_CAPACITY;
+  if ((s = check_ws(plan, d_workspace, workspace_bytes)) != KVC_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t *out = static_cast<uint8_t *>(d_stream);
+  // without lossless stages the payload is written in place after the header
+  uint8_t *Q = plan->prof.n_stages ? ws_payload(plan, d_workspace) : out + KVC_HEADER_BYTES;
+  if ((s = run_prologue(plan, d_workspace, true, true, out, d_stream_bytes, Q, st)) != KVC_OK) return s;
+  if ((s = run_quant(plan, in, Q, d_workspace, true, false, st)) != KVC_OK) return s;
+  if (plan->prof.n_stages == 0) return KVC_OK;
+  return lossless_encode_impl(plan, Q, d_stream, stream_cap, d_workspace, d_stream_bytes, st);
+}
+
+static kvc_status lossless_decode_impl(kvc_plan_s *P, const void *d_stream, size_t stream_bytes, uint8_t *Q, void *ws,
+                                       bool copy_plain, cudaStream_t st) {
+  LosslessParams lp;
+  fill_lossless(P, lp, ws);
+  lp.stream = static_cast<uint8_t *>(const_cast<void *>(d_stream));
+  lp.stream_cap = stream_bytes;
+  lp.out_payload = Q;
+  {
+    Bracket br(P, st);
+    const int rc = launch_decode_prepare(lp, st);
+    br.done("kvc_decode_prepare");
+    P->launches++;
+    if (rc) return KVC_ERR_CUDA;
+  }
+  if (P->prof.n_stages == 0) {
+    // the payload sits after the header; copy only when the caller wants it elsewhere
+    if (copy_plain && P->payload_bytes && stream_bytes >= KVC_HEADER_BYTES + P->payload_bytes &&
+        cudaMemcpyAsync(Q, static_cast<const uint8_t *>(d_stream) + KVC_HEADER_BYTES, P->payload_bytes,
+                        cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+      return KVC_ERR_CUDA;
+    return KVC_OK;
+  }
+  Bracket br(P, st);
+  const int rc = launch_lossless_decode(lp, P->sm_count, st);
+  br.done("kvc_lossless_dec");
+  if (P->n_chunks) P->launches++;
+  return cuda_status(rc);
+}
+
+extern "C" kvc_status kvc_lossless_decode(kvc_plan_t *plan, const void *d_stream, size_t stream_bytes, void *d_payload,
+                                          void *d_workspace, size_t workspace_bytes, kvc_stream_t stream) {
+  if (!plan || !d_stream || !aligned16(d_stream) || (!d_payload && plan->payload_bytes) ||
+      (d_payload && !aligned16(d_payload)))
+    return KVC_ERR_INVALID_ARG;
+  kvc_status s = check_ws(plan, d_workspace, workspace_bytes);
+  if (s != KVC_OK) return s;
+  return lossless_decode_impl(plan, d_stream, stream_bytes, static_cast<uint8_t *>(d_payload), d_workspace, true,
+                              (cudaStream_t)stream);
+}
+
+extern "C" kvc_status kvc_dequantize(kvc_plan_t *plan, const void *d_payload, const kvc_kv *out, void *d_workspace,
+                                     size_t workspace_bytes, kvc_stream_t stream) {
+  if (!plan || (!d_payload && plan->payload_bytes) || (d_payload && !aligned16(d_payload))) return KVC_ERR_INVALID_ARG;
+  kvc_status s = check_kv(plan, out);
+  if (s != KVC_OK) return s;
+  if ((s = check_ws(plan, d_workspace, workspace_bytes)) != KVC_OK) return s;
+  return run_quant(plan, out, static_cast<uint8_t *>(const_cast<void *>(d_payload)), d_workspace, false, false,
+                   (cudaStream_t)stream);
+}
+
+extern "C" kvc_status kvc_decode(kvc_plan_t *plan, const void *d_stream, size_t stream_bytes, const kvc_kv *out,
+                                 void *d_workspace, size_t workspace_bytes, kvc_stream_t stream) {
+  if (!plan || !d_stream || !aligned16(d_stream)) return KVC_ERR_INVALID_ARG;
+  kvc_status s = check_kv(plan, out);
+  if (s != KVC_OK) return s;
+  if ((s = check_ws(plan, d_workspace, workspace_bytes)) != KVC_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t *Q = plan->prof.n_stages ? ws_payload(plan, d_workspace)
+                                   : static_cast<uint8_t *>(const_cast<void *>(d_stream)) + KVC_HEADER_BYTES;
+  if ((s = lossless_decode_impl(plan, d_stream, stream_bytes, Q, d_workspace, false, st)) != KVC_OK) return s;
+  return run_quant(plan, out, Q, d_workspace, false, true, st);
+}
+
+extern "C" kvc_status kvc_query(const void *d_workspace, kvc_stream_t stream, uint64_t *host_stream_bytes,
+                                uint32_t *host_flags) {
+  if (!d_workspace) return KVC_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KVC_ERR_CUDA;
+  uint64_t ctrl[2] = {0, 0};
+  if (cudaMemcpy(ctrl, d_workspace, sizeof ctrl, cudaMemcpyDeviceToHost) != cudaSuccess) return KVC_ERR_CUDA;
+  const uint32_t flags = (uint32_t)(ctrl[0] & 0xffffffffu);
+  if (host_flags) *host_flags = flags;
+  if (host_stream_bytes) *host_stream_bytes = ctrl[1];
+  if (flags & KVC_FLAG_CORRUPT) return KVC_ERR_CORRUPT;
+  if (flags & KVC_FLAG_CAPACITY) return KVC_ERR_CAPACITY;
+  if (flags & KVC_FLAG_TIMEOUT) return KVC_ERR_TIMEOUT;
+  if (flags & KVC_FLAG_BAD_PAGE) return KVC_ERR_INVALID_ARG;
+  if (flags & KVC_FLAG_NONFINITE) return KVC_ERR_NONFINITE;
+  if (flags & KVC_FLAG_RANGE) return KVC_ERR_RANGE;
+  return KVC_OK;
+}
+
+extern "C" const char *kvc_status_str(kvc_status s) {
+  switch (s) {
+    case KVC_OK: return "ok";
+    case KVC_ERR_INVALID_ARG: return "invalid argument";
+    case KVC_ERR_UNSUPPORTED: return "unsupported";
+    case KVC_ERR_CAPACITY: return "capacity too small";
+    case KVC_ERR_CORRUPT: return "corrupt stream";
+    case KVC_ERR_RANGE: return "fp16 metadata overflow (saturated)";
+    case KVC_ERR_NONFINITE: return "non-finite input";
+    case KVC_ERR_TIMEOUT: return "device wait timed out";
+    case KVC_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}

@@ -1,0 +1,99 @@
+// kvc_internal.h -- parameter blocks shared by the C-ABI host code and the kernels.
+//
+// Workspace control block (first 256 bytes of the caller's workspace):
+//   u32 [0]  status flags (KVC_FLAG_*), set with atomicOr by any kernel
+//   u64 @8   stream size written by the last encode
+//   u32 [4]  chunk ticket counter of the lossless encoder
+// followed at byte 256 by one u64 per lossless chunk (encode: look-back words;
+// decode: chunk byte offsets), then (256-aligned) the quantized payload when
+// lossless stages are on.
+#pragma once
+#include <stdint.h>
+
+#include "../../include/kvc.h"
+
+namespace kvc {
+
+constexpr int kHeadDim = 128;       // only head_dim = 128 is built
+constexpr int kSmoothBlock = 128;   // tokens per key-smoothing block
+constexpr uint32_t kCtrlBytes = 256;
+constexpr int kCtrlFlags = 0;       // u32 index
+constexpr int kCtrlStreamBytes = 1; // u64 index
+constexpr int kCtrlTicket = 4;      // u32 index
+
+// Geometry of one KV tensor (K or V) of every layer.
+struct KvGeom {
+  uint32_t L, T, H;
+  uint32_t bf16;            // 1 = bfloat16, 0 = binary16
+  uint64_t token_stride;    // bytes
+  uint64_t page_stride;     // bytes
+  const int32_t *block_table;
+  uint32_t page_shift, page_mask, num_pages;
+  uint32_t pad_;
+};
+
+// One quantize or dequantize launch over one tensor.
+struct QuantParams {
+  KvGeom g;
+  void *layers[KVC_MAX_LAYERS];  // K or V base pointer per layer (const on encode)
+  uint32_t bits, group, axis, smooth;
+  uint32_t n_tg;                 // token groups per (layer, head) = ceil(T / group)
+  uint32_t n_sb;                 // smoothing blocks per (layer, head) = ceil(T / 128)
+  uint32_t sign[4];              // bit j set => Hadamard sign j is -1
+  uint8_t *codes;                // code section
+  uint8_t *meta;                 // {scale, zero} section
+  uint8_t *mu;                   // fp16 smoothing centres (keys)
+  int8_t *ex;                    // int8 smoothing exponents (keys)
+  uint32_t *status;              // workspace status word
+  uint32_t check_corrupt;        // dequantize: skip when the status word carries CORRUPT
+  uint32_t hadamard;             // randomized Hadamard on
+};
+
+// Prologue: reset workspace words, write the stream header.
+struct PrologueParams {
+  uint32_t *ctrl;
+  uint64_t *state;      // look-back words to zero
+  uint64_t n_state;
+  uint32_t zero_flags;  // also clear the status word
+  uint32_t write_header;
+  uint8_t *stream;
+  uint8_t header[KVC_HEADER_BYTES];
+  uint64_t static_size; // nonzero: the stream size is known now (no lossless chunks)
+  uint64_t gap_off;     // zero padding between the chunk table and the first chunk
+  uint32_t gap_len;
+  uint32_t pad_;
+  uint64_t *d_stream_bytes;
+  // zero padding bytes of the payload sections
+  uint8_t *payload;
+  uint64_t pad_off[6];
+  uint32_t pad_len[6];
+};
+
+struct LosslessParams {
+  const uint8_t *payload;
+  uint64_t payload_bytes;
+  uint8_t *stream;         // encode output / decode input
+  uint64_t stream_cap;     // encode: capacity; decode: stream bytes
+  uint64_t data_start;
+  uint32_t chunk_bytes, n_chunks;
+  uint32_t n_stages;
+  uint8_t kind[KVC_MAX_STAGES], param[KVC_MAX_STAGES];
+  uint64_t *state;         // encode: look-back words; decode: chunk offsets
+  uint32_t *ctrl;
+  uint64_t *d_stream_bytes;
+  uint8_t *out_payload;    // decode output
+  int64_t skip_ticket;     // test hook: this ticket does not publish
+  uint32_t poll_limit;
+  uint32_t pad_;
+  uint8_t header[KVC_HEADER_BYTES];  // decode: expected header
+};
+
+// Launchers (return cudaError_t as int).  `occ_grid` = resident-grid size to use.
+int launch_quantize(const QuantParams &p, int sm_count, void *stream, uint64_t *launches, const char **name);
+int launch_dequantize(const QuantParams &p, int sm_count, void *stream, uint64_t *launches, const char **name);
+int launch_prologue(const PrologueParams &p, void *stream);
+int launch_lossless_encode(const LosslessParams &p, int sm_count, void *stream);
+int launch_decode_prepare(const LosslessParams &p, void *stream);
+int launch_lossless_decode(const LosslessParams &p, int sm_count, void *stream);
+
+}  // namespace kvc
