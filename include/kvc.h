@@ -20,7 +20,9 @@
  *    the current device; host pointers are documented as such.  The caller owns
  *    every buffer (inputs, outputs, stream, workspace).  A plan owns host memory
  *    only and never allocates device memory; encode/decode allocate nothing.
- *  - Work is enqueued asynchronously on the caller's CUDA stream.  Argument and
+ *  - Work is enqueued asynchronously on the caller's CUDA stream.  Every entry
+ *    point that enqueues work first resets the workspace status word, so
+ *    kvc_query() reports the errors of the last call only.  Argument and
  *    profile errors are returned synchronously; errors found by the GPU (corrupt
  *    stream, non-finite input, fp16 metadata overflow, look-back timeout) set bits
  *    of a status word in the workspace, which kvc_query() reads after a sync.
@@ -172,8 +174,8 @@ kvc_status kvc_lossless_encode(kvc_plan_t *plan, const void *d_payload, void *d_
 kvc_status kvc_lossless_decode(kvc_plan_t *plan, const void *d_stream, size_t stream_bytes, void *d_payload,
                                void *d_workspace, size_t workspace_bytes, kvc_stream_t stream);
 /* Dequantization, inverse Hadamard, normalization, sign restoration, unsmoothing
- * and conversion to the element type (fused); skipped when the status word
- * already carries KVC_FLAG_CORRUPT. */
+ * and conversion to the element type (fused).  (Inside kvc_decode this step is
+ * skipped on the device when the lossless decode found the stream corrupt.) */
 kvc_status kvc_dequantize(kvc_plan_t *plan, const void *d_payload, const kvc_kv *out, void *d_workspace,
                           size_t workspace_bytes, kvc_stream_t stream);
 

@@ -459,7 +459,7 @@ extern "C" kvc_status kvc_lossless_encode(kvc_plan_t *plan, const void *d_payloa
   kvc_status s = check_ws(plan, d_workspace, workspace_bytes);
   if (s != KVC_OK) return s;
   cudaStream_t st = (cudaStream_t)stream;
-  if ((s = run_prologue(plan, d_workspace, false, true, static_cast<uint8_t *>(d_stream), d_stream_bytes, nullptr, st)) !=
+  if ((s = run_prologue(plan, d_workspace, true, true, static_cast<uint8_t *>(d_stream), d_stream_bytes, nullptr, st)) !=
       KVC_OK)
     return s;
   return lossless_encode_impl(plan, static_cast<const uint8_t *>(d_payload), d_stream, stream_cap, d_workspace,
@@ -530,8 +530,9 @@ extern "C" kvc_status kvc_dequantize(kvc_plan_t *plan, const void *d_payload, co
   kvc_status s = check_kv(plan, out);
   if (s != KVC_OK) return s;
   if ((s = check_ws(plan, d_workspace, workspace_bytes)) != KVC_OK) return s;
-  return run_quant(plan, out, static_cast<uint8_t *>(const_cast<void *>(d_payload)), d_workspace, false, false,
-                   (cudaStream_t)stream);
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((s = run_prologue(plan, d_workspace, true, false, nullptr, nullptr, nullptr, st)) != KVC_OK) return s;
+  return run_quant(plan, out, static_cast<uint8_t *>(const_cast<void *>(d_payload)), d_workspace, false, false, st);
 }
 
 extern "C" kvc_status kvc_decode(kvc_plan_t *plan, const void *d_stream, size_t stream_bytes, const kvc_kv *out,

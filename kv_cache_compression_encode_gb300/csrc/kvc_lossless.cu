@@ -21,7 +21,7 @@
 
 namespace kvc {
 
-constexpr int LT = 512;               // threads per lossless CTA
+constexpr int LT = 512;               // threads per generic lossless CTA
 constexpr int kScratchBytes = 8192 + 1024 + 256;  // RZE bitmap (<= 64 KiB / 8) + scan temporaries
 constexpr uint64_t kFlagAgg = 1ull << 62, kFlagIncl = 2ull << 62, kValMask = (1ull << 62) - 1;
 
@@ -38,7 +38,7 @@ __device__ __forceinline__ uint64_t ld_acquire(const uint64_t *p) {
 
 // Block-wide exclusive scan of one value per thread (LT threads).  tmp holds
 // LT/32 + 1 words.  Ends with a barrier, so tmp can be reused immediately.
-template <typename U>
+template <typename U, int NT = LT>
 __device__ __forceinline__ U block_excl_scan(U v, U *tmp, U &total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   U x = v;
@@ -50,18 +50,18 @@ __device__ __forceinline__ U block_excl_scan(U v, U *tmp, U &total) {
   if (lane == 31) tmp[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    U w = lane < LT / 32 ? tmp[lane] : U(0);
+    U w = lane < NT / 32 ? tmp[lane] : U(0);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const U y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    if (lane < LT / 32) tmp[lane] = w;
-    if (lane == LT / 32 - 1) tmp[LT / 32] = w;
+    if (lane < NT / 32) tmp[lane] = w;
+    if (lane == NT / 32 - 1) tmp[NT / 32] = w;
   }
   __syncthreads();
   const U excl = x - v + (warp ? tmp[warp - 1] : U(0));
-  total = tmp[LT / 32];
+  total = tmp[NT / 32];
   __syncthreads();
   return excl;
 }
@@ -96,12 +96,13 @@ __device__ __forceinline__ void st_word(uint8_t *p, uint32_t w, uint32_t v) {
 // Every stage keeps the tail past the last whole tuple / word as is.
 // ---------------------------------------------------------------------------
 // TUPL_k: m = n/k tuples; column j (byte j of every tuple) is written contiguously.
+template <int NT = LT>
 __device__ void tupl_encode(const uint8_t *in, uint8_t *out, uint32_t n, uint32_t k) {
   const uint32_t m = n / k;
   if ((m & 3u) == 0) {
     // four tuples per thread: read 4k bytes, write k words of 4 bytes
     const uint32_t nq = m / 4;
-    for (uint32_t idx = threadIdx.x; idx < nq; idx += LT) {
+    for (uint32_t idx = threadIdx.x; idx < nq; idx += NT) {
       uint32_t src[8];
       const uint32_t *in32 = reinterpret_cast<const uint32_t *>(in) + idx * k;
       for (uint32_t u = 0; u < k; u++) src[u] = in32[u];
@@ -117,15 +118,16 @@ __device__ void tupl_encode(const uint8_t *in, uint8_t *out, uint32_t n, uint32_
     }
   } else {
     for (uint32_t j = 0; j < k; j++)
-      for (uint32_t i = threadIdx.x; i < m; i += LT) out[j * m + i] = in[i * k + j];
+      for (uint32_t i = threadIdx.x; i < m; i += NT) out[j * m + i] = in[i * k + j];
   }
-  for (uint32_t o = m * k + threadIdx.x; o < n; o += LT) out[o] = in[o];
+  for (uint32_t o = m * k + threadIdx.x; o < n; o += NT) out[o] = in[o];
   __syncthreads();
 }
 
+template <int NT = LT>
 __device__ void tupl_decode(const uint8_t *in, uint8_t *out, uint32_t n, uint32_t k) {
   const uint32_t m = n / k;
-  for (uint32_t i = threadIdx.x; i < m; i += LT) {
+  for (uint32_t i = threadIdx.x; i < m; i += NT) {
     if (k == 8) {
       uint64_t v = 0;
 #pragma unroll
@@ -140,15 +142,16 @@ __device__ void tupl_decode(const uint8_t *in, uint8_t *out, uint32_t n, uint32_
       *reinterpret_cast<uint16_t *>(out + 2 * i) = (uint16_t)(in[i] | (in[m + i] << 8));
     }
   }
-  for (uint32_t o = m * k + threadIdx.x; o < n; o += LT) out[o] = in[o];
+  for (uint32_t o = m * k + threadIdx.x; o < n; o += NT) out[o] = in[o];
   __syncthreads();
 }
 
 // BIT_8: plane p (n8/8 bytes) collects bit p of every byte, byte i -> bit i%8 of byte i/8.
+template <int NT = LT>
 __device__ void bit_encode(const uint8_t *in, uint8_t *out, uint32_t n) {
   const uint32_t n8 = n & ~7u, P = n8 / 8;
   if ((P & 3u) == 0) {
-    for (uint32_t idx = threadIdx.x; idx < P / 4; idx += LT) {
+    for (uint32_t idx = threadIdx.x; idx < P / 4; idx += NT) {
       const uint4 a = reinterpret_cast<const uint4 *>(in)[2 * idx];
       const uint4 b = reinterpret_cast<const uint4 *>(in)[2 * idx + 1];
       const uint64_t x0 = transpose8(((uint64_t)a.y << 32) | a.x), x1 = transpose8(((uint64_t)a.w << 32) | a.z);
@@ -161,65 +164,69 @@ __device__ void bit_encode(const uint8_t *in, uint8_t *out, uint32_t n) {
       }
     }
   } else {
-    for (uint32_t b = threadIdx.x; b < P; b += LT) {
+    for (uint32_t b = threadIdx.x; b < P; b += NT) {
       const uint64_t x = transpose8(*reinterpret_cast<const uint64_t *>(in + 8 * b));
 #pragma unroll
       for (int p = 0; p < 8; p++) out[p * P + b] = (uint8_t)(x >> (8 * p));
     }
   }
-  for (uint32_t o = n8 + threadIdx.x; o < n; o += LT) out[o] = in[o];
+  for (uint32_t o = n8 + threadIdx.x; o < n; o += NT) out[o] = in[o];
   __syncthreads();
 }
 
+template <int NT = LT>
 __device__ void bit_decode(const uint8_t *in, uint8_t *out, uint32_t n) {
   const uint32_t n8 = n & ~7u, P = n8 / 8;
-  for (uint32_t b = threadIdx.x; b < P; b += LT) {
+  for (uint32_t b = threadIdx.x; b < P; b += NT) {
     uint64_t x = 0;
 #pragma unroll
     for (int p = 0; p < 8; p++) x |= (uint64_t)in[p * P + b] << (8 * p);
     *reinterpret_cast<uint64_t *>(out + 8 * b) = transpose8(x);
   }
-  for (uint32_t o = n8 + threadIdx.x; o < n; o += LT) out[o] = in[o];
+  for (uint32_t o = n8 + threadIdx.x; o < n; o += NT) out[o] = in[o];
   __syncthreads();
 }
 
 // DELTA_w: word i -> word i - word (i-1) mod 2^(8w); word 0 kept.
+template <int NT = LT>
 __device__ void delta_encode(const uint8_t *in, uint8_t *out, uint32_t n, uint32_t w) {
   const uint32_t m = n / w;
   const uint32_t mask = w == 4 ? 0xffffffffu : ((1u << (8 * w)) - 1u);
-  for (uint32_t i = threadIdx.x; i < m; i += LT) {
+  for (uint32_t i = threadIdx.x; i < m; i += NT) {
     const uint32_t cur = ld_word(in + i * w, w), prev = i ? ld_word(in + (i - 1) * w, w) : 0u;
     st_word(out + i * w, w, (cur - prev) & mask);
   }
-  for (uint32_t o = m * w + threadIdx.x; o < n; o += LT) out[o] = in[o];
+  for (uint32_t o = m * w + threadIdx.x; o < n; o += NT) out[o] = in[o];
   __syncthreads();
 }
 
 // Inverse: running sum mod 2^(8w); each thread sums a contiguous run, then a block scan.
+template <int NT = LT>
 __device__ void delta_decode(const uint8_t *in, uint8_t *out, uint32_t n, uint32_t w, uint32_t *tmp) {
   const uint32_t m = n / w;
   const uint32_t mask = w == 4 ? 0xffffffffu : ((1u << (8 * w)) - 1u);
-  const uint32_t S = (m + LT - 1) / LT;
+  const uint32_t S = (m + NT - 1) / NT;
   const uint32_t i0 = min(m, threadIdx.x * S), i1 = min(m, i0 + S);
   uint32_t sum = 0;
   for (uint32_t i = i0; i < i1; i++) sum += ld_word(in + i * w, w);
   uint32_t total;
-  uint32_t acc = block_excl_scan<uint32_t>(sum, tmp, total);
+  uint32_t acc = block_excl_scan<uint32_t, NT>(sum, tmp, total);
   for (uint32_t i = i0; i < i1; i++) {
     acc += ld_word(in + i * w, w);
     st_word(out + i * w, w, acc & mask);
   }
-  for (uint32_t o = m * w + threadIdx.x; o < n; o += LT) out[o] = in[o];
+  for (uint32_t o = m * w + threadIdx.x; o < n; o += NT) out[o] = in[o];
   __syncthreads();
 }
 
 // RZE_w: B = bitmap of nonzero words, B2 = bitmap of nonzero bytes of B; output
 // B2 | nonzero B bytes | nonzero words | tail.  Returns the encoded size; when it
 // is >= n nothing is written (the chunk will be stored raw).
+template <int NT = LT>
 __device__ uint32_t rze_encode(const uint8_t *in, uint8_t *out, uint32_t n, uint32_t w, uint8_t *Bs,
                                uint32_t *tmp) {
   const uint32_t m = n / w, nb = (m + 7) / 8, nb2 = (nb + 7) / 8, tail = n - m * w;
-  const uint32_t S = (nb + LT - 1) / LT;
+  const uint32_t S = (nb + NT - 1) / NT;
   const uint32_t j0 = min(nb, threadIdx.x * S), j1 = min(nb, j0 + S);
   uint32_t cw = 0, cb = 0;
   for (uint32_t j = j0; j < j1; j++) {
@@ -233,11 +240,11 @@ __device__ uint32_t rze_encode(const uint8_t *in, uint8_t *out, uint32_t n, uint
     cb += byte != 0;
   }
   uint32_t totW, totB;
-  const uint32_t exW = block_excl_scan<uint32_t>(cw, tmp, totW);
-  const uint32_t exB = block_excl_scan<uint32_t>(cb, tmp, totB);
+  const uint32_t exW = block_excl_scan<uint32_t, NT>(cw, tmp, totW);
+  const uint32_t exB = block_excl_scan<uint32_t, NT>(cb, tmp, totB);
   const uint32_t size = nb2 + totB + w * totW + tail;
   if (size >= n) return size;
-  for (uint32_t b2 = threadIdx.x; b2 < nb2; b2 += LT) {
+  for (uint32_t b2 = threadIdx.x; b2 < nb2; b2 += NT) {
     uint32_t v = 0;
     for (uint32_t q = 0; q < 8; q++) {
       const uint32_t j = 8 * b2 + q;
@@ -258,19 +265,20 @@ __device__ uint32_t rze_encode(const uint8_t *in, uint8_t *out, uint32_t n, uint
       }
   }
   const uint32_t t0 = nb2 + totB + w * totW;
-  for (uint32_t o = threadIdx.x; o < tail; o += LT) out[t0 + o] = in[m * w + o];
+  for (uint32_t o = threadIdx.x; o < tail; o += NT) out[t0 + o] = in[m * w + o];
   __syncthreads();
   return size;
 }
 
 // Inverse of RZE for `size` stored bytes that must expand to exactly n bytes.
 // Returns false (uniformly across the block) when the bytes are inconsistent.
+template <int NT = LT>
 __device__ bool rze_decode(const uint8_t *in, uint32_t size, uint8_t *out, uint32_t n, uint32_t w, uint8_t *Bs,
                            uint32_t *tmp) {
   const uint32_t m = n / w, nb = (m + 7) / 8, nb2 = (nb + 7) / 8, tail = n - m * w;
   if (size < nb2) return false;
   // B bytes listed by B2 (only its first nb bits count)
-  const uint32_t S2 = (nb2 + LT - 1) / LT;
+  const uint32_t S2 = (nb2 + NT - 1) / NT;
   const uint32_t b0 = min(nb2, threadIdx.x * S2), b1 = min(nb2, b0 + S2);
   uint32_t cb = 0;
   for (uint32_t b = b0; b < b1; b++) {
@@ -279,7 +287,7 @@ __device__ bool rze_decode(const uint8_t *in, uint32_t size, uint8_t *out, uint3
     cb += __popc(v);
   }
   uint32_t totB;
-  uint32_t rB = block_excl_scan<uint32_t>(cb, tmp, totB);
+  uint32_t rB = block_excl_scan<uint32_t, NT>(cb, tmp, totB);
   if (nb2 + totB > size) return false;
   for (uint32_t b = b0; b < b1; b++) {
     const uint32_t v = in[b];
@@ -291,7 +299,7 @@ __device__ bool rze_decode(const uint8_t *in, uint32_t size, uint8_t *out, uint3
   }
   __syncthreads();
   // words listed by B (only its first m bits count)
-  const uint32_t S = (nb + LT - 1) / LT;
+  const uint32_t S = (nb + NT - 1) / NT;
   const uint32_t j0 = min(nb, threadIdx.x * S), j1 = min(nb, j0 + S);
   uint32_t cw = 0;
   for (uint32_t j = j0; j < j1; j++) {
@@ -300,7 +308,7 @@ __device__ bool rze_decode(const uint8_t *in, uint32_t size, uint8_t *out, uint3
     cw += __popc(v);
   }
   uint32_t totW;
-  uint32_t rW = block_excl_scan<uint32_t>(cw, tmp, totW);
+  uint32_t rW = block_excl_scan<uint32_t, NT>(cw, tmp, totW);
   if (nb2 + totB + w * totW + tail != size) return false;
   const uint8_t *words = in + nb2 + totB;
   for (uint32_t j = j0; j < j1; j++) {
@@ -317,7 +325,7 @@ __device__ bool rze_decode(const uint8_t *in, uint32_t size, uint8_t *out, uint3
     }
   }
   const uint8_t *tl = words + w * totW;
-  for (uint32_t o = threadIdx.x; o < tail; o += LT) out[m * w + o] = tl[o];
+  for (uint32_t o = threadIdx.x; o < tail; o += NT) out[m * w + o] = tl[o];
   __syncthreads();
   return true;
 }
@@ -440,6 +448,376 @@ __global__ void __launch_bounds__(LT) kvc_lossless_enc(const LosslessParams P) {
     }
     __syncthreads();
   }
+}
+
+// ===========================================================================
+// Fast encoder for the stage lists TUPL_8 [BIT_8] [DELTA_1] RZE_w (w = 1 or 2)
+// and chunks of at most 16 KiB.  Per chunk, in shared memory:
+//  * the chunk arrives by cp.async into a swizzled buffer while the previous
+//    chunk is being encoded (two input buffers per CTA);
+//  * TUPL_8 (and BIT_8) run as one register transform per 8-tuple block: a 4x4
+//    byte transpose (byte_perm) gathers byte j of the 8 tuples, an 8x8 bit
+//    transpose turns them into the 8 bit-plane bytes, which land at their final
+//    offsets;
+//  * DELTA_1 is a per-byte SIMD subtraction (__vsub4) of each 16-byte unit and
+//    its predecessor bytes;
+//  * RZE: each thread turns a 16-byte unit into its bitmap bits, warp scans and
+//    block sums give every unit its output offsets, ballots build the second-
+//    level bitmap; the encoded size is known before anything is written, so an
+//    incompressible chunk costs no compaction;
+//  * warp 0 runs the look-back 32 predecessors at a time.
+// A last chunk whose length is not a multiple of 512 bytes takes the generic
+// stage functions.
+// ===========================================================================
+constexpr int FT = 256;
+constexpr uint32_t kFastMaxChunk = 16384;
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// 16-byte unit u of a fast chunk is stored at swz(u): within each 64-byte block
+// the four units rotate by (block >> 1), so 8 lanes reading unit k of 8
+// consecutive blocks touch 8 distinct bank groups.
+__device__ __forceinline__ uint32_t swz(uint32_t u) { return (u & ~3u) | ((u + (u >> 3)) & 3u); }
+__device__ __forceinline__ bool fast_len(uint32_t n) { return (n & 511u) == 0 && n <= kFastMaxChunk; }
+
+__device__ void issue_chunk_load(const LosslessParams &P, uint32_t t, uint8_t *dst) {
+  const uint64_t off = (uint64_t)t * P.chunk_bytes;
+  const uint32_t n = (uint32_t)min((uint64_t)P.chunk_bytes, P.payload_bytes - off);
+  const bool fast = fast_len(n);
+  const uint8_t *src = P.payload + off;
+  for (uint32_t u = threadIdx.x; u < n / 16; u += FT) cp_async16(dst + 16 * (fast ? swz(u) : u), src + 16 * u);
+}
+
+// 4x4 byte transpose: o[j] = byte j of a, b, c, d.
+__device__ __forceinline__ void byte_t4x4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t (&o)[4]) {
+  const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(c, d, 0x5140);
+  const uint32_t t2 = __byte_perm(a, b, 0x7362), t3 = __byte_perm(c, d, 0x7362);
+  o[0] = __byte_perm(t0, t1, 0x5410);
+  o[1] = __byte_perm(t0, t1, 0x7632);
+  o[2] = __byte_perm(t2, t3, 0x5410);
+  o[3] = __byte_perm(t2, t3, 0x7632);
+}
+
+// transpose8 on the 64-bit value (hi:lo), both 32-bit halves at a time.
+__device__ __forceinline__ void bits8x8(uint32_t &lo, uint32_t &hi) {
+  uint32_t t;
+  t = (lo ^ (lo >> 7)) & 0x00AA00AAu; lo ^= t ^ (t << 7);
+  t = (hi ^ (hi >> 7)) & 0x00AA00AAu; hi ^= t ^ (t << 7);
+  t = (lo ^ (lo >> 14)) & 0x0000CCCCu; lo ^= t ^ (t << 14);
+  t = (hi ^ (hi >> 14)) & 0x0000CCCCu; hi ^= t ^ (t << 14);
+  t = (lo ^ (hi << 4)) & 0xF0F0F0F0u;
+  lo ^= t;
+  hi ^= t >> 4;
+}
+
+// TUPL_8 (and BIT_8 after it) of a fast chunk: `in` swizzled, `out` plain.
+template <bool BIT8>
+__device__ void fast_transform(const uint8_t *in, uint8_t *out, uint32_t n) {
+  const uint32_t nblk = n / 64, m = n / 8, m8 = n / 64;
+  for (uint32_t beta = threadIdx.x; beta < nblk; beta += FT) {
+    uint32_t w[16];
+    const uint4 *blk = reinterpret_cast<const uint4 *>(in) + 4 * beta;
+    const uint32_t rot = (beta >> 1) & 3u;
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      const uint4 v = blk[(k + rot) & 3u];
+      w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+    }
+    uint32_t L0[4], L1[4], H0[4], H1[4];  // byte j (0..3 / 4..7) of tuples 0..3 / 4..7
+    byte_t4x4(w[0], w[2], w[4], w[6], L0);
+    byte_t4x4(w[8], w[10], w[12], w[14], L1);
+    byte_t4x4(w[1], w[3], w[5], w[7], H0);
+    byte_t4x4(w[9], w[11], w[13], w[15], H1);
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      uint32_t lo = j < 4 ? L0[j & 3] : H0[j & 3], hi = j < 4 ? L1[j & 3] : H1[j & 3];
+      if (BIT8) {
+        bits8x8(lo, hi);
+        uint8_t *ob = out + j * m8 + beta;
+#pragma unroll
+        for (int p = 0; p < 4; p++) ob[p * m] = (uint8_t)(lo >> (8 * p));
+#pragma unroll
+        for (int p = 0; p < 4; p++) ob[(p + 4) * m] = (uint8_t)(hi >> (8 * p));
+      } else {
+        *reinterpret_cast<uint2 *>(out + j * m + 8 * beta) = make_uint2(lo, hi);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// DELTA_1 in place on a fast chunk (n <= 16384: at most 4 units per thread).
+__device__ void fast_delta1(uint8_t *buf, uint32_t n) {
+  const uint32_t nu = n / 16;
+  uint4 res[4];
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    const uint32_t u = k * FT + threadIdx.x;
+    if (u < nu) {
+      const uint4 v = reinterpret_cast<const uint4 *>(buf)[u];
+      const uint32_t prev = u ? buf[16 * u - 1] : 0u;
+      res[k].x = __vsub4(v.x, (v.x << 8) | prev);
+      res[k].y = __vsub4(v.y, (v.y << 8) | (v.x >> 24));
+      res[k].z = __vsub4(v.z, (v.z << 8) | (v.y >> 24));
+      res[k].w = __vsub4(v.w, (v.w << 8) | (v.z >> 24));
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    const uint32_t u = k * FT + threadIdx.x;
+    if (u < nu) reinterpret_cast<uint4 *>(buf)[u] = res[k];
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ uint64_t spread_bits(uint32_t m) {
+  uint64_t x = m;
+  x = (x | (x << 16)) & 0x0000FFFF0000FFFFull;
+  x = (x | (x << 8)) & 0x00FF00FF00FF00FFull;
+  x = (x | (x << 4)) & 0x0F0F0F0F0F0F0F0Full;
+  x = (x | (x << 2)) & 0x3333333333333333ull;
+  x = (x | (x << 1)) & 0x5555555555555555ull;
+  return x;
+}
+
+// RZE_W of a fast chunk, in -> out (distinct plain buffers).  Returns the encoded
+// size; nothing is written when it is >= n.
+template <int W>
+__device__ uint32_t fast_rze(const uint8_t *in, uint8_t *out, uint32_t n, uint32_t *offs, uint16_t *Bs,
+                             uint32_t *wsum) {
+  const uint32_t nu = n / 16, nb = n / (8 * W), nb2 = nb / 8;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t baseB = 0, baseW = 0;
+  for (uint32_t p0 = 0; p0 < nu; p0 += FT) {
+    const uint32_t u = p0 + threadIdx.x;
+    uint32_t bits = 0;
+    if (u < nu) {
+      const uint4 v = reinterpret_cast<const uint4 *>(in)[u];
+      const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        if (W == 2) {
+          bits |= (uint32_t)((x[k] & 0xffffu) != 0u) << (2 * k);
+          bits |= (uint32_t)((x[k] >> 16) != 0u) << (2 * k + 1);
+        } else {
+#pragma unroll
+          for (int b = 0; b < 4; b++) bits |= (uint32_t)(((x[k] >> (8 * b)) & 0xffu) != 0u) << (4 * k + b);
+        }
+      }
+      Bs[u] = (uint16_t)bits;
+    }
+    const uint32_t nzB = W == 2 ? (bits != 0u) : ((bits & 0xffu) != 0u) + ((bits >> 8) != 0u);
+    const uint32_t c = (nzB << 16) | (uint32_t)__popc(bits);
+    uint32_t x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    uint32_t wb = 0, tot = 0;
+#pragma unroll
+    for (int i = 0; i < FT / 32; i++) {
+      const uint32_t t = wsum[i];
+      if (i < warp) wb += t;
+      tot += t;
+    }
+    if (u < nu) offs[u] = ((baseB << 16) | baseW) + wb + x - c;
+    baseB += tot >> 16;
+    baseW += tot & 0xffffu;
+    __syncthreads();
+  }
+  const uint32_t totB = baseB, totW = baseW;
+  const uint32_t size = nb2 + totB + W * totW;
+  if (size >= n) return size;
+  uint8_t *oB = out + nb2, *oW = out + nb2 + totB;
+  for (uint32_t p0 = 0; p0 < nu; p0 += FT) {
+    const uint32_t u = p0 + threadIdx.x;
+    const uint32_t bits = u < nu ? Bs[u] : 0u;
+    if (W == 2) {
+      const uint32_t m32 = __ballot_sync(0xffffffffu, bits != 0u);
+      if (lane == 0 && p0 + warp * 32 < nu) reinterpret_cast<uint32_t *>(out)[(p0 + warp * 32) / 32] = m32;
+    } else {
+      const uint32_t ml = __ballot_sync(0xffffffffu, (bits & 0xffu) != 0u);
+      const uint32_t mh = __ballot_sync(0xffffffffu, (bits >> 8) != 0u);
+      if (lane == 0 && p0 + warp * 32 < nu)
+        reinterpret_cast<uint64_t *>(out)[(p0 + warp * 32) / 32] = spread_bits(ml) | (spread_bits(mh) << 1);
+    }
+    if (u < nu && bits) {
+      const uint32_t o = offs[u];
+      uint32_t rB = o >> 16, rW = o & 0xffffu;
+      const uint4 v = reinterpret_cast<const uint4 *>(in)[u];
+      const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+      if (W == 2) {
+        oB[rB] = (uint8_t)bits;
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+          if ((bits >> k) & 1u) {
+            const uint32_t word = (x[k >> 1] >> (16 * (k & 1))) & 0xffffu;
+            oW[2 * rW] = (uint8_t)word;
+            oW[2 * rW + 1] = (uint8_t)(word >> 8);
+            rW++;
+          }
+      } else {
+        if (bits & 0xffu) oB[rB++] = (uint8_t)bits;
+        if (bits >> 8) oB[rB] = (uint8_t)(bits >> 8);
+#pragma unroll
+        for (int k = 0; k < 16; k++)
+          if ((bits >> k) & 1u) oW[rW++] = (uint8_t)(x[k >> 2] >> (8 * (k & 3)));
+      }
+    }
+  }
+  __syncthreads();
+  return size;
+}
+
+__device__ __forceinline__ uint64_t warp_sum64(uint64_t x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Decoupled look-back by one warp: each round reads 32 predecessors' words.
+__device__ uint64_t lookback_warp(const LosslessParams &P, uint32_t ticket, uint64_t agg) {
+  const int lane = threadIdx.x & 31;
+  uint64_t *state = P.state;
+  const bool publish = (int64_t)ticket != P.skip_ticket;
+  if (ticket == 0) {
+    if (lane == 0 && publish) st_release(state, kFlagIncl | agg);
+    return 0;
+  }
+  if (lane == 0 && publish) st_release(state + ticket, kFlagAgg | agg);
+  uint64_t excl = 0;
+  int64_t base = (int64_t)ticket - 1;
+  uint32_t polls = 0;
+  for (;;) {
+    const int64_t j = base - lane;
+    const uint64_t v = j >= 0 ? ld_acquire(state + j) : kFlagIncl;
+    const uint64_t f = v & ~kValMask;
+    const uint32_t nr = __ballot_sync(0xffffffffu, f == 0);
+    const uint32_t inc = __ballot_sync(0xffffffffu, f == kFlagIncl);
+    const int first_inc = inc ? __ffs(inc) - 1 : 32;
+    const int first_nr = nr ? __ffs(nr) - 1 : 32;
+    if (first_inc < first_nr) {
+      excl += warp_sum64(lane <= first_inc ? (v & kValMask) : 0ull);
+      break;
+    }
+    if (first_nr == 32) {
+      excl += warp_sum64(v & kValMask);
+      base -= 32;
+      continue;
+    }
+    if (++polls > P.poll_limit) {
+      if (lane == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
+      break;
+    }
+    __nanosleep(32);
+  }
+  if (lane == 0 && publish) st_release(state + ticket, kFlagIncl | (excl + agg));
+  return excl;
+}
+
+struct FastSpec {
+  uint32_t bit8, delta1, rze_w, pad;
+};
+
+__global__ void __launch_bounds__(FT) kvc_lossless_enc_fast(const LosslessParams P, const FastSpec F) {
+  extern __shared__ uint4 smem_u4[];
+  const uint32_t cb = P.chunk_bytes;
+  uint8_t *const inb0 = reinterpret_cast<uint8_t *>(smem_u4);  // input buffer c at inb0 + c * cb
+  uint8_t *A = inb0 + 2 * cb;
+  uint16_t *Bs = reinterpret_cast<uint16_t *>(A + cb + 64);
+  uint32_t *offs = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(Bs) + cb / 8 + 64);
+  uint32_t *wsum = offs + cb / 16;
+  __shared__ uint32_t s_t[2];
+  __shared__ uint64_t s_excl;
+  const uint32_t nc = P.n_chunks;
+  uint32_t *ticket_ctr = P.ctrl + kCtrlTicket;
+
+  if (threadIdx.x == 0) s_t[0] = atomicAdd(ticket_ctr, 1u);
+  __syncthreads();
+  uint32_t t = s_t[0];
+  uint32_t cur = 0;
+  if (t < nc) issue_chunk_load(P, t, inb0);
+  cp_async_commit();
+  while (t < nc) {
+    if (threadIdx.x == 0) s_t[1] = atomicAdd(ticket_ctr, 1u);
+    __syncthreads();
+    const uint32_t tn = s_t[1];
+    if (tn < nc) issue_chunk_load(P, tn, inb0 + (cur ^ 1) * cb);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+
+    uint8_t *in = inb0 + cur * cb;
+    const uint64_t off = (uint64_t)t * cb;
+    const uint32_t n = (uint32_t)min((uint64_t)cb, P.payload_bytes - off);
+    uint32_t size = n;
+    const uint8_t *outp = in;
+    bool swizzled = false, from_global = false;
+    if (fast_len(n)) {
+      if (F.bit8) fast_transform<true>(in, A, n);
+      else fast_transform<false>(in, A, n);
+      if (F.delta1) fast_delta1(A, n);
+      const uint32_t rs = F.rze_w == 2 ? fast_rze<2>(A, in, n, offs, Bs, wsum) : fast_rze<1>(A, in, n, offs, Bs, wsum);
+      if (rs < n) size = rs;
+      else swizzled = true;  // stored raw: the original bytes are still in `in`
+    } else {
+      uint8_t *cur_b = in, *nxt_b = A;
+      for (uint32_t s = 0; s + 1 < P.n_stages; s++) {
+        const uint32_t k = P.kind[s], prm = P.param[s];
+        if (k == KVC_ST_TUPL) tupl_encode<FT>(cur_b, nxt_b, n, prm);
+        else if (k == KVC_ST_BIT) bit_encode<FT>(cur_b, nxt_b, n);
+        else delta_encode<FT>(cur_b, nxt_b, n, prm);
+        uint8_t *tmpb = cur_b; cur_b = nxt_b; nxt_b = tmpb;
+      }
+      const uint32_t rs = rze_encode<FT>(cur_b, nxt_b, n, P.param[P.n_stages - 1], reinterpret_cast<uint8_t *>(Bs), wsum);
+      if (rs < n) {
+        size = rs;
+        outp = nxt_b;
+      } else {
+        from_global = true;
+      }
+    }
+    const bool raw = size == n;
+    const uint32_t asz = align16u(size);
+    if (!raw && threadIdx.x < asz - size) const_cast<uint8_t *>(outp)[size + threadIdx.x] = 0;
+    if (threadIdx.x < 32) {
+      const uint64_t excl = lookback_warp(P, t, asz);
+      if (threadIdx.x == 0) {
+        s_excl = excl;
+        const uint64_t dst = P.data_start + excl;
+        if (dst + asz > P.stream_cap) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CAPACITY);
+        reinterpret_cast<uint32_t *>(P.stream + KVC_HEADER_BYTES)[t] = size | (raw ? 0x80000000u : 0u);
+        if (t == nc - 1) {
+          const uint64_t total = dst + asz;
+          reinterpret_cast<uint64_t *>(P.ctrl)[kCtrlStreamBytes] = total;
+          if (P.d_stream_bytes) *P.d_stream_bytes = total;
+        }
+      }
+    }
+    __syncthreads();
+    const uint64_t dst = P.data_start + s_excl;
+    if (dst + asz <= P.stream_cap) {
+      uint4 *o = reinterpret_cast<uint4 *>(P.stream + dst);
+      const uint4 *g = reinterpret_cast<const uint4 *>(P.payload + off);
+      const uint4 *sm = reinterpret_cast<const uint4 *>(outp);
+      for (uint32_t i = threadIdx.x; i < asz / 16; i += FT)
+        o[i] = from_global ? __ldg(g + i) : sm[swizzled ? swz(i) : i];
+    }
+    cur ^= 1;
+    t = tn;
+    __syncthreads();
+  }
+  cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------------------
@@ -577,8 +955,37 @@ int launch_prologue(const PrologueParams &p, void *stream) {
   return (int)cudaGetLastError();
 }
 
+static bool fast_spec(const LosslessParams &p, FastSpec &f) {
+  f = FastSpec{0, 0, 0, 0};
+  if (p.chunk_bytes > kFastMaxChunk || p.chunk_bytes % 512) return false;
+  uint32_t s = 0;
+  if (s >= p.n_stages || p.kind[s] != KVC_ST_TUPL || p.param[s] != 8) return false;
+  s++;
+  if (s < p.n_stages && p.kind[s] == KVC_ST_BIT) { f.bit8 = 1; s++; }
+  if (s < p.n_stages && p.kind[s] == KVC_ST_DELTA && p.param[s] == 1) { f.delta1 = 1; s++; }
+  if (s + 1 != p.n_stages || p.kind[s] != KVC_ST_RZE || (p.param[s] != 1 && p.param[s] != 2)) return false;
+  f.rze_w = p.param[s];
+  return true;
+}
+
+static size_t fast_smem(uint32_t cb) { return 3 * (size_t)cb + 64 + cb / 8 + 64 + cb / 4 + 64 * 4; }
+
 int launch_lossless_encode(const LosslessParams &p, int sm_count, void *stream) {
   if (p.n_chunks == 0) return 0;
+  FastSpec f;
+  if (fast_spec(p, f)) {
+    const size_t smem = fast_smem(p.chunk_bytes);
+    cudaError_t e = cudaFuncSetAttribute(kvc_lossless_enc_fast, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kvc_lossless_enc_fast, FT, smem) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    uint64_t blocks = (uint64_t)sm_count * per_sm;
+    if (blocks > p.n_chunks) blocks = p.n_chunks;
+    kvc_lossless_enc_fast<<<(unsigned)blocks, FT, smem, (cudaStream_t)stream>>>(p, f);
+    return (int)cudaGetLastError();
+  }
   const size_t smem = lossless_smem(p.chunk_bytes);
   cudaError_t e = cudaFuncSetAttribute(kvc_lossless_enc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
