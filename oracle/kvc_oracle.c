@@ -619,7 +619,7 @@ void kvo_dequantize(const kvo_profile *p, const kvo_shape *sh, const uint8_t *Q,
 
 /* ------------------------------------------------------------------------ */
 /* Lossless stages ([FastKVComp] §4.2: tuple reordering, bit shuffling,       */
-/* zero-oriented encoding; the benchmark spec adds a delta stage).  READING: the  */
+/* zero-oriented encoding; the workloads add a delta stage).  READING: the   */
 /* byte formats of LC's stages are not on the pages; these are format v1's.   */
 /* Every stage keeps a tail (the bytes past the last whole tuple/word) as is. */
 /* ------------------------------------------------------------------------ */
