@@ -147,6 +147,7 @@ def kernel_bytes(plan, w, name: str, stream_bytes: int) -> int:
     table = 4 * plan.n_chunks
     return {
         "kvc_enc_tile": raw_tensor + k_out,
+        "kvc_enc_ktile": raw_tensor + k_out,
         "kvc_enc_rows": raw_tensor + v_out,
         "kvc_dec_tile": raw_tensor + k_out,
         "kvc_dec_rows": raw_tensor + v_out,

@@ -309,6 +309,11 @@ void kvo_quantize_group(const float *y, uint32_t n, uint32_t bits,
         if (y[i] < mn) mn = y[i];
         if (y[i] > mx) mx = y[i];
     }
+    /* READING: min and max are values; a zero extreme counts as +0 (adding +0
+     * turns -0 into +0 and changes nothing else), so the result does not depend
+     * on the order in which equal zeros of opposite sign are met. */
+    mn = mn + 0.0f;
+    mx = mx + 0.0f;
     uint32_t Q = (1u << bits) - 1u;
     uint16_t zh = kvo_f32_to_f16(mn, 1);
     if ((zh & 0x7fff) == 0x7c00) { zh = (zh & 0x8000) | 0x7bff; *flags |= KVO_FLAG_RANGE; }
@@ -474,6 +479,8 @@ static uint32_t quantize_tensor(const kvo_profile *p, const kvo_shape *sh, int t
                         if (x < mn) mn = x;
                         if (x > mx) mx = x;
                     }
+                    mn = mn + 0.0f; /* a zero extreme counts as +0 (see kvo_quantize_group) */
+                    mx = mx + 0.0f;
                     uint16_t muh = centre_f16(mn, mx, &flags);
                     float mu = kvo_f16_to_f32(muh);
                     float r1 = fabsf(mx - mu), r2 = fabsf(mn - mu);

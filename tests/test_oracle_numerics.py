@@ -223,6 +223,20 @@ def test_quantize_group_bruteforce_exact(oracle, bits):
             assert qi == want, (y, yi, qi, want)
 
 
+def test_signed_zero_extremes_do_not_depend_on_order(oracle):
+    """A group whose minimum (or maximum) is zero gets the same metadata whichever
+    signed zero comes first: the zero point of a zero minimum is +0."""
+    a = np.array([-0.0, 0.0, 1.5, 0.25], np.float32)
+    b = np.array([0.0, -0.0, 1.5, 0.25], np.float32)
+    for bits in (2, 4):
+        ra, rb = oracle.quantize_group(a, bits), oracle.quantize_group(b, bits)
+        assert ra[0] == rb[0] and ra[1] == rb[1] and ra[1] == 0x0000 and np.array_equal(ra[2], rb[2])
+    c = np.array([-1.0, -0.0, -2.0], np.float32)   # maximum is -0
+    d = np.array([-1.0, 0.0, -2.0], np.float32)
+    rc, rd = oracle.quantize_group(c, 4), oracle.quantize_group(d, 4)
+    assert rc[:3][0] == rd[0] and rc[1] == rd[1] and np.array_equal(rc[2], rd[2])
+
+
 def test_quantize_constant_and_range(oracle):
     s_b, z_b, codes, flags = oracle.quantize_group(np.full(16, 0.5, np.float32), 4)
     assert s_b == 0 and _f16(z_b) == 0.5 and not codes.any() and flags == 0
