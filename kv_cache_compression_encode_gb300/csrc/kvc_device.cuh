@@ -119,6 +119,8 @@ template <int BITS>
 __device__ __forceinline__ uint32_t quant_params(float mn, float mx, float &s, float &z, float &r,
                                                  uint32_t &flags) {
   const float Qf = (float)((1u << BITS) - 1u);
+  mn = __fadd_rn(mn, 0.0f);  // a zero extreme counts as +0
+  mx = __fadd_rn(mx, 0.0f);
   const uint32_t zb = saturate_f16(__half_as_ushort(__float2half_rd(mn)), flags);
   z = __half2float(__ushort_as_half((unsigned short)zb));
   const float w = __fsub_rn(mx, z);
@@ -228,6 +230,8 @@ __device__ __forceinline__ float pow2i(int k) {
 
 __device__ __forceinline__ void smooth_params(float mn, float mx, float &mu, float &inv, uint32_t &mu_bits,
                                               int &e, uint32_t &flags) {
+  mn = __fadd_rn(mn, 0.0f);  // a zero extreme counts as +0
+  mx = __fadd_rn(mx, 0.0f);
   const float mid = __fmul_rn(__fadd_rn(mn, mx), 0.5f);
   mu_bits = saturate_f16(__half_as_ushort(__float2half_rn(mid)), flags);
   mu = __half2float(__ushort_as_half((unsigned short)mu_bits));
@@ -242,5 +246,83 @@ __device__ __forceinline__ bool all_finite8(const float *x) {
   for (int i = 0; i < 8; i++) ok &= (fabsf(x[i]) <= 3.402823466e38f);
   return ok;
 }
+
+// ---------------------------------------------------------------------------
+// NaN-propagating min / max (PTX min.NaN / max.NaN, two or three operands): a
+// NaN or infinity anywhere in a group reaches its statistics, so the finite
+// check costs one test per group instead of one per element.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float fmin_n(float a, float b) {
+  float d;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax_n(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ float fmin3_n(float a, float b, float c) {
+  float d;
+  asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmax3_n(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ bool finite2(float a, float b) { return fabsf(a) <= 3.402823466e38f && fabsf(b) <= 3.402823466e38f; }
+
+// ---------------------------------------------------------------------------
+// Packed binary32 pairs (Blackwell f32x2): every lane of a pair is rounded on its
+// own, exactly as the scalar operation.  a - b is written fma(b, -1, a), which is
+// the single rounding of the exact difference.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 bcast2(float a) { return make_float2(a, a); }
+
+// ---------------------------------------------------------------------------
+// Branch-free codes for a pair.  d = (y - z)/s < 2^BITS, p = RN(RN(y - z) * RN(1/s))
+// lies within 2^(BITS-23) of d and RN(d) within 2^(BITS-25); rint(p) therefore
+// equals rint(RN(d)) whenever p is farther than 2^(BITS-22) from a half-integer.
+// rint(p) comes from adding 1.5 * 2^23 (round half to even); the code is the low
+// mantissa bits of that sum.  `bad` is raised for pairs near a half-integer, for
+// s = 0 (p not finite) -- the caller then takes the exact path.
+// ---------------------------------------------------------------------------
+constexpr float kRintMagic = 12582912.0f;  // 1.5 * 2^23
+
+template <int BITS>
+__device__ __forceinline__ float tie_threshold() {
+  return 0.5f - __int_as_float((uint32_t)(127 + BITS - 22) << 23);
+}
+
+// Returns the raw sums; the code of element e is (bits of u.e) & (2^BITS - 1).
+template <int BITS>
+__device__ __forceinline__ float2 qfast2(float2 y, float2 z2, float2 r2, bool &bad) {
+  const float2 t = sub2(y, z2);
+  const float2 p = mul2(t, r2);
+  const float2 u = add2(p, bcast2(kRintMagic));
+  const float2 k = sub2(u, bcast2(kRintMagic));
+  const float2 d = sub2(p, k);
+  const float thr = tie_threshold<BITS>();
+  bad |= !(fabsf(d.x) < thr) || !(fabsf(d.y) < thr);
+  return u;
+}
+
+// The exact rule: clamp(rint_even(RN(RN(y - z) / s)), 0, 2^BITS - 1), 0 when s == 0.
+template <int BITS>
+__device__ __forceinline__ uint32_t qexact(float y, float z, float s) {
+  const float Qf = (float)((1u << BITS) - 1u);
+  if (s == 0.0f) return 0u;
+  const float k = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(y, z), s)), 0.0f), Qf);
+  return (uint32_t)k;
+}
+
+// Code bits of a qfast2 sum, already masked to BITS.
+template <int BITS>
+__device__ __forceinline__ uint32_t code_of(float u) { return __float_as_uint(u) & ((1u << BITS) - 1u); }
 
 }  // namespace kvc

@@ -29,78 +29,179 @@ constexpr int kTS = 144;  // floats per shared-memory tile row (128 + 16: confli
 constexpr size_t kTileSmem = (size_t)(128 * kTS + 2 * 8 * 128 + 2 * 128) * sizeof(float);
 
 // ---------------------------------------------------------------------------
-// rows: encode
+// rows: encode.  Two lanes own a row (token, head): lane half h holds channels
+// 64h .. 64h+63 as 32 packed pairs.  Butterfly stride 1 runs inside each pair,
+// strides 2..32 between pairs, stride 64 across the two lanes; a warp handles 16
+// rows per step.  Groups of 32 or 64 channels are lane-local, groups of 128 take
+// one shuffle.  Codes come from the branch-free pair quantizer; a warp takes the
+// exact division only when one of its lanes met a near-tie.
 // ---------------------------------------------------------------------------
+// Sign masks for the raw element pairs: bit 15 / 31 set where the channel's sign is -1.
+__device__ __forceinline__ uint32_t pair_sign_mask(uint32_t sbits, int j) {
+  return (((sbits >> j) & 1u) << 15) | (((sbits >> (j + 1)) & 1u) << 31);
+}
+
+__device__ __forceinline__ float2 unpack_pair(uint32_t u, bool bf16) {
+  if (bf16) return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+  return __half22float2(*reinterpret_cast<const __half2 *>(&u));
+}
+
+__device__ __forceinline__ uint32_t pack_pair(float2 v, bool bf16) {
+  if (bf16) return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x)) |
+                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y)) << 16);
+  return (uint32_t)__half_as_ushort(__float2half_rn(v.x)) | ((uint32_t)__half_as_ushort(__float2half_rn(v.y)) << 16);
+}
+
+// In-lane butterflies of 64 channels held as 32 pairs: stride 1 within pairs, 2..32 between pairs.
+__device__ __forceinline__ void fwht64_pairs(float2 (&w)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; i++) {
+    const float a = w[i].x, b = w[i].y;
+    w[i] = make_float2(__fadd_rn(a, b), __fsub_rn(a, b));
+  }
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 32; i++)
+      if ((i & h) == 0) {
+        const float2 a = w[i], b = w[i + h];
+        w[i] = add2(a, b);
+        w[i + h] = sub2(a, b);
+      }
+  }
+}
+
+// Insert code c (low BITS bits of c, higher bits ignored) as field `idx` of a
+// little-endian bit string held in 32-bit words.
+template <int BITS, int NW>
+__device__ __forceinline__ void put_code(uint32_t (&w)[NW], int idx, uint32_t c) {
+  constexpr uint32_t M = (1u << BITS) - 1u;
+  const int bit = idx * BITS, wi = bit >> 5, sh = bit & 31;
+  w[wi] |= (c << sh) & (M << sh);
+  if (sh + BITS > 32) w[wi + 1] |= (c & M) >> (32 - sh);
+}
+
 template <int BITS, bool HAD>
-__global__ void __launch_bounds__(kThreads) kvc_enc_rows(const QuantParams P) {
+__global__ void __launch_bounds__(kThreads, 2) kvc_enc_rows(const QuantParams P) {
+  __shared__ uint32_t smask[2][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int part = lane & 3, rsub = lane >> 2;
+  const int half = lane & 1, rsub = lane >> 1;
   const bool bf16 = P.g.bf16 != 0;
   const uint32_t H = P.g.H, T = P.g.T;
   const uint32_t NR = P.g.L * T * H;
-  const uint32_t n_it = (NR + 7) / 8;
-  const int gl = (int)(P.group >> 5);  // lanes per group: 1, 2 or 4
-  const uint32_t row_code_bytes = kHeadDim * BITS / 8;
-  const uint32_t groups_per_row = kHeadDim / P.group;
-  const uint32_t sbits = P.sign[part];
+  const uint32_t n_it = (NR + 15) / 16;
+  const uint32_t G = P.group;
+  if (HAD && threadIdx.x < 64) {
+    const int hh = threadIdx.x >> 5, j = threadIdx.x & 31;  // pair j of half hh: channels 64hh + 2j, +1
+    smask[hh][j] = pair_sign_mask(P.sign[2 * hh + (j >> 4)], (2 * j) & 31);
+  }
+  __syncthreads();
+  const float sg = half ? -1.0f : 1.0f;  // stride 64: lower lane a + b, upper lane a - b = -b + a
   uint32_t flags = 0;
 
   for (uint32_t it = blockIdx.x * (kThreads / 32) + warp; it < n_it; it += gridDim.x * (kThreads / 32)) {
-    const uint32_t R = it * 8 + rsub;
+    const uint32_t R = it * 16 + rsub;
     const bool valid = R < NR;
-    float v[32];
+    float2 w[32];
+    {
+      uint4 q[8];
 #pragma unroll
-    for (int i = 0; i < 32; i++) v[i] = 0.0f;
-    if (valid) {
-      const uint32_t h = R % H, lt = R / H, t = lt % T, l = lt / T;
-      const uint64_t ro = row_offset(P.g, t);
-      if (ro == ~0ull) {
-        flags |= KVC_FLAG_BAD_PAGE;
-      } else {
-        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(P.layers[l]) + ro +
-                                                           (size_t)(h * kHeadDim + 32 * part) * 2);
-        uint4 w[4];
+      for (int j = 0; j < 8; j++) q[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (valid) {
+        const uint32_t h = R % H, lt = R / H, t = lt % T, l = lt / T;
+        const uint64_t ro = row_offset(P.g, t);
+        if (ro == ~0ull) {
+          flags |= KVC_FLAG_BAD_PAGE;
+        } else {
+          const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(P.layers[l]) + ro +
+                                                             (size_t)(h * kHeadDim + 64 * half) * 2);
 #pragma unroll
-        for (int j = 0; j < 4; j++) w[j] = __ldg(src + j);
+          for (int j = 0; j < 8; j++) q[j] = __ldg(src + j);
+        }
+      }
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-          unpack8(w[j], bf16, v + 8 * j);
-          if (!all_finite8(v + 8 * j)) flags |= KVC_FLAG_NONFINITE;
+      for (int j = 0; j < 8; j++) {
+        uint32_t r4[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          if (HAD) r4[e] ^= smask[half][4 * j + e];
+          w[4 * j + e] = unpack_pair(r4[e], bf16);
         }
       }
     }
     if (HAD) {
-      apply_signs(v, sbits);
-      fwht128(v, part);
-      scale_all(v, hadamard_scale());
-    }
-    float mn = v[0], mx = v[0];
+      fwht64_pairs(w);
+      const float2 c2 = bcast2(hadamard_scale()), sg2 = bcast2(sg);
 #pragma unroll
-    for (int i = 1; i < 32; i++) {
-      mn = fminf(mn, v[i]);
-      mx = fmaxf(mx, v[i]);
+      for (int i = 0; i < 32; i++) {
+        const float2 o = make_float2(__shfl_xor_sync(kFull, w[i].x, 1), __shfl_xor_sync(kFull, w[i].y, 1));
+        w[i] = mul2(__ffma2_rn(w[i], sg2, o), c2);
+      }
     }
-    if (gl >= 2) {
-      mn = fminf(mn, __shfl_xor_sync(kFull, mn, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-    }
-    if (gl >= 4) {
-      mn = fminf(mn, __shfl_xor_sync(kFull, mn, 2));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-    }
-    float s, z, r;
-    uint32_t fl = 0;
-    const uint32_t meta = quant_params<BITS>(mn, mx, s, z, r, fl);
-    uint32_t q[32];
+    // group statistics (NaN-propagating): G = 32 -> two groups per lane, 64 -> one, 128 -> lane pair
+    float mn0 = fmin_n(w[0].x, w[0].y), mx0 = fmax_n(w[0].x, w[0].y);
+    float mn1 = fmin_n(w[16].x, w[16].y), mx1 = fmax_n(w[16].x, w[16].y);
 #pragma unroll
-    for (int i = 0; i < 32; i++) q[i] = quant_code<BITS>(v[i], z, s, r);
-    uint32_t wds[BITS];
-    pack32<BITS>(q, wds);
+    for (int i = 1; i < 16; i++) {
+      mn0 = fmin3_n(mn0, w[i].x, w[i].y);
+      mx0 = fmax3_n(mx0, w[i].x, w[i].y);
+      mn1 = fmin3_n(mn1, w[16 + i].x, w[16 + i].y);
+      mx1 = fmax3_n(mx1, w[16 + i].x, w[16 + i].y);
+    }
+    if (G >= 64) {
+      mn0 = mn1 = fmin_n(mn0, mn1);
+      mx0 = mx1 = fmax_n(mx0, mx1);
+    }
+    if (G == 128) {
+      mn0 = mn1 = fmin_n(mn0, __shfl_xor_sync(kFull, mn0, 1));
+      mx0 = mx1 = fmax_n(mx0, __shfl_xor_sync(kFull, mx0, 1));
+    }
+    if (valid && !finite2(mn0, mx0)) flags |= KVC_FLAG_NONFINITE;
+    if (valid && !finite2(mn1, mx1)) flags |= KVC_FLAG_NONFINITE;
+    float s0, z0, r0, s1, z1, r1;
+    uint32_t f0 = 0, f1 = 0;
+    const uint32_t meta0 = quant_params<BITS>(mn0, mx0, s0, z0, r0, f0);
+    const uint32_t meta1 = quant_params<BITS>(mn1, mx1, s1, z1, r1, f1);
+    bool bad = f0 != 0 || f1 != 0;
+    uint32_t wds[2 * BITS];
+#pragma unroll
+    for (int j = 0; j < 2 * BITS; j++) wds[j] = 0u;
+    {
+      const float2 za = bcast2(z0), ra = bcast2(r0), zb = bcast2(z1), rb = bcast2(r1);
+#pragma unroll
+      for (int i = 0; i < 32; i++) {
+        const float2 u = qfast2<BITS>(w[i], i < 16 ? za : zb, i < 16 ? ra : rb, bad);
+        put_code<BITS>(wds, 2 * i, __float_as_uint(u.x));
+        put_code<BITS>(wds, 2 * i + 1, __float_as_uint(u.y));
+      }
+    }
+    if (__any_sync(kFull, bad)) {
+      if (bad) {
+#pragma unroll
+        for (int j = 0; j < 2 * BITS; j++) wds[j] = 0u;
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+          const float z = i < 16 ? z0 : z1, sc = i < 16 ? s0 : s1;
+          put_code<BITS>(wds, 2 * i, qexact<BITS>(w[i].x, z, sc));
+          put_code<BITS>(wds, 2 * i + 1, qexact<BITS>(w[i].y, z, sc));
+        }
+      }
+    }
     if (valid) {
-      flags |= fl;
-      store_words<BITS>(P.codes + (size_t)R * row_code_bytes + 4 * BITS * part, wds);
-      if ((part & (gl - 1)) == 0)
-        *reinterpret_cast<uint32_t *>(P.meta + ((size_t)R * groups_per_row + part / gl) * 4) = meta;
+      flags |= f0 | f1;
+      uint8_t *dst = P.codes + (size_t)R * (kHeadDim * BITS / 8) + 8 * BITS * half;
+      if constexpr ((2 * BITS) % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < 2 * BITS; j += 4)
+          *reinterpret_cast<uint4 *>(dst + 4 * j) = make_uint4(wds[j], wds[j + 1], wds[j + 2], wds[j + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 2 * BITS; j += 2) *reinterpret_cast<uint2 *>(dst + 4 * j) = make_uint2(wds[j], wds[j + 1]);
+      }
+      uint32_t *mp = reinterpret_cast<uint32_t *>(P.meta);
+      if (G == 32) *reinterpret_cast<uint2 *>(mp + (size_t)R * 4 + 2 * half) = make_uint2(meta0, meta1);
+      else if (G == 64) mp[(size_t)R * 2 + half] = meta0;
+      else if (half == 0) mp[R] = meta0;
     }
   }
   if (flags) atomicOr(P.status, flags);
@@ -461,34 +562,39 @@ __device__ __forceinline__ void ktile_issue(const QuantParams &P, uint32_t tile,
   cp_async_commit_q();
 }
 
+// 16 codes (BITS each) -> the channel's 2*BITS bytes inside its record.
 template <int BITS>
-__device__ __forceinline__ void store_codes16(uint8_t *dst, const uint32_t (&q)[16]) {
+__device__ __forceinline__ void store_code_words(uint8_t *dst, const uint32_t (&w)[(16 * BITS + 31) / 32]) {
   if constexpr (BITS == 2) {
-    uint32_t w = 0;
-#pragma unroll
-    for (int i = 0; i < 16; i++) w |= q[i] << (2 * i);
-    *reinterpret_cast<uint32_t *>(dst) = w;
+    *reinterpret_cast<uint32_t *>(dst) = w[0];
   } else if constexpr (BITS == 4) {
-    uint32_t a = 0, b = 0;
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-      a |= q[i] << (4 * i);
-      b |= q[i + 8] << (4 * i);
-    }
-    *reinterpret_cast<uint2 *>(dst) = make_uint2(a, b);
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
   } else if constexpr (BITS == 8) {
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; j++) w[j] = q[4 * j] | (q[4 * j + 1] << 8) | (q[4 * j + 2] << 16) | (q[4 * j + 3] << 24);
     *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-  } else {  // 3 bits: 48 bits = three 16-bit halves (2-byte aligned)
-    uint64_t v = 0;
-#pragma unroll
-    for (int i = 0; i < 16; i++) v |= (uint64_t)q[i] << (3 * i);
+  } else {  // 48 bits, 2-byte aligned
     uint16_t *d16 = reinterpret_cast<uint16_t *>(dst);
-    d16[0] = (uint16_t)v;
-    d16[1] = (uint16_t)(v >> 16);
-    d16[2] = (uint16_t)(v >> 32);
+    d16[0] = (uint16_t)w[0];
+    d16[1] = (uint16_t)(w[0] >> 16);
+    d16[2] = (uint16_t)w[1];
+  }
+}
+
+// In-lane butterflies of 32 channels held as 16 pairs: stride 1 within pairs, 2..16 between pairs.
+__device__ __forceinline__ void fwht32_pairs(float2 (&w)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; i++) {
+    const float a = w[i].x, b = w[i].y;
+    w[i] = make_float2(__fadd_rn(a, b), __fsub_rn(a, b));
+  }
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; i++)
+      if ((i & h) == 0) {
+        const float2 a = w[i], b = w[i + h];
+        w[i] = add2(a, b);
+        w[i + h] = sub2(a, b);
+      }
   }
 }
 
@@ -505,6 +611,7 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_ktile(const QuantParams P
   const uint32_t H = P.g.H, T = P.g.T, n_sb = P.n_sb, G = P.group;
   const uint32_t n_tiles = P.g.L * H * n_sb;
   const int rg = tid >> 4, c8 = tid & 15;
+  const bool smooth = P.smooth != 0;
   uint32_t flags = 0;
 
   uint32_t tile = blockIdx.x;
@@ -514,38 +621,62 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_ktile(const QuantParams P
     const uint32_t t0 = sb * kSmoothBlock;
     const uint32_t nvalid = min((uint32_t)kSmoothBlock, T - t0);
 
-    // ---- A: own staged rows -> registers; then start fetching the next tile
+    // ---- A: own staged rows -> registers (8 rows x 4 channel pairs); prefetch the next tile
     cp_async_wait_all_q();
-    float x[8][8];
+    float2 x[8][4];
 #pragma unroll
     for (int i = 0; i < 8; i++) {
       const uint32_t r = rg + 16 * i;
       uint4 w = make_uint4(0u, 0u, 0u, 0u);
       if (r < nvalid) w = *reinterpret_cast<const uint4 *>(stage + r * 256 + 16 * c8);
-      unpack8(w, bf16, x[i]);
-      if (!all_finite8(x[i])) flags |= KVC_FLAG_NONFINITE;
+      x[i][0] = unpack_pair(w.x, bf16);
+      x[i][1] = unpack_pair(w.y, bf16);
+      x[i][2] = unpack_pair(w.z, bf16);
+      x[i][3] = unpack_pair(w.w, bf16);
     }
     if (tile + gridDim.x < n_tiles) ktile_issue(P, tile + gridDim.x, stage, rg, c8, flags);
 
-    if (P.smooth) {
+    if (smooth) {
+      // per-channel min / max over the valid rows (rows past the end repeat row rg)
       float mn[8], mx[8];
 #pragma unroll
-      for (int j = 0; j < 8; j++) {
-        mn[j] = __int_as_float(0x7f800000);
-        mx[j] = __int_as_float(0xff800000);
+      for (int j = 0; j < 4; j++) {
+        mn[2 * j] = mx[2 * j] = x[0][j].x;
+        mn[2 * j + 1] = mx[2 * j + 1] = x[0][j].y;
       }
+      if (nvalid >= 128) {
 #pragma unroll
-      for (int i = 0; i < 8; i++)
-        if (rg + 16 * i < nvalid)
+        for (int i = 1; i < 8; i += 2)
 #pragma unroll
-          for (int j = 0; j < 8; j++) {
-            mn[j] = fminf(mn[j], x[i][j]);
-            mx[j] = fmaxf(mx[j], x[i][j]);
+          for (int j = 0; j < 4; j++) {
+            mn[2 * j] = fmin3_n(mn[2 * j], x[i][j].x, x[i + 1 < 8 ? i + 1 : i][j].x);
+            mx[2 * j] = fmax3_n(mx[2 * j], x[i][j].x, x[i + 1 < 8 ? i + 1 : i][j].x);
+            mn[2 * j + 1] = fmin3_n(mn[2 * j + 1], x[i][j].y, x[i + 1 < 8 ? i + 1 : i][j].y);
+            mx[2 * j + 1] = fmax3_n(mx[2 * j + 1], x[i][j].y, x[i + 1 < 8 ? i + 1 : i][j].y);
           }
+      } else {
+#pragma unroll
+        for (int i = 1; i < 8; i++)
+          if (rg + 16 * i < (int)nvalid)
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+              mn[2 * j] = fmin_n(mn[2 * j], x[i][j].x);
+              mx[2 * j] = fmax_n(mx[2 * j], x[i][j].x);
+              mn[2 * j + 1] = fmin_n(mn[2 * j + 1], x[i][j].y);
+              mx[2 * j + 1] = fmax_n(mx[2 * j + 1], x[i][j].y);
+            }
+      }
+      // rows >= nvalid hold zeros: a half-warp whose row rg is past the end must not contribute
+      const bool has_rows = (uint32_t)rg < nvalid;
 #pragma unroll
       for (int j = 0; j < 8; j++) {
-        mn[j] = fminf(mn[j], __shfl_xor_sync(kFull, mn[j], 16));
-        mx[j] = fmaxf(mx[j], __shfl_xor_sync(kFull, mx[j], 16));
+        float a = mn[j], b = mx[j];
+        const float oa = __shfl_xor_sync(kFull, a, 16), ob = __shfl_xor_sync(kFull, b, 16);
+        const bool other = (uint32_t)(rg ^ 1) < nvalid;
+        if (!has_rows) { a = oa; b = ob; }
+        else if (other) { a = fmin_n(a, oa); b = fmax_n(b, ob); }
+        mn[j] = a;
+        mx[j] = b;
       }
       if (lane < 16) {
         reinterpret_cast<float4 *>(red + warp * 128 + 8 * c8)[0] = make_float4(mn[0], mn[1], mn[2], mn[3]);
@@ -555,16 +686,21 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_ktile(const QuantParams P
       }
       __syncthreads();
       if (tid < 128) {
+        // warp k holds rows 2k, 2k+1, 2k+16, ...: it has data iff row 2k is valid
         float a = red[tid], b = red[1024 + tid];
-#pragma unroll
         for (int k = 1; k < 8; k++) {
-          a = fminf(a, red[k * 128 + tid]);
-          b = fmaxf(b, red[1024 + k * 128 + tid]);
+          if (2 * k < (int)nvalid) {
+            a = fmin_n(a, red[k * 128 + tid]);
+            b = fmax_n(b, red[1024 + k * 128 + tid]);
+          }
         }
+        if (!finite2(a, b)) flags |= KVC_FLAG_NONFINITE;
         float mu, inv;
         uint32_t mub;
         int e;
         smooth_params(a, b, mu, inv, mub, e, flags);
+        // the Hadamard sign of the channel folds into the exact power-of-two scale
+        if (HAD && ((P.sign[tid >> 5] >> (tid & 31)) & 1u)) inv = -inv;
         mu_s[tid] = mu;
         inv_s[tid] = inv;
         const size_t cell = ((size_t)lh * n_sb + sb) * kHeadDim + tid;
@@ -576,23 +712,30 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_ktile(const QuantParams P
       const float4 m1 = reinterpret_cast<const float4 *>(mu_s + 8 * c8)[1];
       const float4 s0 = reinterpret_cast<const float4 *>(inv_s + 8 * c8)[0];
       const float4 s1 = reinterpret_cast<const float4 *>(inv_s + 8 * c8)[1];
-      const float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-      const float iv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+      const float2 m[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
+                           make_float2(m1.z, m1.w)};
+      const float2 iv[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
+                            make_float2(s1.z, s1.w)};
 #pragma unroll
       for (int i = 0; i < 8; i++)
 #pragma unroll
-        for (int j = 0; j < 8; j++) x[i][j] = (rg + 16 * i < nvalid) ? __fmul_rn(__fsub_rn(x[i][j], m[j]), iv[j]) : 0.0f;
+        for (int j = 0; j < 4; j++) x[i][j] = mul2(sub2(x[i][j], m[j]), iv[j]);
+#pragma unroll
+      for (int i = 0; i < 8; i++)
+        if (rg + 16 * i >= (int)nvalid)
+#pragma unroll
+          for (int j = 0; j < 4; j++) x[i][j] = make_float2(0.0f, 0.0f);
     }
 #pragma unroll
     for (int i = 0; i < 8; i++) {
       const int r = rg + 16 * i;
       float4 *row = reinterpret_cast<float4 *>(Y + r * 128);
-      row[kchunk(2 * c8, r)] = make_float4(x[i][0], x[i][1], x[i][2], x[i][3]);
-      row[kchunk(2 * c8 + 1, r)] = make_float4(x[i][4], x[i][5], x[i][6], x[i][7]);
+      row[kchunk(2 * c8, r)] = make_float4(x[i][0].x, x[i][0].y, x[i][1].x, x[i][1].y);
+      row[kchunk(2 * c8 + 1, r)] = make_float4(x[i][2].x, x[i][2].y, x[i][3].x, x[i][3].y);
     }
     __syncthreads();
 
-    // ---- C: butterfly strides 1..16 along each row
+    // ---- C: butterfly strides 1..16 along each row (signs already applied when smoothing)
     if (HAD) {
       const int part = lane & 3, rsub = lane >> 2;
       const uint32_t sbits = P.sign[part];
@@ -601,56 +744,72 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_ktile(const QuantParams P
         const int r = warp * 16 + k * 8 + rsub;
         float4 *row = reinterpret_cast<float4 *>(Y + r * 128) + 8 * part;
         const int rot = (part + 4 * (r & 1)) & 7;
-        float v[32];
+        float2 w[16];
 #pragma unroll
         for (int q = 0; q < 8; q++) {
           const float4 a = row[(q + rot) & 7];
-          v[4 * q] = a.x; v[4 * q + 1] = a.y; v[4 * q + 2] = a.z; v[4 * q + 3] = a.w;
+          w[2 * q] = make_float2(a.x, a.y);
+          w[2 * q + 1] = make_float2(a.z, a.w);
         }
-        apply_signs(v, sbits);
-        fwht_in_thread(v);
+        if (!smooth) {
 #pragma unroll
-        for (int q = 0; q < 8; q++) row[(q + rot) & 7] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          for (int i = 0; i < 16; i++) {
+            w[i].x = __uint_as_float(__float_as_uint(w[i].x) ^ (((sbits >> (2 * i)) & 1u) << 31));
+            w[i].y = __uint_as_float(__float_as_uint(w[i].y) ^ (((sbits >> (2 * i + 1)) & 1u) << 31));
+          }
+        }
+        fwht32_pairs(w);
+#pragma unroll
+        for (int q = 0; q < 8; q++)
+          row[(q + rot) & 7] = make_float4(w[2 * q].x, w[2 * q].y, w[2 * q + 1].x, w[2 * q + 1].y);
       }
       __syncthreads();
     }
 
-    // ---- D: columns {cq, cq+32, cq+64, cq+96} x tokens 16*warp .. +15
+    // ---- D: columns {cq, cq+32, cq+64, cq+96} x tokens 16*warp .. +15 (rows in pairs)
     {
       const int cq = lane, rs = warp;
-      float v[4][16];
+      float2 v[4][8];
 #pragma unroll
-      for (int i = 0; i < 16; i++) {
-        const int r = 16 * rs + i;
+      for (int i = 0; i < 8; i++) {
+        const int r = 16 * rs + 2 * i;
 #pragma unroll
-        for (int k = 0; k < 4; k++) v[k][i] = Y[r * 128 + kcol(cq + 32 * k, r)];
+        for (int k = 0; k < 4; k++)
+          v[k][i] = make_float2(Y[r * 128 + kcol(cq + 32 * k, r)], Y[(r + 1) * 128 + kcol(cq + 32 * k, r + 1)]);
       }
       if (HAD) {
-        const float c = hadamard_scale();
+        const float2 c2 = bcast2(hadamard_scale());
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-          const float a0 = __fadd_rn(v[0][i], v[1][i]), a1 = __fsub_rn(v[0][i], v[1][i]);
-          const float a2 = __fadd_rn(v[2][i], v[3][i]), a3 = __fsub_rn(v[2][i], v[3][i]);
-          v[0][i] = __fmul_rn(__fadd_rn(a0, a2), c);
-          v[2][i] = __fmul_rn(__fsub_rn(a0, a2), c);
-          v[1][i] = __fmul_rn(__fadd_rn(a1, a3), c);
-          v[3][i] = __fmul_rn(__fsub_rn(a1, a3), c);
+        for (int i = 0; i < 8; i++) {
+          const float2 a0 = add2(v[0][i], v[1][i]), a1 = sub2(v[0][i], v[1][i]);
+          const float2 a2 = add2(v[2][i], v[3][i]), a3 = sub2(v[2][i], v[3][i]);
+          v[0][i] = mul2(add2(a0, a2), c2);
+          v[2][i] = mul2(sub2(a0, a2), c2);
+          v[1][i] = mul2(add2(a1, a3), c2);
+          v[3][i] = mul2(sub2(a1, a3), c2);
         }
       }
       const int nv = (int)nvalid - 16 * rs;  // valid rows in this segment (may be <= 0)
-      float mn[4], mx[4];
 #pragma unroll
       for (int k = 0; k < 4; k++) {
-        mn[k] = __int_as_float(0x7f800000);
-        mx[k] = __int_as_float(0xff800000);
+        float a = fmin_n(v[k][0].x, v[k][0].y), b = fmax_n(v[k][0].x, v[k][0].y);
+        if (nv >= 16) {
 #pragma unroll
-        for (int i = 0; i < 16; i++)
-          if (i < nv) {
-            mn[k] = fminf(mn[k], v[k][i]);
-            mx[k] = fmaxf(mx[k], v[k][i]);
+          for (int i = 1; i < 8; i++) {
+            a = fmin3_n(a, v[k][i].x, v[k][i].y);
+            b = fmax3_n(b, v[k][i].x, v[k][i].y);
           }
-        red[rs * 128 + cq + 32 * k] = mn[k];
-        red[1024 + rs * 128 + cq + 32 * k] = mx[k];
+        } else {
+          a = v[k][0].x;
+          b = a;
+#pragma unroll
+          for (int i = 0; i < 8; i++) {
+            if (2 * i < nv) { a = fmin_n(a, v[k][i].x); b = fmax_n(b, v[k][i].x); }
+            if (2 * i + 1 < nv) { a = fmin_n(a, v[k][i].y); b = fmax_n(b, v[k][i].y); }
+          }
+        }
+        red[rs * 128 + cq + 32 * k] = a;
+        red[1024 + rs * 128 + cq + 32 * k] = b;
       }
       __syncthreads();
       const int spg = (int)(G >> 4);           // 16-token segments per group
@@ -658,21 +817,53 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_ktile(const QuantParams P
       const uint32_t row0 = 16 * rs;
       const uint32_t tg = (t0 + (uint32_t)s0 * 16) / G;
       if (tg < P.n_tg) {
+        const int nseg = min(spg, (int)((nvalid + 15) / 16) - s0);  // segments of the group holding rows
 #pragma unroll
         for (int k = 0; k < 4; k++) {
           const int ch = cq + 32 * k;
           float a = red[s0 * 128 + ch], b = red[1024 + s0 * 128 + ch];
-          for (int s = 1; s < spg; s++) {
-            a = fminf(a, red[(s0 + s) * 128 + ch]);
-            b = fmaxf(b, red[1024 + (s0 + s) * 128 + ch]);
+          for (int sg = 1; sg < nseg; sg++) {
+            a = fmin_n(a, red[(s0 + sg) * 128 + ch]);
+            b = fmax_n(b, red[1024 + (s0 + sg) * 128 + ch]);
           }
+          if (!finite2(a, b)) flags |= KVC_FLAG_NONFINITE;
           float sc, z, rr;
-          const uint32_t meta = quant_params<BITS>(a, b, sc, z, rr, flags);
-          uint32_t q[16];
+          uint32_t fl = 0;
+          const uint32_t meta = quant_params<BITS>(a, b, sc, z, rr, fl);
+          flags |= fl;
+          bool bad = fl != 0;
+          uint32_t cw[(16 * BITS + 31) / 32];
 #pragma unroll
-          for (int i = 0; i < 16; i++) q[i] = i < nv ? quant_code<BITS>(v[k][i], z, sc, rr) : 0u;
+          for (int j = 0; j < (16 * BITS + 31) / 32; j++) cw[j] = 0u;
+          const float2 z2 = bcast2(z), r2 = bcast2(rr);
+#pragma unroll
+          for (int i = 0; i < 8; i++) {
+            const float2 u = qfast2<BITS>(v[k][i], z2, r2, bad);
+            put_code<BITS>(cw, 2 * i, __float_as_uint(u.x));
+            put_code<BITS>(cw, 2 * i + 1, __float_as_uint(u.y));
+          }
+          if (__any_sync(kFull, bad)) {
+            if (bad) {
+#pragma unroll
+              for (int j = 0; j < (16 * BITS + 31) / 32; j++) cw[j] = 0u;
+#pragma unroll
+              for (int i = 0; i < 8; i++) {
+                put_code<BITS>(cw, 2 * i, qexact<BITS>(v[k][i].x, z, sc));
+                put_code<BITS>(cw, 2 * i + 1, qexact<BITS>(v[k][i].y, z, sc));
+              }
+            }
+          }
+          if (nv < 16) {  // codes of rows past the end are 0
+            const int keep = nv > 0 ? nv * BITS : 0;
+#pragma unroll
+            for (int j = 0; j < (16 * BITS + 31) / 32; j++) {
+              const int lo = 32 * j;
+              if (keep <= lo) cw[j] = 0u;
+              else if (keep < lo + 32) cw[j] &= (1u << (keep - lo)) - 1u;
+            }
+          }
           const size_t g = ((size_t)lh * P.n_tg + tg) * kHeadDim + ch;
-          store_codes16<BITS>(P.codes + g * (G * BITS / 8) + ((row0 % G) / 16) * (2 * BITS), q);
+          store_code_words<BITS>(P.codes + g * (G * BITS / 8) + ((row0 % G) / 16) * (2 * BITS), cw);
           if (row0 % G == 0) *reinterpret_cast<uint32_t *>(P.meta + g * 4) = meta;
         }
       }
@@ -820,7 +1011,7 @@ static int run(K kernel, bool tile, const QuantParams &p, int sm_count, void *st
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
   }
-  const uint64_t want = tile ? work_units : (work_units + 7) / 8;  // tiles, or CTAs of 8 warps x 8 rows
+  const uint64_t want = work_units;  // tiles, or CTAs of 8 warps
   uint64_t blocks = (uint64_t)sm_count * resident_blocks(kernel, smem);
   if (want < blocks) blocks = want;
   if (blocks == 0) return 0;
@@ -833,7 +1024,8 @@ static bool use_tile(const QuantParams &p) { return p.smooth || p.axis == KVC_AX
 template <int BITS>
 static int dispatch(const QuantParams &p, bool had, bool enc, int sm, void *st, const char **name) {
   const bool tile = use_tile(p);
-  const uint64_t units = tile ? (uint64_t)p.g.L * p.g.H * p.n_sb : ((uint64_t)p.g.L * p.g.T * p.g.H + 7) / 8;
+  const uint64_t rows = (uint64_t)p.g.L * p.g.T * p.g.H;
+  const uint64_t units = tile ? (uint64_t)p.g.L * p.g.H * p.n_sb : (enc ? (rows + 127) / 128 : (rows + 63) / 64);
   if (enc) {
     if (p.axis == KVC_AXIS_OVER_TOKENS) {
       *name = "kvc_enc_ktile";
