@@ -81,12 +81,12 @@ __device__ __forceinline__ void put_code(uint32_t (&w)[NW], int idx, uint32_t c)
   if (sh + BITS > 32) w[wi + 1] |= (c & M) >> (32 - sh);
 }
 
-template <int BITS, bool HAD>
+template <int BITS, bool HAD, bool BF16>
 __global__ void __launch_bounds__(kThreads, 2) kvc_enc_rows(const QuantParams P) {
   __shared__ uint32_t smask[2][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int half = lane & 1, rsub = lane >> 1;
-  const bool bf16 = P.g.bf16 != 0;
+  constexpr bool bf16 = BF16;
   const uint32_t H = P.g.H, T = P.g.T;
   const uint32_t NR = P.g.L * T * H;
   const uint32_t n_it = (NR + 15) / 16;
@@ -598,35 +598,106 @@ __device__ __forceinline__ void fwht32_pairs(float2 (&w)[16]) {
   }
 }
 
-template <int BITS, bool HAD>
-__global__ void __launch_bounds__(kThreads, 2) kvc_enc_ktile(const QuantParams P) {
+// Key tile with 512 threads (kvc_enc_ktile): per (layer, head, 128-token) tile
+//  A  thread (rg = tid/16, c8 = tid%16) takes rows rg + 32i (i < 4) x 8 channels
+//     from the stage buffer; smoothing statistics combine through the idle tile
+//     buffer; the smoothed rows (signs folded into the power-of-two scale) go to Y;
+//  C  one row per lane quarter-warp: butterfly strides 1..16 in registers;
+//  D  thread (cq = lane, rs = warp) takes channels {cq + 32k} x rows 8rs .. 8rs+7:
+//     strides 32/64 and the normalization in registers, per-channel statistics of
+//     its 8 rows; one thread per (group, channel) then turns the segment partials
+//     into the group's parameters (written once to a shared table and to the
+//     metadata section); every thread quantizes and packs its 8 codes per channel.
+constexpr int kKT = 512;
+constexpr size_t kKtile3Smem = (size_t)128 * 128 * 4 + 128 * 256 + 4 * 128 * 16 + 2 * 128 * 4;
+
+__device__ __forceinline__ void ktile3_issue(const QuantParams &P, uint32_t tile, uint8_t *stage, int rg, int c8,
+                                             uint32_t &flags) {
+  const uint32_t n_sb = P.n_sb, H = P.g.H;
+  const uint32_t sb = tile % n_sb, lh = tile / n_sb, h = lh % H, l = lh / H;
+  const uint32_t t0 = sb * kSmoothBlock, nvalid = min((uint32_t)kSmoothBlock, P.g.T - t0);
+  const uint8_t *lbase = static_cast<const uint8_t *>(P.layers[l]) + (size_t)(h * kHeadDim + 8 * c8) * 2;
+  uint8_t *dst = stage + rg * 256 + 16 * c8;
+  if (!P.g.block_table) {
+    const uint64_t ts = P.g.token_stride;
+    const uint8_t *src = lbase + (uint64_t)(t0 + rg) * ts;
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+      if (rg + 32 * i < (int)nvalid) cp_async16_q(dst + i * 32 * 256, src + (uint64_t)i * 32 * ts);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const uint32_t r = rg + 32 * i;
+      if (r < nvalid) {
+        const uint64_t ro = row_offset(P.g, t0 + r);
+        if (ro == ~0ull) {
+          flags |= KVC_FLAG_BAD_PAGE;
+          *reinterpret_cast<uint4 *>(dst + i * 32 * 256) = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          cp_async16_q(dst + i * 32 * 256, lbase + ro);
+        }
+      }
+    }
+  }
+  cp_async_commit_q();
+}
+
+template <int BITS>
+__device__ __forceinline__ void store_codes8(uint8_t *dst, uint32_t lo, uint32_t hi) {
+  if constexpr (BITS == 2) *reinterpret_cast<uint16_t *>(dst) = (uint16_t)lo;
+  else if constexpr (BITS == 4) *reinterpret_cast<uint32_t *>(dst) = lo;
+  else if constexpr (BITS == 8) *reinterpret_cast<uint2 *>(dst) = make_uint2(lo, hi);
+  else {
+    dst[0] = (uint8_t)lo;
+    dst[1] = (uint8_t)(lo >> 8);
+    dst[2] = (uint8_t)(lo >> 16);
+  }
+}
+
+template <int BITS, bool HAD, bool BF16>
+__global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P) {
   extern __shared__ float4 smem_f4[];
-  float *Y = reinterpret_cast<float *>(smem_f4);                           // [128][128], swizzled
-  uint8_t *stage = reinterpret_cast<uint8_t *>(Y + 128 * 128);              // [128][256] raw rows
-  float *red = reinterpret_cast<float *>(stage + 128 * 256);               // [2][8][128]
-  float *mu_s = red + 2 * 8 * 128;
+  float *Y = reinterpret_cast<float *>(smem_f4);                       // [128][128] swizzled; also reduction space
+  uint8_t *stage = reinterpret_cast<uint8_t *>(Y + 128 * 128);          // [128][256] raw rows of the next tile
+  float4 *prm = reinterpret_cast<float4 *>(stage + 128 * 256);          // [4 groups][128] {z, r, s, meta}
+  float *mu_s = reinterpret_cast<float *>(prm + 4 * 128);
   float *inv_s = mu_s + 128;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool bf16 = P.g.bf16 != 0;
+  constexpr bool bf16 = BF16;
   const uint32_t H = P.g.H, T = P.g.T, n_sb = P.n_sb, G = P.group;
   const uint32_t n_tiles = P.g.L * H * n_sb;
   const int rg = tid >> 4, c8 = tid & 15;
   const bool smooth = P.smooth != 0;
   uint32_t flags = 0;
 
+  // tile-invariant quantities
+  const int spg = (int)(G >> 3);                      // 8-row segments per group
+  const int tiles_groups = 128 / (int)G;              // token groups per tile
+  const int my_gi = (8 * warp) / (int)G;              // phase-D group of this warp's rows
+  const uint32_t rec_bytes = G * BITS / 8;
+  const uint32_t my_seg_off = (uint32_t)(((8 * warp) % (int)G) / 8) * BITS;
+  const int chA = kchunk(2 * c8, rg), chB = kchunk(2 * c8 + 1, rg);  // phase-A store chunks (rg parity fixed)
+  // phase-D column offsets: channel cq + 32k of an even / odd row
+  int coff[8];
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    coff[2 * k] = kcol(lane + 32 * k, 0);
+    coff[2 * k + 1] = kcol(lane + 32 * k, 1);
+  }
+
   uint32_t tile = blockIdx.x;
-  if (tile < n_tiles) ktile_issue(P, tile, stage, rg, c8, flags);
+  if (tile < n_tiles) ktile3_issue(P, tile, stage, rg, c8, flags);
   for (; tile < n_tiles; tile += gridDim.x) {
     const uint32_t sb = tile % n_sb, lh = tile / n_sb;
     const uint32_t t0 = sb * kSmoothBlock;
     const uint32_t nvalid = min((uint32_t)kSmoothBlock, T - t0);
 
-    // ---- A: own staged rows -> registers (8 rows x 4 channel pairs); prefetch the next tile
+    // ---- A
     cp_async_wait_all_q();
-    float2 x[8][4];
+    float2 x[4][4];
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-      const uint32_t r = rg + 16 * i;
+    for (int i = 0; i < 4; i++) {
+      const uint32_t r = rg + 32 * i;
       uint4 w = make_uint4(0u, 0u, 0u, 0u);
       if (r < nvalid) w = *reinterpret_cast<const uint4 *>(stage + r * 256 + 16 * c8);
       x[i][0] = unpack_pair(w.x, bf16);
@@ -634,30 +705,31 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_ktile(const QuantParams P
       x[i][2] = unpack_pair(w.z, bf16);
       x[i][3] = unpack_pair(w.w, bf16);
     }
-    if (tile + gridDim.x < n_tiles) ktile_issue(P, tile + gridDim.x, stage, rg, c8, flags);
+    if (tile + gridDim.x < n_tiles) ktile3_issue(P, tile + gridDim.x, stage, rg, c8, flags);
 
     if (smooth) {
-      // per-channel min / max over the valid rows (rows past the end repeat row rg)
       float mn[8], mx[8];
 #pragma unroll
       for (int j = 0; j < 4; j++) {
         mn[2 * j] = mx[2 * j] = x[0][j].x;
         mn[2 * j + 1] = mx[2 * j + 1] = x[0][j].y;
       }
-      if (nvalid >= 128) {
+      if (nvalid == 128) {
 #pragma unroll
-        for (int i = 1; i < 8; i += 2)
-#pragma unroll
-          for (int j = 0; j < 4; j++) {
-            mn[2 * j] = fmin3_n(mn[2 * j], x[i][j].x, x[i + 1 < 8 ? i + 1 : i][j].x);
-            mx[2 * j] = fmax3_n(mx[2 * j], x[i][j].x, x[i + 1 < 8 ? i + 1 : i][j].x);
-            mn[2 * j + 1] = fmin3_n(mn[2 * j + 1], x[i][j].y, x[i + 1 < 8 ? i + 1 : i][j].y);
-            mx[2 * j + 1] = fmax3_n(mx[2 * j + 1], x[i][j].y, x[i + 1 < 8 ? i + 1 : i][j].y);
-          }
+        for (int j = 0; j < 4; j++) {
+          mn[2 * j] = fmin3_n(mn[2 * j], x[1][j].x, x[2][j].x);
+          mn[2 * j] = fmin_n(mn[2 * j], x[3][j].x);
+          mx[2 * j] = fmax3_n(mx[2 * j], x[1][j].x, x[2][j].x);
+          mx[2 * j] = fmax_n(mx[2 * j], x[3][j].x);
+          mn[2 * j + 1] = fmin3_n(mn[2 * j + 1], x[1][j].y, x[2][j].y);
+          mn[2 * j + 1] = fmin_n(mn[2 * j + 1], x[3][j].y);
+          mx[2 * j + 1] = fmax3_n(mx[2 * j + 1], x[1][j].y, x[2][j].y);
+          mx[2 * j + 1] = fmax_n(mx[2 * j + 1], x[3][j].y);
+        }
       } else {
 #pragma unroll
-        for (int i = 1; i < 8; i++)
-          if (rg + 16 * i < (int)nvalid)
+        for (int i = 1; i < 4; i++)
+          if (rg + 32 * i < (int)nvalid)
 #pragma unroll
             for (int j = 0; j < 4; j++) {
               mn[2 * j] = fmin_n(mn[2 * j], x[i][j].x);
@@ -666,32 +738,27 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_ktile(const QuantParams P
               mx[2 * j + 1] = fmax_n(mx[2 * j + 1], x[i][j].y);
             }
       }
-      // rows >= nvalid hold zeros: a half-warp whose row rg is past the end must not contribute
-      const bool has_rows = (uint32_t)rg < nvalid;
+      const bool mine = rg < (int)nvalid, other = (rg ^ 1) < (int)nvalid;
 #pragma unroll
       for (int j = 0; j < 8; j++) {
-        float a = mn[j], b = mx[j];
-        const float oa = __shfl_xor_sync(kFull, a, 16), ob = __shfl_xor_sync(kFull, b, 16);
-        const bool other = (uint32_t)(rg ^ 1) < nvalid;
-        if (!has_rows) { a = oa; b = ob; }
-        else if (other) { a = fmin_n(a, oa); b = fmax_n(b, ob); }
-        mn[j] = a;
-        mx[j] = b;
+        const float oa = __shfl_xor_sync(kFull, mn[j], 16), ob = __shfl_xor_sync(kFull, mx[j], 16);
+        if (!mine) { mn[j] = oa; mx[j] = ob; }
+        else if (other) { mn[j] = fmin_n(mn[j], oa); mx[j] = fmax_n(mx[j], ob); }
       }
+      float *red = Y;  // [16 warps][128] minima, then maxima
       if (lane < 16) {
         reinterpret_cast<float4 *>(red + warp * 128 + 8 * c8)[0] = make_float4(mn[0], mn[1], mn[2], mn[3]);
         reinterpret_cast<float4 *>(red + warp * 128 + 8 * c8)[1] = make_float4(mn[4], mn[5], mn[6], mn[7]);
-        reinterpret_cast<float4 *>(red + 1024 + warp * 128 + 8 * c8)[0] = make_float4(mx[0], mx[1], mx[2], mx[3]);
-        reinterpret_cast<float4 *>(red + 1024 + warp * 128 + 8 * c8)[1] = make_float4(mx[4], mx[5], mx[6], mx[7]);
+        reinterpret_cast<float4 *>(red + 2048 + warp * 128 + 8 * c8)[0] = make_float4(mx[0], mx[1], mx[2], mx[3]);
+        reinterpret_cast<float4 *>(red + 2048 + warp * 128 + 8 * c8)[1] = make_float4(mx[4], mx[5], mx[6], mx[7]);
       }
       __syncthreads();
       if (tid < 128) {
-        // warp k holds rows 2k, 2k+1, 2k+16, ...: it has data iff row 2k is valid
-        float a = red[tid], b = red[1024 + tid];
-        for (int k = 1; k < 8; k++) {
-          if (2 * k < (int)nvalid) {
+        float a = red[tid], b = red[2048 + tid];
+        for (int k = 1; k < 16; k++) {
+          if (2 * k < (int)nvalid) {  // warp k holds rows 2k, 2k+1, 2k+32, ...
             a = fmin_n(a, red[k * 128 + tid]);
-            b = fmax_n(b, red[1024 + k * 128 + tid]);
+            b = fmax_n(b, red[2048 + k * 128 + tid]);
           }
         }
         if (!finite2(a, b)) flags |= KVC_FLAG_NONFINITE;
@@ -699,8 +766,7 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_ktile(const QuantParams P
         uint32_t mub;
         int e;
         smooth_params(a, b, mu, inv, mub, e, flags);
-        // the Hadamard sign of the channel folds into the exact power-of-two scale
-        if (HAD && ((P.sign[tid >> 5] >> (tid & 31)) & 1u)) inv = -inv;
+        if (HAD && ((P.sign[tid >> 5] >> (tid & 31)) & 1u)) inv = -inv;  // sign folded into the exact scale
         mu_s[tid] = mu;
         inv_s[tid] = inv;
         const size_t cell = ((size_t)lh * n_sb + sb) * kHeadDim + tid;
@@ -717,154 +783,166 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_ktile(const QuantParams P
       const float2 iv[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
                             make_float2(s1.z, s1.w)};
 #pragma unroll
-      for (int i = 0; i < 8; i++)
+      for (int i = 0; i < 4; i++)
 #pragma unroll
         for (int j = 0; j < 4; j++) x[i][j] = mul2(sub2(x[i][j], m[j]), iv[j]);
+      if (nvalid < 128) {
 #pragma unroll
-      for (int i = 0; i < 8; i++)
-        if (rg + 16 * i >= (int)nvalid)
+        for (int i = 0; i < 4; i++)
+          if (rg + 32 * i >= (int)nvalid)
 #pragma unroll
-          for (int j = 0; j < 4; j++) x[i][j] = make_float2(0.0f, 0.0f);
+            for (int j = 0; j < 4; j++) x[i][j] = make_float2(0.0f, 0.0f);
+      }
     }
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-      const int r = rg + 16 * i;
-      float4 *row = reinterpret_cast<float4 *>(Y + r * 128);
-      row[kchunk(2 * c8, r)] = make_float4(x[i][0].x, x[i][0].y, x[i][1].x, x[i][1].y);
-      row[kchunk(2 * c8 + 1, r)] = make_float4(x[i][2].x, x[i][2].y, x[i][3].x, x[i][3].y);
+    for (int i = 0; i < 4; i++) {
+      float4 *row = reinterpret_cast<float4 *>(Y + (rg + 32 * i) * 128);
+      row[chA] = make_float4(x[i][0].x, x[i][0].y, x[i][1].x, x[i][1].y);
+      row[chB] = make_float4(x[i][2].x, x[i][2].y, x[i][3].x, x[i][3].y);
     }
     __syncthreads();
 
-    // ---- C: butterfly strides 1..16 along each row (signs already applied when smoothing)
+    // ---- C
     if (HAD) {
-      const int part = lane & 3, rsub = lane >> 2;
-      const uint32_t sbits = P.sign[part];
-#pragma unroll 1
-      for (int k = 0; k < 2; k++) {
-        const int r = warp * 16 + k * 8 + rsub;
-        float4 *row = reinterpret_cast<float4 *>(Y + r * 128) + 8 * part;
-        const int rot = (part + 4 * (r & 1)) & 7;
-        float2 w[16];
+      const int part = lane & 3, r = warp * 8 + (lane >> 2);
+      float4 *row = reinterpret_cast<float4 *>(Y + r * 128) + 8 * part;
+      const int rot = (part + 4 * (r & 1)) & 7;
+      float2 w[16];
 #pragma unroll
-        for (int q = 0; q < 8; q++) {
-          const float4 a = row[(q + rot) & 7];
-          w[2 * q] = make_float2(a.x, a.y);
-          w[2 * q + 1] = make_float2(a.z, a.w);
-        }
-        if (!smooth) {
-#pragma unroll
-          for (int i = 0; i < 16; i++) {
-            w[i].x = __uint_as_float(__float_as_uint(w[i].x) ^ (((sbits >> (2 * i)) & 1u) << 31));
-            w[i].y = __uint_as_float(__float_as_uint(w[i].y) ^ (((sbits >> (2 * i + 1)) & 1u) << 31));
-          }
-        }
-        fwht32_pairs(w);
-#pragma unroll
-        for (int q = 0; q < 8; q++)
-          row[(q + rot) & 7] = make_float4(w[2 * q].x, w[2 * q].y, w[2 * q + 1].x, w[2 * q + 1].y);
+      for (int q = 0; q < 8; q++) {
+        const float4 a = row[(q + rot) & 7];
+        w[2 * q] = make_float2(a.x, a.y);
+        w[2 * q + 1] = make_float2(a.z, a.w);
       }
+      if (!smooth) {
+        const uint32_t sbits = P.sign[part];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+          w[i].x = __uint_as_float(__float_as_uint(w[i].x) ^ (((sbits >> (2 * i)) & 1u) << 31));
+          w[i].y = __uint_as_float(__float_as_uint(w[i].y) ^ (((sbits >> (2 * i + 1)) & 1u) << 31));
+        }
+      }
+      fwht32_pairs(w);
+#pragma unroll
+      for (int q = 0; q < 8; q++) row[(q + rot) & 7] = make_float4(w[2 * q].x, w[2 * q].y, w[2 * q + 1].x, w[2 * q + 1].y);
       __syncthreads();
     }
 
-    // ---- D: columns {cq, cq+32, cq+64, cq+96} x tokens 16*warp .. +15 (rows in pairs)
+    // ---- D1: 8 rows x 4 channels into registers, strides 32 / 64, per-channel partials
+    const int cq = lane, rs = warp;
+    const int nv = (int)nvalid - 8 * rs;
+    float2 v[4][4];
     {
-      const int cq = lane, rs = warp;
-      float2 v[4][8];
+      const float *Yr = Y + 8 * rs * 128;
 #pragma unroll
-      for (int i = 0; i < 8; i++) {
-        const int r = 16 * rs + 2 * i;
+      for (int i = 0; i < 4; i++)
 #pragma unroll
         for (int k = 0; k < 4; k++)
-          v[k][i] = make_float2(Y[r * 128 + kcol(cq + 32 * k, r)], Y[(r + 1) * 128 + kcol(cq + 32 * k, r + 1)]);
-      }
-      if (HAD) {
-        const float2 c2 = bcast2(hadamard_scale());
+          v[k][i] = make_float2(Yr[2 * i * 128 + coff[2 * k]], Yr[(2 * i + 1) * 128 + coff[2 * k + 1]]);
+    }
+    if (HAD) {
+      const float2 c2 = bcast2(hadamard_scale());
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-          const float2 a0 = add2(v[0][i], v[1][i]), a1 = sub2(v[0][i], v[1][i]);
-          const float2 a2 = add2(v[2][i], v[3][i]), a3 = sub2(v[2][i], v[3][i]);
-          v[0][i] = mul2(add2(a0, a2), c2);
-          v[2][i] = mul2(sub2(a0, a2), c2);
-          v[1][i] = mul2(add2(a1, a3), c2);
-          v[3][i] = mul2(sub2(a1, a3), c2);
+      for (int i = 0; i < 4; i++) {
+        const float2 a0 = add2(v[0][i], v[1][i]), a1 = sub2(v[0][i], v[1][i]);
+        const float2 a2 = add2(v[2][i], v[3][i]), a3 = sub2(v[2][i], v[3][i]);
+        v[0][i] = mul2(add2(a0, a2), c2);
+        v[2][i] = mul2(sub2(a0, a2), c2);
+        v[1][i] = mul2(add2(a1, a3), c2);
+        v[3][i] = mul2(sub2(a1, a3), c2);
+      }
+    }
+    float pmn[4], pmx[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      if (nv >= 8) {
+        pmn[k] = fmin3_n(fmin_n(v[k][0].x, v[k][0].y), v[k][1].x, v[k][1].y);
+        pmx[k] = fmax3_n(fmax_n(v[k][0].x, v[k][0].y), v[k][1].x, v[k][1].y);
+        pmn[k] = fmin3_n(fmin3_n(pmn[k], v[k][2].x, v[k][2].y), v[k][3].x, v[k][3].y);
+        pmx[k] = fmax3_n(fmax3_n(pmx[k], v[k][2].x, v[k][2].y), v[k][3].x, v[k][3].y);
+      } else {
+        pmn[k] = pmx[k] = v[k][0].x;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          if (2 * i < nv) { pmn[k] = fmin_n(pmn[k], v[k][i].x); pmx[k] = fmax_n(pmx[k], v[k][i].x); }
+          if (2 * i + 1 < nv) { pmn[k] = fmin_n(pmn[k], v[k][i].y); pmx[k] = fmax_n(pmx[k], v[k][i].y); }
         }
       }
-      const int nv = (int)nvalid - 16 * rs;  // valid rows in this segment (may be <= 0)
+    }
+    __syncthreads();  // every thread has read Y: its space holds the partials now
+    float *red = Y;   // [16 segments][128] minima at 0, maxima at 2048
 #pragma unroll
-      for (int k = 0; k < 4; k++) {
-        float a = fmin_n(v[k][0].x, v[k][0].y), b = fmax_n(v[k][0].x, v[k][0].y);
-        if (nv >= 16) {
-#pragma unroll
-          for (int i = 1; i < 8; i++) {
-            a = fmin3_n(a, v[k][i].x, v[k][i].y);
-            b = fmax3_n(b, v[k][i].x, v[k][i].y);
-          }
-        } else {
-          a = v[k][0].x;
-          b = a;
-#pragma unroll
-          for (int i = 0; i < 8; i++) {
-            if (2 * i < nv) { a = fmin_n(a, v[k][i].x); b = fmax_n(b, v[k][i].x); }
-            if (2 * i + 1 < nv) { a = fmin_n(a, v[k][i].y); b = fmax_n(b, v[k][i].y); }
-          }
-        }
-        red[rs * 128 + cq + 32 * k] = a;
-        red[1024 + rs * 128 + cq + 32 * k] = b;
-      }
-      __syncthreads();
-      const int spg = (int)(G >> 4);           // 16-token segments per group
-      const int s0 = (rs / spg) * spg;         // first segment of this thread's group
-      const uint32_t row0 = 16 * rs;
-      const uint32_t tg = (t0 + (uint32_t)s0 * 16) / G;
-      if (tg < P.n_tg) {
-        const int nseg = min(spg, (int)((nvalid + 15) / 16) - s0);  // segments of the group holding rows
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          const int ch = cq + 32 * k;
-          float a = red[s0 * 128 + ch], b = red[1024 + s0 * 128 + ch];
-          for (int sg = 1; sg < nseg; sg++) {
+    for (int k = 0; k < 4; k++) {
+      red[rs * 128 + cq + 32 * k] = pmn[k];
+      red[2048 + rs * 128 + cq + 32 * k] = pmx[k];
+    }
+    __syncthreads();
+
+    // ---- D2: one thread per (group, channel) of the tile
+    {
+      const int nseg_valid = (int)((nvalid + 7) / 8);
+      const uint32_t tg_base = sb * tiles_groups;    // first token group of the tile
+      for (int j = tid; j < tiles_groups * 128; j += kKT) {
+        const int gi = j >> 7, ch = j & 127;
+        const int s0 = gi * spg;
+        const uint32_t tg = tg_base + gi;
+        if (s0 < nseg_valid && tg < P.n_tg) {
+          float a = red[s0 * 128 + ch], b = red[2048 + s0 * 128 + ch];
+          const int ns = min(spg, nseg_valid - s0);
+          for (int sg = 1; sg < ns; sg++) {
             a = fmin_n(a, red[(s0 + sg) * 128 + ch]);
-            b = fmax_n(b, red[1024 + (s0 + sg) * 128 + ch]);
+            b = fmax_n(b, red[2048 + (s0 + sg) * 128 + ch]);
           }
           if (!finite2(a, b)) flags |= KVC_FLAG_NONFINITE;
           float sc, z, rr;
           uint32_t fl = 0;
           const uint32_t meta = quant_params<BITS>(a, b, sc, z, rr, fl);
           flags |= fl;
-          bool bad = fl != 0;
-          uint32_t cw[(16 * BITS + 31) / 32];
+          // a saturated group (fl != 0) is marked by r = NaN: its codes take the exact path
+          prm[gi * 128 + ch] = make_float4(z, fl ? __int_as_float(0x7fc00000) : rr, sc, __uint_as_float(meta));
+          const size_t g = ((size_t)lh * P.n_tg + tg) * kHeadDim + ch;
+          *reinterpret_cast<uint32_t *>(P.meta + g * 4) = meta;
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- D3: codes
+    {
+      const uint32_t tg = sb * tiles_groups + my_gi;
+      if (tg < P.n_tg) {  // a segment past the end of an existing group still writes its (zero) codes
+        const int gi = my_gi;
 #pragma unroll
-          for (int j = 0; j < (16 * BITS + 31) / 32; j++) cw[j] = 0u;
+        for (int k = 0; k < 4; k++) {
+          const int ch = cq + 32 * k;
+          const float4 pp = prm[gi * 128 + ch];
+          const float z = pp.x, rr = pp.y, sc = pp.z;
+          bool bad = false;
+          uint32_t cw[2] = {0u, 0u};
           const float2 z2 = bcast2(z), r2 = bcast2(rr);
 #pragma unroll
-          for (int i = 0; i < 8; i++) {
+          for (int i = 0; i < 4; i++) {
             const float2 u = qfast2<BITS>(v[k][i], z2, r2, bad);
             put_code<BITS>(cw, 2 * i, __float_as_uint(u.x));
             put_code<BITS>(cw, 2 * i + 1, __float_as_uint(u.y));
           }
           if (__any_sync(kFull, bad)) {
             if (bad) {
+              cw[0] = cw[1] = 0u;
 #pragma unroll
-              for (int j = 0; j < (16 * BITS + 31) / 32; j++) cw[j] = 0u;
-#pragma unroll
-              for (int i = 0; i < 8; i++) {
+              for (int i = 0; i < 4; i++) {
                 put_code<BITS>(cw, 2 * i, qexact<BITS>(v[k][i].x, z, sc));
                 put_code<BITS>(cw, 2 * i + 1, qexact<BITS>(v[k][i].y, z, sc));
               }
             }
           }
-          if (nv < 16) {  // codes of rows past the end are 0
-            const int keep = nv > 0 ? nv * BITS : 0;
-#pragma unroll
-            for (int j = 0; j < (16 * BITS + 31) / 32; j++) {
-              const int lo = 32 * j;
-              if (keep <= lo) cw[j] = 0u;
-              else if (keep < lo + 32) cw[j] &= (1u << (keep - lo)) - 1u;
-            }
+          if (nv < 8) {  // codes of rows past the end are 0
+            const int keep = (nv > 0 ? nv : 0) * BITS;
+            if (keep < 32) { cw[0] &= (1u << keep) - 1u; cw[1] = 0u; }
+            else if (keep < 64) cw[1] &= (1u << (keep - 32)) - 1u;
           }
           const size_t g = ((size_t)lh * P.n_tg + tg) * kHeadDim + ch;
-          store_code_words<BITS>(P.codes + g * (G * BITS / 8) + ((row0 % G) / 16) * (2 * BITS), cw);
-          if (row0 % G == 0) *reinterpret_cast<uint32_t *>(P.meta + g * 4) = meta;
+          store_codes8<BITS>(P.codes + g * rec_bytes + my_seg_off, cw[0], cw[1]);
         }
       }
     }
@@ -997,25 +1075,25 @@ __global__ void __launch_bounds__(kThreads) kvc_dec_tile(const QuantParams P) {
 // launchers
 // ---------------------------------------------------------------------------
 template <typename K>
-static int resident_blocks(K kernel, size_t smem) {
+static int resident_blocks(K kernel, size_t smem, int threads = kThreads) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, smem) != cudaSuccess || n < 1) n = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
   return n;
 }
 
 template <typename K>
 static int run(K kernel, bool tile, const QuantParams &p, int sm_count, void *stream, uint64_t work_units,
-               size_t smem_override = 0) {
+               size_t smem_override = 0, int threads = kThreads) {
   const size_t smem = smem_override ? smem_override : (tile ? kTileSmem : 0);
   if (tile) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
   }
   const uint64_t want = work_units;  // tiles, or CTAs of 8 warps
-  uint64_t blocks = (uint64_t)sm_count * resident_blocks(kernel, smem);
+  uint64_t blocks = (uint64_t)sm_count * resident_blocks(kernel, smem, threads);
   if (want < blocks) blocks = want;
   if (blocks == 0) return 0;
-  kernel<<<(unsigned)blocks, kThreads, smem, (cudaStream_t)stream>>>(p);
+  kernel<<<(unsigned)blocks, threads, smem, (cudaStream_t)stream>>>(p);
   return (int)cudaGetLastError();
 }
 
@@ -1029,8 +1107,11 @@ static int dispatch(const QuantParams &p, bool had, bool enc, int sm, void *st, 
   if (enc) {
     if (p.axis == KVC_AXIS_OVER_TOKENS) {
       *name = "kvc_enc_ktile";
-      return had ? run(kvc_enc_ktile<BITS, true>, true, p, sm, st, units, kKtileSmem)
-                 : run(kvc_enc_ktile<BITS, false>, true, p, sm, st, units, kKtileSmem);
+      if (p.g.bf16)
+        return had ? run(kvc_enc_ktile<BITS, true, true>, true, p, sm, st, units, kKtile3Smem, kKT)
+                   : run(kvc_enc_ktile<BITS, false, true>, true, p, sm, st, units, kKtile3Smem, kKT);
+      return had ? run(kvc_enc_ktile<BITS, true, false>, true, p, sm, st, units, kKtile3Smem, kKT)
+                 : run(kvc_enc_ktile<BITS, false, false>, true, p, sm, st, units, kKtile3Smem, kKT);
     }
     if (tile) {
       *name = "kvc_enc_tile";
@@ -1038,8 +1119,11 @@ static int dispatch(const QuantParams &p, bool had, bool enc, int sm, void *st, 
                  : run(kvc_enc_tile<BITS, false>, true, p, sm, st, units);
     }
     *name = "kvc_enc_rows";
-    return had ? run(kvc_enc_rows<BITS, true>, false, p, sm, st, units)
-               : run(kvc_enc_rows<BITS, false>, false, p, sm, st, units);
+    if (p.g.bf16)
+      return had ? run(kvc_enc_rows<BITS, true, true>, false, p, sm, st, units)
+                 : run(kvc_enc_rows<BITS, false, true>, false, p, sm, st, units);
+    return had ? run(kvc_enc_rows<BITS, true, false>, false, p, sm, st, units)
+               : run(kvc_enc_rows<BITS, false, false>, false, p, sm, st, units);
   }
   if (tile) {
     *name = "kvc_dec_tile";
