@@ -188,6 +188,28 @@ kvc_status kvc_query(const void *d_workspace, kvc_stream_t stream, uint64_t *hos
 
 const char *kvc_status_str(kvc_status status);
 
+/* Allocation-free variant of kvc_lossless_encode (no counterpart in the pages; an
+ * addition for callers that cannot allocate device memory, e.g. a transport or
+ * storage plugin called from inside another runtime's send path that receives
+ * only the payload and output buffers and must not call cudaMalloc there, which
+ * can synchronize the device or is barred by the host framework's memory pool).
+ * The encoder's scratch -- the 256-byte control block and one 64-bit look-back
+ * word per chunk -- lives in a device array of KVC_NOALLOC_SCRATCH_BYTES inside
+ * the library, which every GPU that loads the library holds until the process
+ * exits.  Plans whose 256 + 8 * kvc_num_chunks(plan) bytes exceed that size are
+ * rejected with KVC_ERR_CAPACITY (1 MiB: up to 131040 chunks, i.e. 2 GiB of
+ * payload at 16 KiB chunks).  Arguments as kvc_lossless_encode, except:
+ * d_stream_bytes (device u64, required) receives the stream size, and d_status
+ * (device u32, may be NULL) receives the status bits (KVC_FLAG_*); kvc_query does
+ * not apply.  Allocates nothing (no cudaMalloc / cudaFree).  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) and caches
+ * it; make that first call before any stream capture.  All calls share the one
+ * array (its words are reset at the start of every call), so calls whose GPU work
+ * overlaps -- on different streams or from different threads -- race; serialize them. */
+#define KVC_NOALLOC_SCRATCH_BYTES (1u << 20)
+kvc_status kvc_lossless_encode_noalloc(kvc_plan_t *plan, const void *d_payload, void *d_stream, size_t stream_cap,
+                                       uint64_t *d_stream_bytes, uint32_t *d_status, kvc_stream_t stream);
+
 /* ---- measurement hooks ---------------------------------------------------- */
 /* Number of kernel launches this plan has enqueued so far. */
 uint64_t kvc_launch_count(const kvc_plan_t *plan);

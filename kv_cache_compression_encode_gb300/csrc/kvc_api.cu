@@ -11,6 +11,7 @@
 // least significant bit first.
 #include <cuda_runtime.h>
 
+#include <mutex>
 #include <new>
 #include <stdlib.h>
 #include <string.h>
@@ -579,4 +580,54 @@ extern "C" const char *kvc_status_str(kvc_status s) {
     case KVC_ERR_CUDA: return "CUDA error";
   }
   return "unknown status";
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free lossless encode (kvc_lossless_encode_noalloc).
+//
+// The lossless encoder's scratch (256-byte control block + one 64-bit look-back
+// word per chunk) lives in this file-scope device array instead of a caller
+// workspace.  Every GPU that loads the library holds the array until the process
+// exits.  In host code `g_noalloc_scratch` only names a host-side stand-in, so
+// its device address is looked up once per device with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_noalloc_scratch[KVC_NOALLOC_SCRATCH_BYTES];
+
+static std::mutex g_noalloc_mutex;
+static void *g_noalloc_addr[256];  // device address of the array, per device ordinal
+
+static kvc_status noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVC_ERR_CUDA;
+  if (dev < 0 || dev >= 256) return KVC_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return KVC_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return KVC_OK;
+}
+
+extern "C" kvc_status kvc_lossless_encode_noalloc(kvc_plan_t *plan, const void *d_payload, void *d_stream,
+                                                  size_t stream_cap, uint64_t *d_stream_bytes, uint32_t *d_status,
+                                                  kvc_stream_t stream) {
+  if (!plan || !d_stream || !aligned16(d_stream) || !d_stream_bytes || (!d_payload && plan->payload_bytes) ||
+      (d_payload && !aligned16(d_payload)))
+    return KVC_ERR_INVALID_ARG;
+  if (stream_cap < plan->max_stream_bytes) return KVC_ERR_CAPACITY;
+  if ((uint64_t)kCtrlBytes + 8 * plan->n_chunks > KVC_NOALLOC_SCRATCH_BYTES) return KVC_ERR_CAPACITY;
+  void *ws = nullptr;
+  kvc_status s = noalloc_scratch(&ws);
+  if (s != KVC_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((s = run_prologue(plan, ws, true, true, static_cast<uint8_t *>(d_stream), d_stream_bytes, nullptr, st)) != KVC_OK)
+    return s;
+  if ((s = lossless_encode_impl(plan, static_cast<const uint8_t *>(d_payload), d_stream, stream_cap, ws,
+                                d_stream_bytes, st)) != KVC_OK)
+    return s;
+  if (d_status && cudaMemcpyAsync(d_status, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  return KVC_OK;
 }

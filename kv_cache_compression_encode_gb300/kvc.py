@@ -24,7 +24,7 @@ MAX_STAGES, MAX_LAYERS, HEADER_BYTES = 4, 256, 64
 EXPORTS = ["kvc_plan", "kvc_plan_destroy", "kvc_workspace_bytes", "kvc_max_stream_bytes", "kvc_payload_bytes",
            "kvc_section", "kvc_num_chunks", "kvc_encode", "kvc_decode", "kvc_quantize", "kvc_lossless_encode",
            "kvc_lossless_decode", "kvc_dequantize", "kvc_query", "kvc_status_str", "kvc_launch_count",
-           "kvc_timing_enable", "kvc_timing_read", "kvc_debug_lookback"]
+           "kvc_timing_enable", "kvc_timing_read", "kvc_debug_lookback", "kvc_lossless_encode_noalloc"]
 
 
 class KvcError(RuntimeError):
@@ -105,6 +105,7 @@ def load(build_if_missing: bool = True):
             "kvc_timing_enable": (st, [P, C.c_int, C.c_int]),
             "kvc_timing_read": (C.c_int, [P, C.POINTER(Timing), C.c_int]),
             "kvc_debug_lookback": (st, [P, C.c_int64, C.c_uint32]),
+            "kvc_lossless_encode_noalloc": (st, [P, vp, vp, sz, vp, vp, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -290,3 +291,12 @@ def kvc_timing_read(plan: Plan, max_records: int = 4096):
 
 def kvc_debug_lookback(plan: Plan, ticket: int, poll_limit: int = 0):
     _check(plan.lib.kvc_debug_lookback(plan.handle, ticket, poll_limit), "kvc_debug_lookback")
+
+
+def kvc_lossless_encode_noalloc(plan: Plan, d_payload: int, d_stream: int, stream_cap: int, d_stream_bytes: int,
+                                d_status: int = 0, stream: int = 0):
+    """Lossless encode whose scratch is the library's own device array (no workspace,
+    nothing allocated); the size goes to the device u64 at d_stream_bytes and the
+    status bits to the device u32 at d_status."""
+    _check(plan.lib.kvc_lossless_encode_noalloc(plan.handle, d_payload or None, d_stream, stream_cap, d_stream_bytes,
+                                                d_status or None, stream or None), "kvc_lossless_encode_noalloc")
