@@ -27,12 +27,16 @@ constexpr uint64_t kFlagAgg = 1ull << 62, kFlagIncl = 2ull << 62, kValMask = (1u
 
 __device__ __forceinline__ uint32_t align16u(uint32_t x) { return (x + 15u) & ~15u; }
 
-__device__ __forceinline__ void st_release(uint64_t *p, uint64_t v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+// A look-back word carries its flag and its value in one 64-bit access and no
+// other data is read through it, so relaxed (non-ordering) device-scope accesses
+// suffice -- and unlike acquire loads, a lane's loads of a whole window can all
+// be in flight at once.
+__device__ __forceinline__ void st_word64(uint64_t *p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ uint64_t ld_acquire(const uint64_t *p) {
+__device__ __forceinline__ uint64_t ld_word64(const uint64_t *p) {
   uint64_t v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -352,6 +356,57 @@ __global__ void kvc_prologue(const PrologueParams P) {
   }
 }
 
+__device__ __forceinline__ uint64_t warp_sum64(uint64_t x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Decoupled look-back by one warp, 256 predecessors per round: lane l reads the
+// words of chunks base - 8l - i (i = 0..7) in one batch of loads.  A chunk's
+// inclusive prefix only exists once its own look-back has finished, so the
+// prefix "frontier" advances by at most one round's window per memory round
+// trip; a 256-wide window keeps that chain short.  Every wait is bounded.
+__device__ uint64_t lookback_warp(const LosslessParams &P, uint32_t ticket, uint64_t agg) {
+  const int lane = threadIdx.x & 31;
+  uint64_t *state = P.state;
+  const bool publish = (int64_t)ticket != P.skip_ticket;
+  if (ticket == 0) {
+    if (lane == 0 && publish) st_word64(state, kFlagIncl | agg);
+    return 0;
+  }
+  if (lane == 0 && publish) st_word64(state + ticket, kFlagAgg | agg);
+  uint64_t excl = 0;
+  int64_t base = (int64_t)ticket - 1;  // lane i looks at chunk base - i
+  uint32_t polls = 0;
+  for (;;) {
+    const int64_t j = base - lane;
+    const uint64_t v = j >= 0 ? ld_word64(state + j) : kFlagIncl;  // before chunk 0: an inclusive prefix of 0
+    const uint64_t f = v & ~kValMask;
+    const uint32_t not_ready = __ballot_sync(0xffffffffu, f == 0);
+    const uint32_t incl = __ballot_sync(0xffffffffu, f == kFlagIncl);
+    const int first_nr = not_ready ? __ffs(not_ready) - 1 : 32;
+    const int first_inc = incl ? __ffs(incl) - 1 : 32;
+    if (first_inc < first_nr) {  // an inclusive prefix with only aggregates before it
+      excl += warp_sum64(lane <= first_inc ? (v & kValMask) : 0ull);
+      break;
+    }
+    excl += warp_sum64(lane < first_nr ? (v & kValMask) : 0ull);
+    if (first_nr == 32) {  // 32 aggregates: keep walking back
+      base -= 32;
+      continue;
+    }
+    base -= first_nr;  // resume at the predecessor that has not published yet
+    if (++polls > P.poll_limit) {
+      if (lane == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
+      break;
+    }
+    __nanosleep(64);
+  }
+  if (lane == 0 && publish) st_word64(state + ticket, kFlagIncl | (excl + agg));
+  return excl;
+}
+
 // ---------------------------------------------------------------------------
 // Encode: one chunk per CTA iteration, in ticket order.
 // ---------------------------------------------------------------------------
@@ -399,41 +454,19 @@ __global__ void __launch_bounds__(LT) kvc_lossless_enc(const LosslessParams P) {
     }
     const uint32_t asz = align16u(size);
 
-    // decoupled look-back: publish this chunk's aggregate, then add predecessors' until an inclusive prefix
-    if (threadIdx.x == 0) {
-      uint64_t *state = P.state;
-      const bool publish = (int64_t)ticket != P.skip_ticket;
-      uint64_t excl = 0;
-      if (ticket == 0) {
-        if (publish) st_release(state, kFlagIncl | asz);
-      } else {
-        if (publish) st_release(state + ticket, kFlagAgg | asz);
-        uint32_t j = ticket - 1, polls = 0;
-        for (;;) {
-          const uint64_t v = ld_acquire(state + j);
-          const uint64_t f = v & ~kValMask;
-          if (f == 0) {
-            if (++polls > P.poll_limit) {
-              atomicOr(ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
-              break;
-            }
-            __nanosleep(64);
-            continue;
-          }
-          excl += v & kValMask;
-          if (f == kFlagIncl || j == 0) break;
-          --j;
+    // decoupled look-back (warp 0): publish this chunk's aggregate, then add predecessors' until an inclusive prefix
+    if (threadIdx.x < 32) {
+      const uint64_t excl = lookback_warp(P, ticket, asz);
+      if (threadIdx.x == 0) {
+        s_excl = excl;
+        const uint64_t dst = P.data_start + excl;
+        if (dst + asz > P.stream_cap) atomicOr(ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CAPACITY);
+        reinterpret_cast<uint32_t *>(P.stream + KVC_HEADER_BYTES)[ticket] = size | (raw ? 0x80000000u : 0u);
+        if (ticket == P.n_chunks - 1) {
+          const uint64_t total = dst + asz;
+          reinterpret_cast<uint64_t *>(ctrl)[kCtrlStreamBytes] = total;
+          if (P.d_stream_bytes) *P.d_stream_bytes = total;
         }
-        if (publish) st_release(state + ticket, kFlagIncl | (excl + asz));
-      }
-      s_excl = excl;
-      const uint64_t dst = P.data_start + excl;
-      if (dst + asz > P.stream_cap) atomicOr(ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CAPACITY);
-      reinterpret_cast<uint32_t *>(P.stream + KVC_HEADER_BYTES)[ticket] = size | (raw ? 0x80000000u : 0u);
-      if (ticket == P.n_chunks - 1) {
-        const uint64_t total = dst + asz;
-        reinterpret_cast<uint64_t *>(ctrl)[kCtrlStreamBytes] = total;
-        if (P.d_stream_bytes) *P.d_stream_bytes = total;
       }
     }
     __syncthreads();
@@ -459,12 +492,11 @@ __global__ void __launch_bounds__(LT) kvc_lossless_enc(const LosslessParams P) {
 //    byte transpose (byte_perm) gathers byte j of the 8 tuples, an 8x8 bit
 //    transpose turns them into the 8 bit-plane bytes, which land at their final
 //    offsets;
-//  * DELTA_1 is a per-byte SIMD subtraction (__vsub4) of each 16-byte unit and
-//    its predecessor bytes;
-//  * RZE: each thread turns a 16-byte unit into its bitmap bits, warp scans and
-//    block sums give every unit its output offsets, ballots build the second-
-//    level bitmap; the encoded size is known before anything is written, so an
-//    incompressible chunk costs no compaction;
+//  * DELTA_1 and RZE run as one register pass: a thread owns 64 contiguous
+//    bytes, takes the byte differences (__vsub4) and the word bitmaps, and one
+//    block scan of its counts gives its output offsets; the encoded size is
+//    known before anything is written, so an incompressible chunk costs no
+//    compaction;
 //  * warp 0 runs the look-back 32 predecessors at a time.
 // A last chunk whose length is not a multiple of 512 bytes takes the generic
 // stage functions.
@@ -552,177 +584,122 @@ __device__ void fast_transform(const uint8_t *in, uint8_t *out, uint32_t n) {
   __syncthreads();
 }
 
-// DELTA_1 in place on a fast chunk (n <= 16384: at most 4 units per thread).
-__device__ void fast_delta1(uint8_t *buf, uint32_t n) {
-  const uint32_t nu = n / 16;
-  uint4 res[4];
-#pragma unroll
-  for (int k = 0; k < 4; k++) {
-    const uint32_t u = k * FT + threadIdx.x;
-    if (u < nu) {
-      const uint4 v = reinterpret_cast<const uint4 *>(buf)[u];
-      const uint32_t prev = u ? buf[16 * u - 1] : 0u;
-      res[k].x = __vsub4(v.x, (v.x << 8) | prev);
-      res[k].y = __vsub4(v.y, (v.y << 8) | (v.x >> 24));
-      res[k].z = __vsub4(v.z, (v.z << 8) | (v.y >> 24));
-      res[k].w = __vsub4(v.w, (v.w << 8) | (v.z >> 24));
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int k = 0; k < 4; k++) {
-    const uint32_t u = k * FT + threadIdx.x;
-    if (u < nu) reinterpret_cast<uint4 *>(buf)[u] = res[k];
-  }
-  __syncthreads();
-}
-
-__device__ __forceinline__ uint64_t spread_bits(uint32_t m) {
-  uint64_t x = m;
-  x = (x | (x << 16)) & 0x0000FFFF0000FFFFull;
-  x = (x | (x << 8)) & 0x00FF00FF00FF00FFull;
-  x = (x | (x << 4)) & 0x0F0F0F0F0F0F0F0Full;
-  x = (x | (x << 2)) & 0x3333333333333333ull;
-  x = (x | (x << 1)) & 0x5555555555555555ull;
-  return x;
-}
-
-// RZE_W of a fast chunk, in -> out (distinct plain buffers).  Returns the encoded
-// size; nothing is written when it is >= n.
-template <int W>
-__device__ uint32_t fast_rze(const uint8_t *in, uint8_t *out, uint32_t n, uint32_t *offs, uint16_t *Bs,
-                             uint32_t *wsum) {
-  const uint32_t nu = n / 16, nb = n / (8 * W), nb2 = nb / 8;
+// DELTA_1 (optional) and RZE_W of a fast chunk in one register pass: thread t owns
+// the 64 contiguous bytes [64t, 64t + 64) of `in` (n/64 threads active), takes the
+// byte differences and the word bitmaps in registers, and one block scan of its
+// (nonzero bitmap bytes, nonzero words) counts gives every thread its output
+// offsets.  Returns the encoded size; nothing is written when it is >= n.
+template <int W, bool DELTA>
+__device__ uint32_t fast_delta_rze(const uint8_t *in, uint8_t *out, uint32_t n, uint32_t *wsum) {
+  const uint32_t nthr = n / 64, nb = n / (8 * W), nb2 = nb / 8;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t baseB = 0, baseW = 0;
-  for (uint32_t p0 = 0; p0 < nu; p0 += FT) {
-    const uint32_t u = p0 + threadIdx.x;
-    uint32_t bits = 0;
-    if (u < nu) {
-      const uint4 v = reinterpret_cast<const uint4 *>(in)[u];
-      const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+  const uint32_t t = threadIdx.x;
+  const bool active = t < nthr;
+  uint32_t x[16];
 #pragma unroll
-      for (int k = 0; k < 4; k++) {
-        if (W == 2) {
-          bits |= (uint32_t)((x[k] & 0xffffu) != 0u) << (2 * k);
-          bits |= (uint32_t)((x[k] >> 16) != 0u) << (2 * k + 1);
-        } else {
+  for (int i = 0; i < 16; i++) x[i] = 0u;
+  if (active) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(in) + 4 * t;
 #pragma unroll
-          for (int b = 0; b < 4; b++) bits |= (uint32_t)(((x[k] >> (8 * b)) & 0xffu) != 0u) << (4 * k + b);
-        }
+    for (int k = 0; k < 4; k++) {
+      const uint4 v = src[k];
+      x[4 * k] = v.x; x[4 * k + 1] = v.y; x[4 * k + 2] = v.z; x[4 * k + 3] = v.w;
+    }
+    if (DELTA) {
+      uint32_t prev = t ? in[64 * t - 1] : 0u;
+#pragma unroll
+      for (int i = 0; i < 16; i++) {
+        const uint32_t cur = x[i];
+        x[i] = __vsub4(cur, (cur << 8) | prev);
+        prev = cur >> 24;
       }
-      Bs[u] = (uint16_t)bits;
     }
-    const uint32_t nzB = W == 2 ? (bits != 0u) : ((bits & 0xffu) != 0u) + ((bits >> 8) != 0u);
-    const uint32_t c = (nzB << 16) | (uint32_t)__popc(bits);
-    uint32_t x = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) wsum[warp] = x;
-    __syncthreads();
-    uint32_t wb = 0, tot = 0;
-#pragma unroll
-    for (int i = 0; i < FT / 32; i++) {
-      const uint32_t t = wsum[i];
-      if (i < warp) wb += t;
-      tot += t;
-    }
-    if (u < nu) offs[u] = ((baseB << 16) | baseW) + wb + x - c;
-    baseB += tot >> 16;
-    baseW += tot & 0xffffu;
-    __syncthreads();
   }
-  const uint32_t totB = baseB, totW = baseW;
-  const uint32_t size = nb2 + totB + W * totW;
-  if (size >= n) return size;
-  uint8_t *oB = out + nb2, *oW = out + nb2 + totB;
-  for (uint32_t p0 = 0; p0 < nu; p0 += FT) {
-    const uint32_t u = p0 + threadIdx.x;
-    const uint32_t bits = u < nu ? Bs[u] : 0u;
+  // word bitmap: W = 2 -> 32 words (one bit each, 4 bitmap bytes); W = 1 -> 64 bytes (8 bitmap bytes)
+  uint32_t blo = 0, bhi = 0;
+#pragma unroll
+  for (int i = 0; i < 16; i++) {
     if (W == 2) {
-      const uint32_t m32 = __ballot_sync(0xffffffffu, bits != 0u);
-      if (lane == 0 && p0 + warp * 32 < nu) reinterpret_cast<uint32_t *>(out)[(p0 + warp * 32) / 32] = m32;
+      blo |= (uint32_t)((x[i] & 0xffffu) != 0u) << (2 * i);
+      blo |= (uint32_t)((x[i] >> 16) != 0u) << (2 * i + 1);
     } else {
-      const uint32_t ml = __ballot_sync(0xffffffffu, (bits & 0xffu) != 0u);
-      const uint32_t mh = __ballot_sync(0xffffffffu, (bits >> 8) != 0u);
-      if (lane == 0 && p0 + warp * 32 < nu)
-        reinterpret_cast<uint64_t *>(out)[(p0 + warp * 32) / 32] = spread_bits(ml) | (spread_bits(mh) << 1);
-    }
-    if (u < nu && bits) {
-      const uint32_t o = offs[u];
-      uint32_t rB = o >> 16, rW = o & 0xffffu;
-      const uint4 v = reinterpret_cast<const uint4 *>(in)[u];
-      const uint32_t x[4] = {v.x, v.y, v.z, v.w};
-      if (W == 2) {
-        oB[rB] = (uint8_t)bits;
 #pragma unroll
-        for (int k = 0; k < 8; k++)
-          if ((bits >> k) & 1u) {
-            const uint32_t word = (x[k >> 1] >> (16 * (k & 1))) & 0xffffu;
-            oW[2 * rW] = (uint8_t)word;
-            oW[2 * rW + 1] = (uint8_t)(word >> 8);
-            rW++;
-          }
-      } else {
-        if (bits & 0xffu) oB[rB++] = (uint8_t)bits;
-        if (bits >> 8) oB[rB] = (uint8_t)(bits >> 8);
-#pragma unroll
-        for (int k = 0; k < 16; k++)
-          if ((bits >> k) & 1u) oW[rW++] = (uint8_t)(x[k >> 2] >> (8 * (k & 3)));
+      for (int b = 0; b < 4; b++) {
+        const uint32_t bit = (uint32_t)(((x[i] >> (8 * b)) & 0xffu) != 0u);
+        if (i < 8) blo |= bit << (4 * i + b);
+        else bhi |= bit << (4 * (i - 8) + b);
       }
     }
   }
-  __syncthreads();
-  return size;
-}
-
-__device__ __forceinline__ uint64_t warp_sum64(uint64_t x) {
+  uint32_t nzB = 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-
-// Decoupled look-back by one warp: each round reads 32 predecessors' words.
-__device__ uint64_t lookback_warp(const LosslessParams &P, uint32_t ticket, uint64_t agg) {
-  const int lane = threadIdx.x & 31;
-  uint64_t *state = P.state;
-  const bool publish = (int64_t)ticket != P.skip_ticket;
-  if (ticket == 0) {
-    if (lane == 0 && publish) st_release(state, kFlagIncl | agg);
-    return 0;
+  for (int j = 0; j < 4; j++) nzB += ((blo >> (8 * j)) & 0xffu) != 0u;
+  if (W == 1) {
+#pragma unroll
+    for (int j = 0; j < 4; j++) nzB += ((bhi >> (8 * j)) & 0xffu) != 0u;
   }
-  if (lane == 0 && publish) st_release(state + ticket, kFlagAgg | agg);
-  uint64_t excl = 0;
-  int64_t base = (int64_t)ticket - 1;
-  uint32_t polls = 0;
-  for (;;) {
-    const int64_t j = base - lane;
-    const uint64_t v = j >= 0 ? ld_acquire(state + j) : kFlagIncl;
-    const uint64_t f = v & ~kValMask;
-    const uint32_t nr = __ballot_sync(0xffffffffu, f == 0);
-    const uint32_t inc = __ballot_sync(0xffffffffu, f == kFlagIncl);
-    const int first_inc = inc ? __ffs(inc) - 1 : 32;
-    const int first_nr = nr ? __ffs(nr) - 1 : 32;
-    if (first_inc < first_nr) {
-      excl += warp_sum64(lane <= first_inc ? (v & kValMask) : 0ull);
-      break;
-    }
-    if (first_nr == 32) {
-      excl += warp_sum64(v & kValMask);
-      base -= 32;
-      continue;
-    }
-    if (++polls > P.poll_limit) {
-      if (lane == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
-      break;
-    }
-    __nanosleep(32);
+  const uint32_t nzW = __popc(blo) + (W == 1 ? __popc(bhi) : 0u);
+  const uint32_t c = (nzB << 16) | nzW;
+  uint32_t sc = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, sc, o);
+    if (lane >= o) sc += y;
   }
-  if (lane == 0 && publish) st_release(state + ticket, kFlagIncl | (excl + agg));
-  return excl;
+  if (lane == 31) wsum[warp] = sc;
+  __syncthreads();
+  uint32_t wb = 0, tot = 0;
+#pragma unroll
+  for (int i = 0; i < FT / 32; i++) {
+    const uint32_t v = wsum[i];
+    if (i < warp) wb += v;
+    tot += v;
+  }
+  const uint32_t totB = tot >> 16, totW = tot & 0xffffu;
+  const uint32_t size = nb2 + totB + W * totW;
+  if (size >= n) return size;  // uniform: the chunk is stored raw
+  const uint32_t ex = wb + sc - c;
+  uint32_t rB = ex >> 16, rW = ex & 0xffffu;
+  // second-level bitmap: W = 2 -> 4 bits per thread (two threads per byte); W = 1 -> one byte per thread
+  uint32_t nib = 0;
+#pragma unroll
+  for (int j = 0; j < 4; j++) nib |= (uint32_t)(((blo >> (8 * j)) & 0xffu) != 0u) << j;
+  if (W == 2) {
+    const uint32_t hi = __shfl_down_sync(0xffffffffu, nib, 1);
+    if (active && (t & 1) == 0) out[t >> 1] = (uint8_t)(nib | (hi << 4));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; j++) nib |= (uint32_t)(((bhi >> (8 * j)) & 0xffu) != 0u) << (4 + j);
+    if (active) out[t] = (uint8_t)nib;
+  }
+  if (active) {
+    uint8_t *oB = out + nb2, *oW = out + nb2 + totB;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const uint32_t b = (blo >> (8 * j)) & 0xffu;
+      if (b) oB[rB++] = (uint8_t)b;
+    }
+    if (W == 1) {
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        const uint32_t b = (bhi >> (8 * j)) & 0xffu;
+        if (b) oB[rB++] = (uint8_t)b;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      if (W == 2) {
+        if ((blo >> (2 * i)) & 1u) { oW[2 * rW] = (uint8_t)x[i]; oW[2 * rW + 1] = (uint8_t)(x[i] >> 8); rW++; }
+        if ((blo >> (2 * i + 1)) & 1u) { oW[2 * rW] = (uint8_t)(x[i] >> 16); oW[2 * rW + 1] = (uint8_t)(x[i] >> 24); rW++; }
+      } else {
+        const uint32_t bits = i < 8 ? (blo >> (4 * i)) : (bhi >> (4 * (i - 8)));
+#pragma unroll
+        for (int b = 0; b < 4; b++)
+          if ((bits >> b) & 1u) oW[rW++] = (uint8_t)(x[i] >> (8 * b));
+      }
+    }
+  }
+  return size;
 }
 
 struct FastSpec {
@@ -734,14 +711,17 @@ __global__ void __launch_bounds__(FT) kvc_lossless_enc_fast(const LosslessParams
   const uint32_t cb = P.chunk_bytes;
   uint8_t *const inb0 = reinterpret_cast<uint8_t *>(smem_u4);  // input buffer c at inb0 + c * cb
   uint8_t *A = inb0 + 2 * cb;
-  uint16_t *Bs = reinterpret_cast<uint16_t *>(A + cb + 64);
-  uint32_t *offs = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(Bs) + cb / 8 + 64);
-  uint32_t *wsum = offs + cb / 16;
+  uint16_t *Bs = reinterpret_cast<uint16_t *>(A + cb + 64);                          // generic-path bitmap
+  uint32_t *wsum = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(Bs) + cb / 8 + 64);  // scan words
   __shared__ uint32_t s_t[2];
   __shared__ uint64_t s_excl;
   const uint32_t nc = P.n_chunks;
   uint32_t *ticket_ctr = P.ctrl + kCtrlTicket;
 
+  // A ticket is taken only when this CTA is about to encode it (the next one right
+  // after the current chunk has published its prefix): a CTA never holds a ticket
+  // that others wait on while it is busy with an earlier chunk.  The next chunk's
+  // load overlaps the current chunk's copy-out.
   if (threadIdx.x == 0) s_t[0] = atomicAdd(ticket_ctr, 1u);
   __syncthreads();
   uint32_t t = s_t[0];
@@ -749,12 +729,7 @@ __global__ void __launch_bounds__(FT) kvc_lossless_enc_fast(const LosslessParams
   if (t < nc) issue_chunk_load(P, t, inb0);
   cp_async_commit();
   while (t < nc) {
-    if (threadIdx.x == 0) s_t[1] = atomicAdd(ticket_ctr, 1u);
-    __syncthreads();
-    const uint32_t tn = s_t[1];
-    if (tn < nc) issue_chunk_load(P, tn, inb0 + (cur ^ 1) * cb);
-    cp_async_commit();
-    cp_async_wait<1>();
+    cp_async_wait<0>();
     __syncthreads();
 
     uint8_t *in = inb0 + cur * cb;
@@ -766,8 +741,9 @@ __global__ void __launch_bounds__(FT) kvc_lossless_enc_fast(const LosslessParams
     if (fast_len(n)) {
       if (F.bit8) fast_transform<true>(in, A, n);
       else fast_transform<false>(in, A, n);
-      if (F.delta1) fast_delta1(A, n);
-      const uint32_t rs = F.rze_w == 2 ? fast_rze<2>(A, in, n, offs, Bs, wsum) : fast_rze<1>(A, in, n, offs, Bs, wsum);
+      uint32_t rs;
+      if (F.rze_w == 2) rs = F.delta1 ? fast_delta_rze<2, true>(A, in, n, wsum) : fast_delta_rze<2, false>(A, in, n, wsum);
+      else rs = F.delta1 ? fast_delta_rze<1, true>(A, in, n, wsum) : fast_delta_rze<1, false>(A, in, n, wsum);
       if (rs < n) size = rs;
       else swizzled = true;  // stored raw: the original bytes are still in `in`
     } else {
@@ -793,6 +769,7 @@ __global__ void __launch_bounds__(FT) kvc_lossless_enc_fast(const LosslessParams
     if (threadIdx.x < 32) {
       const uint64_t excl = lookback_warp(P, t, asz);
       if (threadIdx.x == 0) {
+        s_t[1] = atomicAdd(ticket_ctr, 1u);
         s_excl = excl;
         const uint64_t dst = P.data_start + excl;
         if (dst + asz > P.stream_cap) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CAPACITY);
@@ -805,6 +782,9 @@ __global__ void __launch_bounds__(FT) kvc_lossless_enc_fast(const LosslessParams
       }
     }
     __syncthreads();
+    const uint32_t tn = s_t[1];
+    if (tn < nc) issue_chunk_load(P, tn, inb0 + (cur ^ 1) * cb);
+    cp_async_commit();
     const uint64_t dst = P.data_start + s_excl;
     if (dst + asz <= P.stream_cap) {
       uint4 *o = reinterpret_cast<uint4 *>(P.stream + dst);
@@ -968,7 +948,7 @@ static bool fast_spec(const LosslessParams &p, FastSpec &f) {
   return true;
 }
 
-static size_t fast_smem(uint32_t cb) { return 3 * (size_t)cb + 64 + cb / 8 + 64 + cb / 4 + 64 * 4; }
+static size_t fast_smem(uint32_t cb) { return 3 * (size_t)cb + 64 + cb / 8 + 64 + 64 * 4; }
 
 int launch_lossless_encode(const LosslessParams &p, int sm_count, void *stream) {
   if (p.n_chunks == 0) return 0;
