@@ -40,6 +40,15 @@ __device__ __forceinline__ uint64_t ld_word64(const uint64_t *p) {
   return v;
 }
 
+// Barrier over the first NT threads of the CTA (named barrier 1).  Stage functions
+// use it instead of __syncthreads so that a CTA can hold threads outside the
+// group that runs them (the encoder's publisher warp); in a CTA of exactly NT
+// threads it is an ordinary CTA barrier.
+template <int NT>
+__device__ __forceinline__ void bsync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+
 // Block-wide exclusive scan of one value per thread (LT threads).  tmp holds
 // LT/32 + 1 words.  Ends with a barrier, so tmp can be reused immediately.
 template <typename U, int NT = LT>
@@ -52,7 +61,7 @@ __device__ __forceinline__ U block_excl_scan(U v, U *tmp, U &total) {
     if (lane >= o) x += y;
   }
   if (lane == 31) tmp[warp] = x;
-  __syncthreads();
+  bsync<NT>();
   if (warp == 0) {
     U w = lane < NT / 32 ? tmp[lane] : U(0);
 #pragma unroll
@@ -63,10 +72,10 @@ __device__ __forceinline__ U block_excl_scan(U v, U *tmp, U &total) {
     if (lane < NT / 32) tmp[lane] = w;
     if (lane == NT / 32 - 1) tmp[NT / 32] = w;
   }
-  __syncthreads();
+  bsync<NT>();
   const U excl = x - v + (warp ? tmp[warp - 1] : U(0));
   total = tmp[NT / 32];
-  __syncthreads();
+  bsync<NT>();
   return excl;
 }
 
@@ -125,7 +134,7 @@ __device__ void tupl_encode(const uint8_t *in, uint8_t *out, uint32_t n, uint32_
       for (uint32_t i = threadIdx.x; i < m; i += NT) out[j * m + i] = in[i * k + j];
   }
   for (uint32_t o = m * k + threadIdx.x; o < n; o += NT) out[o] = in[o];
-  __syncthreads();
+  bsync<NT>();
 }
 
 template <int NT = LT>
@@ -147,7 +156,7 @@ __device__ void tupl_decode(const uint8_t *in, uint8_t *out, uint32_t n, uint32_
     }
   }
   for (uint32_t o = m * k + threadIdx.x; o < n; o += NT) out[o] = in[o];
-  __syncthreads();
+  bsync<NT>();
 }
 
 // BIT_8: plane p (n8/8 bytes) collects bit p of every byte, byte i -> bit i%8 of byte i/8.
@@ -175,7 +184,7 @@ __device__ void bit_encode(const uint8_t *in, uint8_t *out, uint32_t n) {
     }
   }
   for (uint32_t o = n8 + threadIdx.x; o < n; o += NT) out[o] = in[o];
-  __syncthreads();
+  bsync<NT>();
 }
 
 template <int NT = LT>
@@ -188,7 +197,7 @@ __device__ void bit_decode(const uint8_t *in, uint8_t *out, uint32_t n) {
     *reinterpret_cast<uint64_t *>(out + 8 * b) = transpose8(x);
   }
   for (uint32_t o = n8 + threadIdx.x; o < n; o += NT) out[o] = in[o];
-  __syncthreads();
+  bsync<NT>();
 }
 
 // DELTA_w: word i -> word i - word (i-1) mod 2^(8w); word 0 kept.
@@ -201,7 +210,7 @@ __device__ void delta_encode(const uint8_t *in, uint8_t *out, uint32_t n, uint32
     st_word(out + i * w, w, (cur - prev) & mask);
   }
   for (uint32_t o = m * w + threadIdx.x; o < n; o += NT) out[o] = in[o];
-  __syncthreads();
+  bsync<NT>();
 }
 
 // Inverse: running sum mod 2^(8w); each thread sums a contiguous run, then a block scan.
@@ -220,7 +229,7 @@ __device__ void delta_decode(const uint8_t *in, uint8_t *out, uint32_t n, uint32
     st_word(out + i * w, w, acc & mask);
   }
   for (uint32_t o = m * w + threadIdx.x; o < n; o += NT) out[o] = in[o];
-  __syncthreads();
+  bsync<NT>();
 }
 
 // RZE_w: B = bitmap of nonzero words, B2 = bitmap of nonzero bytes of B; output
@@ -270,7 +279,7 @@ __device__ uint32_t rze_encode(const uint8_t *in, uint8_t *out, uint32_t n, uint
   }
   const uint32_t t0 = nb2 + totB + w * totW;
   for (uint32_t o = threadIdx.x; o < tail; o += NT) out[t0 + o] = in[m * w + o];
-  __syncthreads();
+  bsync<NT>();
   return size;
 }
 
@@ -301,7 +310,7 @@ __device__ bool rze_decode(const uint8_t *in, uint32_t size, uint8_t *out, uint3
       Bs[j] = ((v >> q) & 1u) ? in[nb2 + rB++] : (uint8_t)0;
     }
   }
-  __syncthreads();
+  bsync<NT>();
   // words listed by B (only its first m bits count)
   const uint32_t S = (nb + NT - 1) / NT;
   const uint32_t j0 = min(nb, threadIdx.x * S), j1 = min(nb, j0 + S);
@@ -330,7 +339,7 @@ __device__ bool rze_decode(const uint8_t *in, uint32_t size, uint8_t *out, uint3
   }
   const uint8_t *tl = words + w * totW;
   for (uint32_t o = threadIdx.x; o < tail; o += NT) out[m * w + o] = tl[o];
-  __syncthreads();
+  bsync<NT>();
   return true;
 }
 
@@ -367,15 +376,15 @@ __device__ __forceinline__ uint64_t warp_sum64(uint64_t x) {
 // inclusive prefix only exists once its own look-back has finished, so the
 // prefix "frontier" advances by at most one round's window per memory round
 // trip; a 256-wide window keeps that chain short.  Every wait is bounded.
-__device__ uint64_t lookback_warp(const LosslessParams &P, uint32_t ticket, uint64_t agg) {
+__device__ uint64_t lookback_warp(const LosslessParams &P, uint32_t ticket, uint64_t agg, bool publish_agg) {
   const int lane = threadIdx.x & 31;
   uint64_t *state = P.state;
   const bool publish = (int64_t)ticket != P.skip_ticket;
   if (ticket == 0) {
-    if (lane == 0 && publish) st_word64(state, kFlagIncl | agg);
+    if (lane == 0 && publish && publish_agg) st_word64(state, kFlagIncl | agg);
     return 0;
   }
-  if (lane == 0 && publish) st_word64(state + ticket, kFlagAgg | agg);
+  if (lane == 0 && publish && publish_agg) st_word64(state + ticket, kFlagAgg | agg);
   uint64_t excl = 0;
   int64_t base = (int64_t)ticket - 1;  // lane i looks at chunk base - i
   uint32_t polls = 0;
@@ -456,7 +465,7 @@ __global__ void __launch_bounds__(LT) kvc_lossless_enc(const LosslessParams P) {
 
     // decoupled look-back (warp 0): publish this chunk's aggregate, then add predecessors' until an inclusive prefix
     if (threadIdx.x < 32) {
-      const uint64_t excl = lookback_warp(P, ticket, asz);
+      const uint64_t excl = lookback_warp(P, ticket, asz, true);
       if (threadIdx.x == 0) {
         s_excl = excl;
         const uint64_t dst = P.data_start + excl;
@@ -485,24 +494,36 @@ __global__ void __launch_bounds__(LT) kvc_lossless_enc(const LosslessParams P) {
 
 // ===========================================================================
 // Fast encoder for the stage lists TUPL_8 [BIT_8] [DELTA_1] RZE_w (w = 1 or 2)
-// and chunks of at most 16 KiB.  Per chunk, in shared memory:
-//  * the chunk arrives by cp.async into a swizzled buffer while the previous
-//    chunk is being encoded (two input buffers per CTA);
-//  * TUPL_8 (and BIT_8) run as one register transform per 8-tuple block: a 4x4
-//    byte transpose (byte_perm) gathers byte j of the 8 tuples, an 8x8 bit
-//    transpose turns them into the 8 bit-plane bytes, which land at their final
-//    offsets;
-//  * DELTA_1 and RZE run as one register pass: a thread owns 64 contiguous
-//    bytes, takes the byte differences (__vsub4) and the word bitmaps, and one
-//    block scan of its counts gives its output offsets; the encoded size is
-//    known before anything is written, so an incompressible chunk costs no
-//    compaction;
-//  * warp 0 runs the look-back 32 predecessors at a time.
-// A last chunk whose length is not a multiple of 512 bytes takes the generic
-// stage functions.
+// and chunk sizes that are multiples of 4 KiB up to 16 KiB.  A CTA holds eight
+// worker warps and one publisher warp.
+//  * Workers: a chunk arrives by cp.async into a swizzled input buffer.  TUPL_8
+//    (and BIT_8) run as one register transform per 8-tuple block (a 4x4 byte
+//    transpose gathers byte j of the 8 tuples, an 8x8 bit transpose makes the 8
+//    bit-plane bytes) into a ring slot, stored with the same swizzle so that the
+//    next pass reads it without bank conflicts.  The input buffer is then free
+//    and the next chunk's load is issued.  DELTA_1 and RZE run as one register
+//    pass: a thread owns 64 contiguous bytes, takes the byte differences
+//    (__vsub4) and the word bitmaps, one block scan of its counts gives its
+//    output offsets, and the encoded chunk is written over its own input in the
+//    slot.  The encoded size is known before anything is written, so an
+//    incompressible chunk costs no compaction.  The chunk's aligned size is
+//    published for the look-back at once and the slot handed to the publisher.
+//  * Publisher: takes the slots in ticket order, finds each chunk's stream
+//    offset by the look-back over its predecessors (32 at a time), publishes
+//    the inclusive prefix, writes the chunk-table entry, copies the chunk to the
+//    stream and hands the slot back.  Workers never wait on other CTAs, only on
+//    a slot of their own ring.
+// Slots pass between the two sides through one "full" and one "empty" mbarrier
+// per slot; every wait is bounded and sets KVC_FLAG_TIMEOUT when it runs out.  A
+// chunk whose length is not a multiple of 4 KiB (only the last one can be) runs
+// the generic stage functions on the worker threads.
 // ===========================================================================
-constexpr int FT = 256;
+constexpr int FT = 256;        // worker threads
+constexpr int FW = FT + 32;    // workers + the publisher warp
+constexpr int kRing = 3;       // slots per CTA
 constexpr uint32_t kFastMaxChunk = 16384;
+constexpr uint32_t kEndTicket = 0xffffffffu;
+constexpr uint32_t kMbarTries = 1u << 20;
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
   const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
@@ -512,11 +533,33 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// 16-byte unit u of a fast chunk is stored at swz(u): within each 64-byte block
-// the four units rotate by (block >> 1), so 8 lanes reading unit k of 8
-// consecutive blocks touch 8 distinct bank groups.
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(b)) : "memory");
+}
+// Waits until the phase of parity `par` has completed; false after kMbarTries tries.
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t par) {
+  for (uint32_t i = 0; i < kMbarTries; i++) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done)
+                 : "r"(smem_addr(b)), "r"(par)
+                 : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// 16-byte unit u of a fast chunk buffer is stored at swz(u): within each 64-byte
+// block the four units rotate by (block >> 1), so 8 lanes reading unit k of 8
+// consecutive blocks touch 8 distinct bank groups.  swzb is the same map on a
+// byte offset.
 __device__ __forceinline__ uint32_t swz(uint32_t u) { return (u & ~3u) | ((u + (u >> 3)) & 3u); }
-__device__ __forceinline__ bool fast_len(uint32_t n) { return (n & 511u) == 0 && n <= kFastMaxChunk; }
+__device__ __forceinline__ uint32_t swzb(uint32_t x) { return (x & ~0x30u) | ((((x >> 4) + (x >> 7)) & 3u) << 4); }
+__device__ __forceinline__ bool fast_len(uint32_t n) { return (n & 4095u) == 0 && n <= kFastMaxChunk; }
 
 __device__ void issue_chunk_load(const LosslessParams &P, uint32_t t, uint8_t *dst) {
   const uint64_t off = (uint64_t)t * P.chunk_bytes;
@@ -548,7 +591,11 @@ __device__ __forceinline__ void bits8x8(uint32_t &lo, uint32_t &hi) {
   hi ^= t >> 4;
 }
 
-// TUPL_8 (and BIT_8 after it) of a fast chunk: `in` swizzled, `out` plain.
+// TUPL_8 (and BIT_8 after it) of a fast chunk, swizzled in and swizzled out.
+// Without BIT_8, tuple byte j of block beta goes to byte 8*beta.. of row j (m
+// bytes per row); with BIT_8, bit p of those 8 bytes forms byte beta of row j of
+// bit plane p.  n is a multiple of 4 KiB, so a row start never changes the
+// swizzle rotation and each thread computes its offsets once per row.
 template <bool BIT8>
 __device__ void fast_transform(const uint8_t *in, uint8_t *out, uint32_t n) {
   const uint32_t nblk = n / 64, m = n / 8, m8 = n / 64;
@@ -566,29 +613,28 @@ __device__ void fast_transform(const uint8_t *in, uint8_t *out, uint32_t n) {
     byte_t4x4(w[8], w[10], w[12], w[14], L1);
     byte_t4x4(w[1], w[3], w[5], w[7], H0);
     byte_t4x4(w[9], w[11], w[13], w[15], H1);
+    const uint32_t off8 = 64 * (beta >> 3) + 16 * (((beta >> 1) + (beta >> 4)) & 3u) + 8 * (beta & 1u);
 #pragma unroll
     for (int j = 0; j < 8; j++) {
       uint32_t lo = j < 4 ? L0[j & 3] : H0[j & 3], hi = j < 4 ? L1[j & 3] : H1[j & 3];
       if (BIT8) {
         bits8x8(lo, hi);
-        uint8_t *ob = out + j * m8 + beta;
+        uint8_t *ob = out + swzb(j * m8 + beta);
 #pragma unroll
         for (int p = 0; p < 4; p++) ob[p * m] = (uint8_t)(lo >> (8 * p));
 #pragma unroll
         for (int p = 0; p < 4; p++) ob[(p + 4) * m] = (uint8_t)(hi >> (8 * p));
       } else {
-        *reinterpret_cast<uint2 *>(out + j * m + 8 * beta) = make_uint2(lo, hi);
+        *reinterpret_cast<uint2 *>(out + j * m + off8) = make_uint2(lo, hi);
       }
     }
   }
-  __syncthreads();
+  bsync<FT>();
 }
 
-// DELTA_1 (optional) and RZE_W of a fast chunk in one register pass: thread t owns
-// the 64 contiguous bytes [64t, 64t + 64) of `in` (n/64 threads active), takes the
-// byte differences and the word bitmaps in registers, and one block scan of its
-// (nonzero bitmap bytes, nonzero words) counts gives every thread its output
-// offsets.  Returns the encoded size; nothing is written when it is >= n.
+// DELTA_1 (optional) and RZE_w of a fast chunk held swizzled in `in`; the encoded
+// chunk goes to `out`, which may be `in` itself: every read happens before the
+// first barrier.  Returns the encoded size; nothing is written when it is >= n.
 template <int W, bool DELTA>
 __device__ uint32_t fast_delta_rze(const uint8_t *in, uint8_t *out, uint32_t n, uint32_t *wsum) {
   const uint32_t nthr = n / 64, nb = n / (8 * W), nb2 = nb / 8;
@@ -600,13 +646,15 @@ __device__ uint32_t fast_delta_rze(const uint8_t *in, uint8_t *out, uint32_t n, 
   for (int i = 0; i < 16; i++) x[i] = 0u;
   if (active) {
     const uint4 *src = reinterpret_cast<const uint4 *>(in) + 4 * t;
+    const uint32_t rot = (t >> 1) & 3u;  // logical unit k of this block sits at unit (k + rot) & 3
 #pragma unroll
     for (int k = 0; k < 4; k++) {
-      const uint4 v = src[k];
+      const uint4 v = src[(k + rot) & 3u];
       x[4 * k] = v.x; x[4 * k + 1] = v.y; x[4 * k + 2] = v.z; x[4 * k + 3] = v.w;
     }
     if (DELTA) {
-      uint32_t prev = t ? in[64 * t - 1] : 0u;
+      // last byte of the previous block: logical unit 3 of block t - 1
+      uint32_t prev = t ? in[16 * (4 * (t - 1) + ((3u + ((t - 1) >> 1)) & 3u)) + 15] : 0u;
 #pragma unroll
       for (int i = 0; i < 16; i++) {
         const uint32_t cur = x[i];
@@ -647,7 +695,7 @@ __device__ uint32_t fast_delta_rze(const uint8_t *in, uint8_t *out, uint32_t n, 
     if (lane >= o) sc += y;
   }
   if (lane == 31) wsum[warp] = sc;
-  __syncthreads();
+  bsync<FT>();
   uint32_t wb = 0, tot = 0;
 #pragma unroll
   for (int i = 0; i < FT / 32; i++) {
@@ -706,96 +754,137 @@ struct FastSpec {
   uint32_t bit8, delta1, rze_w, pad;
 };
 
-__global__ void __launch_bounds__(FT) kvc_lossless_enc_fast(const LosslessParams P, const FastSpec F) {
+__global__ void __launch_bounds__(FW, 3) kvc_lossless_enc_fast(const LosslessParams P, const FastSpec F) {
   extern __shared__ uint4 smem_u4[];
-  const uint32_t cb = P.chunk_bytes;
-  uint8_t *const inb0 = reinterpret_cast<uint8_t *>(smem_u4);  // input buffer c at inb0 + c * cb
-  uint8_t *A = inb0 + 2 * cb;
-  uint16_t *Bs = reinterpret_cast<uint16_t *>(A + cb + 64);                          // generic-path bitmap
+  const uint32_t cb = P.chunk_bytes, slot_bytes = cb + 64;
+  uint8_t *const IN = reinterpret_cast<uint8_t *>(smem_u4);  // input buffer
+  uint8_t *const ring = IN + slot_bytes;                       // slot s at ring + s * slot_bytes
+  uint16_t *Bs = reinterpret_cast<uint16_t *>(ring + kRing * slot_bytes);                       // generic-path bitmap
   uint32_t *wsum = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(Bs) + cb / 8 + 64);  // scan words
-  __shared__ uint32_t s_t[2];
-  __shared__ uint64_t s_excl;
+  __shared__ __align__(8) uint64_t s_full[kRing], s_empty[kRing];
+  __shared__ uint32_t s_meta[kRing][2];  // ticket, table word (size | raw bit)
+  __shared__ uint32_t s_t;
   const uint32_t nc = P.n_chunks;
   uint32_t *ticket_ctr = P.ctrl + kCtrlTicket;
-
-  // A ticket is taken only when this CTA is about to encode it (the next one right
-  // after the current chunk has published its prefix): a CTA never holds a ticket
-  // that others wait on while it is busy with an earlier chunk.  The next chunk's
-  // load overlaps the current chunk's copy-out.
-  if (threadIdx.x == 0) s_t[0] = atomicAdd(ticket_ctr, 1u);
-  __syncthreads();
-  uint32_t t = s_t[0];
-  uint32_t cur = 0;
-  if (t < nc) issue_chunk_load(P, t, inb0);
-  cp_async_commit();
-  while (t < nc) {
-    cp_async_wait<0>();
-    __syncthreads();
-
-    uint8_t *in = inb0 + cur * cb;
-    const uint64_t off = (uint64_t)t * cb;
-    const uint32_t n = (uint32_t)min((uint64_t)cb, P.payload_bytes - off);
-    uint32_t size = n;
-    const uint8_t *outp = in;
-    bool swizzled = false, from_global = false;
-    if (fast_len(n)) {
-      if (F.bit8) fast_transform<true>(in, A, n);
-      else fast_transform<false>(in, A, n);
-      uint32_t rs;
-      if (F.rze_w == 2) rs = F.delta1 ? fast_delta_rze<2, true>(A, in, n, wsum) : fast_delta_rze<2, false>(A, in, n, wsum);
-      else rs = F.delta1 ? fast_delta_rze<1, true>(A, in, n, wsum) : fast_delta_rze<1, false>(A, in, n, wsum);
-      if (rs < n) size = rs;
-      else swizzled = true;  // stored raw: the original bytes are still in `in`
-    } else {
-      uint8_t *cur_b = in, *nxt_b = A;
-      for (uint32_t s = 0; s + 1 < P.n_stages; s++) {
-        const uint32_t k = P.kind[s], prm = P.param[s];
-        if (k == KVC_ST_TUPL) tupl_encode<FT>(cur_b, nxt_b, n, prm);
-        else if (k == KVC_ST_BIT) bit_encode<FT>(cur_b, nxt_b, n);
-        else delta_encode<FT>(cur_b, nxt_b, n, prm);
-        uint8_t *tmpb = cur_b; cur_b = nxt_b; nxt_b = tmpb;
-      }
-      const uint32_t rs = rze_encode<FT>(cur_b, nxt_b, n, P.param[P.n_stages - 1], reinterpret_cast<uint8_t *>(Bs), wsum);
-      if (rs < n) {
-        size = rs;
-        outp = nxt_b;
-      } else {
-        from_global = true;
-      }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRing; s++) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], 1);
     }
-    const bool raw = size == n;
-    const uint32_t asz = align16u(size);
-    if (!raw && threadIdx.x < asz - size) const_cast<uint8_t *>(outp)[size + threadIdx.x] = 0;
-    if (threadIdx.x < 32) {
-      const uint64_t excl = lookback_warp(P, t, asz);
-      if (threadIdx.x == 0) {
-        s_t[1] = atomicAdd(ticket_ctr, 1u);
-        s_excl = excl;
-        const uint64_t dst = P.data_start + excl;
+    s_t = atomicAdd(ticket_ctr, 1u);
+  }
+  __syncthreads();
+
+  if (threadIdx.x >= FT) {  // ---- publisher warp
+    const int lane = threadIdx.x & 31;
+    for (uint32_t k = 0;; k++) {
+      const uint32_t s = k % kRing;
+      if (!mbar_wait(&s_full[s], (k / kRing) & 1u)) {
+        if (lane == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
+        break;
+      }
+      const uint32_t t = s_meta[s][0], word = s_meta[s][1];
+      if (t == kEndTicket) break;
+      const bool raw = (word >> 31) != 0;
+      const uint32_t asz = align16u(word & 0x7fffffffu);
+      const uint64_t excl = lookback_warp(P, t, asz, false);
+      const uint64_t dst = P.data_start + excl;
+      if (lane == 0) {
         if (dst + asz > P.stream_cap) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CAPACITY);
-        reinterpret_cast<uint32_t *>(P.stream + KVC_HEADER_BYTES)[t] = size | (raw ? 0x80000000u : 0u);
+        reinterpret_cast<uint32_t *>(P.stream + KVC_HEADER_BYTES)[t] = word;
         if (t == nc - 1) {
           const uint64_t total = dst + asz;
           reinterpret_cast<uint64_t *>(P.ctrl)[kCtrlStreamBytes] = total;
           if (P.d_stream_bytes) *P.d_stream_bytes = total;
         }
       }
+      if (dst + asz <= P.stream_cap) {
+        uint4 *o = reinterpret_cast<uint4 *>(P.stream + dst);
+        if (raw) {
+          const uint4 *g = reinterpret_cast<const uint4 *>(P.payload + (uint64_t)t * cb);
+          for (uint32_t i = lane; i < asz / 16; i += 32) o[i] = __ldg(g + i);
+        } else {
+          const uint4 *sm = reinterpret_cast<const uint4 *>(ring + s * slot_bytes);
+#pragma unroll 4
+          for (uint32_t i = lane; i < asz / 16; i += 32) o[i] = sm[i];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[s]);
     }
-    __syncthreads();
-    const uint32_t tn = s_t[1];
-    if (tn < nc) issue_chunk_load(P, tn, inb0 + (cur ^ 1) * cb);
-    cp_async_commit();
-    const uint64_t dst = P.data_start + s_excl;
-    if (dst + asz <= P.stream_cap) {
-      uint4 *o = reinterpret_cast<uint4 *>(P.stream + dst);
-      const uint4 *g = reinterpret_cast<const uint4 *>(P.payload + off);
-      const uint4 *sm = reinterpret_cast<const uint4 *>(outp);
-      for (uint32_t i = threadIdx.x; i < asz / 16; i += FT)
-        o[i] = from_global ? __ldg(g + i) : sm[swizzled ? swz(i) : i];
+    return;
+  }
+
+  // ---- workers
+  uint32_t t = s_t;
+  if (t < nc) issue_chunk_load(P, t, IN);
+  cp_async_commit();
+  uint32_t k = 0;
+  for (; t < nc; k++) {
+    const uint32_t s = k % kRing;
+    uint8_t *const A = ring + s * slot_bytes;
+    if (threadIdx.x == 0 && k >= kRing && !mbar_wait(&s_empty[s], (k / kRing - 1) & 1u))
+      atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
+    cp_async_wait<0>();
+    bsync<FT>();
+
+    const uint64_t off = (uint64_t)t * cb;
+    const uint32_t n = (uint32_t)min((uint64_t)cb, P.payload_bytes - off);
+    uint32_t size = n, tn;
+    bool raw;
+    if (fast_len(n)) {
+      if (threadIdx.x == 0) s_t = atomicAdd(ticket_ctr, 1u);
+      if (F.bit8) fast_transform<true>(IN, A, n);
+      else fast_transform<false>(IN, A, n);
+      tn = s_t;
+      if (tn < nc) issue_chunk_load(P, tn, IN);
+      cp_async_commit();
+      uint32_t rs;
+      if (F.rze_w == 2) rs = F.delta1 ? fast_delta_rze<2, true>(A, A, n, wsum) : fast_delta_rze<2, false>(A, A, n, wsum);
+      else rs = F.delta1 ? fast_delta_rze<1, true>(A, A, n, wsum) : fast_delta_rze<1, false>(A, A, n, wsum);
+      raw = rs >= n;  // stored raw: the publisher copies the chunk from the payload
+      if (!raw) size = rs;
+    } else {
+      uint8_t *cur_b = IN, *nxt_b = A;
+      for (uint32_t st = 0; st + 1 < P.n_stages; st++) {
+        const uint32_t kind = P.kind[st], prm = P.param[st];
+        if (kind == KVC_ST_TUPL) tupl_encode<FT>(cur_b, nxt_b, n, prm);
+        else if (kind == KVC_ST_BIT) bit_encode<FT>(cur_b, nxt_b, n);
+        else delta_encode<FT>(cur_b, nxt_b, n, prm);
+        uint8_t *tmpb = cur_b; cur_b = nxt_b; nxt_b = tmpb;
+      }
+      const uint32_t rs = rze_encode<FT>(cur_b, nxt_b, n, P.param[P.n_stages - 1], reinterpret_cast<uint8_t *>(Bs), wsum);
+      raw = rs >= n;
+      if (!raw) {
+        size = rs;
+        if (nxt_b != A) {
+          for (uint32_t i = threadIdx.x; i < align16u(rs) / 16; i += FT)
+            reinterpret_cast<uint4 *>(A)[i] = reinterpret_cast<const uint4 *>(nxt_b)[i];
+        }
+      }
+      if (threadIdx.x == 0) s_t = atomicAdd(ticket_ctr, 1u);
+      bsync<FT>();
+      tn = s_t;
+      if (tn < nc) issue_chunk_load(P, tn, IN);
+      cp_async_commit();
     }
-    cur ^= 1;
+    const uint32_t asz = align16u(size);
+    if (!raw && threadIdx.x < asz - size) A[size + threadIdx.x] = 0;
+    if (threadIdx.x == 0) {
+      if ((int64_t)t != P.skip_ticket) st_word64(P.state + t, (t == 0 ? kFlagIncl : kFlagAgg) | asz);
+      s_meta[s][0] = t;
+      s_meta[s][1] = size | (raw ? 0x80000000u : 0u);
+    }
+    bsync<FT>();
+    if (threadIdx.x == 0) mbar_arrive(&s_full[s]);
     t = tn;
-    __syncthreads();
+  }
+  if (threadIdx.x == 0) {  // tell the publisher to stop
+    const uint32_t s = k % kRing;
+    if (k >= kRing && !mbar_wait(&s_empty[s], (k / kRing - 1) & 1u))
+      atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
+    s_meta[s][0] = kEndTicket;
+    mbar_arrive(&s_full[s]);
   }
   cp_async_wait<0>();
 }
@@ -937,7 +1026,7 @@ int launch_prologue(const PrologueParams &p, void *stream) {
 
 static bool fast_spec(const LosslessParams &p, FastSpec &f) {
   f = FastSpec{0, 0, 0, 0};
-  if (p.chunk_bytes > kFastMaxChunk || p.chunk_bytes % 512) return false;
+  if (p.chunk_bytes > kFastMaxChunk || p.chunk_bytes % 4096) return false;
   uint32_t s = 0;
   if (s >= p.n_stages || p.kind[s] != KVC_ST_TUPL || p.param[s] != 8) return false;
   s++;
@@ -948,7 +1037,7 @@ static bool fast_spec(const LosslessParams &p, FastSpec &f) {
   return true;
 }
 
-static size_t fast_smem(uint32_t cb) { return 3 * (size_t)cb + 64 + cb / 8 + 64 + 64 * 4; }
+static size_t fast_smem(uint32_t cb) { return (1 + kRing) * ((size_t)cb + 64) + cb / 8 + 64 + 64 * 4; }
 
 int launch_lossless_encode(const LosslessParams &p, int sm_count, void *stream) {
   if (p.n_chunks == 0) return 0;
@@ -958,12 +1047,12 @@ int launch_lossless_encode(const LosslessParams &p, int sm_count, void *stream) 
     cudaError_t e = cudaFuncSetAttribute(kvc_lossless_enc_fast, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kvc_lossless_enc_fast, FT, smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kvc_lossless_enc_fast, FW, smem) != cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
     uint64_t blocks = (uint64_t)sm_count * per_sm;
     if (blocks > p.n_chunks) blocks = p.n_chunks;
-    kvc_lossless_enc_fast<<<(unsigned)blocks, FT, smem, (cudaStream_t)stream>>>(p, f);
+    kvc_lossless_enc_fast<<<(unsigned)blocks, FW, smem, (cudaStream_t)stream>>>(p, f);
     return (int)cudaGetLastError();
   }
   const size_t smem = lossless_smem(p.chunk_bytes);

@@ -227,11 +227,13 @@ def test_corrupt_streams_are_rejected_and_outputs_untouched():
             assert bool((t.view(torch.int16) == 0x1234).all()), name
 
 
-def test_lookback_wait_is_bounded():
+@pytest.mark.parametrize("chunk", [1024, 4096])
+def test_lookback_wait_is_bounded(chunk):
     """A chunk that never publishes its size: the successor's wait runs out,
-    the status says TIMEOUT, and the GPU stays usable."""
-    prof = dict(bits_k=4, bits_v=4, group_k=64, group_v=64, stages=LC, chunk_bytes=1024)
-    case = U.Case(L=1, T=256, H=2, profile=prof, seed=6).materialize()
+    the status says TIMEOUT, and the GPU stays usable.  1 KiB chunks run the
+    generic encoder, 4 KiB chunks the worker/publisher encoder."""
+    prof = dict(bits_k=4, bits_v=4, group_k=64, group_v=64, stages=LC, chunk_bytes=chunk)
+    case = U.Case(L=1, T=256 if chunk == 1024 else 512, H=2, profile=prof, seed=6).materialize()
     codec = Codec(kvc.make_profile(**prof), case.kvc_shape())
     kvc.kvc_debug_lookback(codec.plan, 3, 2000)
     codec.encode(case.k, case.v)
