@@ -371,20 +371,14 @@ __device__ __forceinline__ uint64_t warp_sum64(uint64_t x) {
   return x;
 }
 
-// Decoupled look-back by one warp, 256 predecessors per round: lane l reads the
-// words of chunks base - 8l - i (i = 0..7) in one batch of loads.  A chunk's
-// inclusive prefix only exists once its own look-back has finished, so the
-// prefix "frontier" advances by at most one round's window per memory round
-// trip; a 256-wide window keeps that chain short.  Every wait is bounded.
-__device__ uint64_t lookback_warp(const LosslessParams &P, uint32_t ticket, uint64_t agg, bool publish_agg) {
+// Exclusive prefix of chunk `ticket` by the decoupled look-back of one warp:
+// lane l reads the word of chunk base - l, 32 predecessors per round; aggregates
+// are summed until an inclusive prefix is reached, and a predecessor that has not
+// published yet is polled again (bounded by poll_limit, then KVC_FLAG_TIMEOUT).
+// Publishes nothing.
+__device__ uint64_t lookback_excl(const LosslessParams &P, uint32_t ticket) {
   const int lane = threadIdx.x & 31;
-  uint64_t *state = P.state;
-  const bool publish = (int64_t)ticket != P.skip_ticket;
-  if (ticket == 0) {
-    if (lane == 0 && publish && publish_agg) st_word64(state, kFlagIncl | agg);
-    return 0;
-  }
-  if (lane == 0 && publish && publish_agg) st_word64(state + ticket, kFlagAgg | agg);
+  const uint64_t *state = P.state;
   uint64_t excl = 0;
   int64_t base = (int64_t)ticket - 1;  // lane i looks at chunk base - i
   uint32_t polls = 0;
@@ -412,7 +406,21 @@ __device__ uint64_t lookback_warp(const LosslessParams &P, uint32_t ticket, uint
     }
     __nanosleep(64);
   }
-  if (lane == 0 && publish) st_word64(state + ticket, kFlagIncl | (excl + agg));
+  return excl;
+}
+
+// The whole look-back for one chunk of `agg` bytes: publish the aggregate, find
+// the exclusive prefix, publish the inclusive one.
+__device__ uint64_t lookback_warp(const LosslessParams &P, uint32_t ticket, uint64_t agg) {
+  const int lane = threadIdx.x & 31;
+  const bool publish = (int64_t)ticket != P.skip_ticket;
+  if (ticket == 0) {
+    if (lane == 0 && publish) st_word64(P.state, kFlagIncl | agg);
+    return 0;
+  }
+  if (lane == 0 && publish) st_word64(P.state + ticket, kFlagAgg | agg);
+  const uint64_t excl = lookback_excl(P, ticket);
+  if (lane == 0 && publish) st_word64(P.state + ticket, kFlagIncl | (excl + agg));
   return excl;
 }
 
@@ -465,7 +473,7 @@ __global__ void __launch_bounds__(LT) kvc_lossless_enc(const LosslessParams P) {
 
     // decoupled look-back (warp 0): publish this chunk's aggregate, then add predecessors' until an inclusive prefix
     if (threadIdx.x < 32) {
-      const uint64_t excl = lookback_warp(P, ticket, asz, true);
+      const uint64_t excl = lookback_warp(P, ticket, asz);
       if (threadIdx.x == 0) {
         s_excl = excl;
         const uint64_t dst = P.data_start + excl;
@@ -496,33 +504,35 @@ __global__ void __launch_bounds__(LT) kvc_lossless_enc(const LosslessParams P) {
 // Fast encoder for the stage lists TUPL_8 [BIT_8] [DELTA_1] RZE_w (w = 1 or 2)
 // and chunk sizes that are multiples of 4 KiB up to 16 KiB.  A CTA holds eight
 // worker warps and one publisher warp.
-//  * Workers: a chunk arrives by cp.async into a swizzled input buffer.  TUPL_8
-//    (and BIT_8) run as one register transform per 8-tuple block (a 4x4 byte
+//  * Workers: each chunk arrives by cp.async in a slot of a ring.  TUPL_8 (and
+//    BIT_8) run as one register transform per 8-tuple block (a 4x4 byte
 //    transpose gathers byte j of the 8 tuples, an 8x8 bit transpose makes the 8
-//    bit-plane bytes) into a ring slot, stored with the same swizzle so that the
-//    next pass reads it without bank conflicts.  The input buffer is then free
-//    and the next chunk's load is issued.  DELTA_1 and RZE run as one register
-//    pass: a thread owns 64 contiguous bytes, takes the byte differences
-//    (__vsub4) and the word bitmaps, one block scan of its counts gives its
-//    output offsets, and the encoded chunk is written over its own input in the
-//    slot.  The encoded size is known before anything is written, so an
-//    incompressible chunk costs no compaction.  The chunk's aligned size is
-//    published for the look-back at once and the slot handed to the publisher.
-//  * Publisher: takes the slots in ticket order, finds each chunk's stream
-//    offset by the look-back over its predecessors (32 at a time), publishes
-//    the inclusive prefix, writes the chunk-table entry, copies the chunk to the
-//    stream and hands the slot back.  Workers never wait on other CTAs, only on
-//    a slot of their own ring.
-// Slots pass between the two sides through one "full" and one "empty" mbarrier
-// per slot; every wait is bounded and sets KVC_FLAG_TIMEOUT when it runs out.  A
+//    bit-plane bytes) into a scratch buffer, stored swizzled so that the next
+//    pass reads it without bank conflicts; then the next chunk's load is
+//    issued into the next slot.  DELTA_1 and RZE run as one register pass: a
+//    thread owns 64 contiguous bytes, takes the word bitmaps of the byte
+//    differences, and one block scan of its counts gives its output offsets.  The encoded size is known before anything is written, so the
+//    chunk's aligned size is published for the look-back right then, and an
+//    incompressible chunk costs no compaction: its slot still holds it as
+//    loaded.  Otherwise the encoded chunk is written over it.  The slot is then
+//    handed to the publisher.
+//  * Publisher: the workers announce each ticket the moment they take it, so
+//    the publisher walks back over the chunk's predecessors (32 at a time)
+//    while the chunk is still being encoded.  When the slot is full it
+//    publishes the inclusive prefix, writes the chunk-table entry, copies the
+//    chunk to the stream with one bulk copy and hands the slot back once the
+//    copy has read it.  Workers never wait on other CTAs, only on a slot of
+//    their own ring.
+// Tickets, full slots and free slots pass between the two sides through
+// mbarriers; every wait is bounded and sets KVC_FLAG_TIMEOUT when it runs out.  A
 // chunk whose length is not a multiple of 4 KiB (only the last one can be) runs
 // the generic stage functions on the worker threads.
 // ===========================================================================
 constexpr int FT = 256;        // worker threads
 constexpr int FW = FT + 32;    // workers + the publisher warp
-constexpr int kRing = 3;       // slots per CTA
+constexpr int kRing = 5;       // slots per CTA (16 KiB chunks: 2 CTAs per SM)
+constexpr int kFastCtasPerSm = 2;
 constexpr uint32_t kFastMaxChunk = 16384;
-constexpr uint32_t kEndTicket = 0xffffffffu;
 constexpr uint32_t kMbarTries = 1u << 20;
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
@@ -553,20 +563,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t par) {
   return false;
 }
 
-// 16-byte unit u of a fast chunk buffer is stored at swz(u): within each 64-byte
-// block the four units rotate by (block >> 1), so 8 lanes reading unit k of 8
-// consecutive blocks touch 8 distinct bank groups.  swzb is the same map on a
-// byte offset.
-__device__ __forceinline__ uint32_t swz(uint32_t u) { return (u & ~3u) | ((u + (u >> 3)) & 3u); }
+// The transform's output is stored swizzled: 16-byte unit u at unit
+// (u & ~3) | ((u + (u >> 3)) & 3), i.e. within each 64-byte block the four units
+// rotate by (block >> 1), so 8 lanes reading unit k of 8 consecutive blocks touch
+// 8 distinct bank groups.  swzb is that map on a byte offset.
 __device__ __forceinline__ uint32_t swzb(uint32_t x) { return (x & ~0x30u) | ((((x >> 4) + (x >> 7)) & 3u) << 4); }
 __device__ __forceinline__ bool fast_len(uint32_t n) { return (n & 4095u) == 0 && n <= kFastMaxChunk; }
 
 __device__ void issue_chunk_load(const LosslessParams &P, uint32_t t, uint8_t *dst) {
   const uint64_t off = (uint64_t)t * P.chunk_bytes;
   const uint32_t n = (uint32_t)min((uint64_t)P.chunk_bytes, P.payload_bytes - off);
-  const bool fast = fast_len(n);
   const uint8_t *src = P.payload + off;
-  for (uint32_t u = threadIdx.x; u < n / 16; u += FT) cp_async16(dst + 16 * (fast ? swz(u) : u), src + 16 * u);
+  for (uint32_t u = threadIdx.x; u < n / 16; u += FT) cp_async16(dst + 16 * u, src + 16 * u);
 }
 
 // 4x4 byte transpose: o[j] = byte j of a, b, c, d.
@@ -591,7 +599,7 @@ __device__ __forceinline__ void bits8x8(uint32_t &lo, uint32_t &hi) {
   hi ^= t >> 4;
 }
 
-// TUPL_8 (and BIT_8 after it) of a fast chunk, swizzled in and swizzled out.
+// TUPL_8 (and BIT_8 after it) of a fast chunk, plain in and swizzled out.
 // Without BIT_8, tuple byte j of block beta goes to byte 8*beta.. of row j (m
 // bytes per row); with BIT_8, bit p of those 8 bytes forms byte beta of row j of
 // bit plane p.  n is a multiple of 4 KiB, so a row start never changes the
@@ -602,10 +610,9 @@ __device__ void fast_transform(const uint8_t *in, uint8_t *out, uint32_t n) {
   for (uint32_t beta = threadIdx.x; beta < nblk; beta += FT) {
     uint32_t w[16];
     const uint4 *blk = reinterpret_cast<const uint4 *>(in) + 4 * beta;
-    const uint32_t rot = (beta >> 1) & 3u;
 #pragma unroll
     for (int k = 0; k < 4; k++) {
-      const uint4 v = blk[(k + rot) & 3u];
+      const uint4 v = blk[k];
       w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
     }
     uint32_t L0[4], L1[4], H0[4], H1[4];  // byte j (0..3 / 4..7) of tuples 0..3 / 4..7
@@ -632,16 +639,24 @@ __device__ void fast_transform(const uint8_t *in, uint8_t *out, uint32_t n) {
   bsync<FT>();
 }
 
-// DELTA_1 (optional) and RZE_w of a fast chunk held swizzled in `in`; the encoded
-// chunk goes to `out`, which may be `in` itself: every read happens before the
-// first barrier.  Returns the encoded size; nothing is written when it is >= n.
+// DELTA_1 (optional) and RZE_w of a transformed fast chunk held swizzled in `in`;
+// the encoded chunk goes to `out` (which may be `in` itself: every read happens
+// before the first barrier).  Returns the encoded size; nothing is written when it
+// is >= n.
+// Publishes chunk t's aligned encoded size for the look-back of its successors
+// (chunk 0's size is its inclusive prefix).
+__device__ __forceinline__ void publish_size(const LosslessParams &P, uint32_t t, uint32_t asz) {
+  if ((int64_t)t != P.skip_ticket) st_word64(P.state + t, (t == 0 ? kFlagIncl : kFlagAgg) | asz);
+}
+
 template <int W, bool DELTA>
-__device__ uint32_t fast_delta_rze(const uint8_t *in, uint8_t *out, uint32_t n, uint32_t *wsum) {
+__device__ uint32_t fast_delta_rze(const uint8_t *in, uint8_t *out, uint32_t n, uint32_t *wsum, const LosslessParams &P,
+                                   uint32_t ticket) {
   const uint32_t nthr = n / 64, nb = n / (8 * W), nb2 = nb / 8;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t t = threadIdx.x;
   const bool active = t < nthr;
-  uint32_t x[16];
+  uint32_t x[16], prevw = 0;  // prevw: byte 3 = the byte before this thread's first byte
 #pragma unroll
   for (int i = 0; i < 16; i++) x[i] = 0u;
   if (active) {
@@ -652,28 +667,25 @@ __device__ uint32_t fast_delta_rze(const uint8_t *in, uint8_t *out, uint32_t n, 
       const uint4 v = src[(k + rot) & 3u];
       x[4 * k] = v.x; x[4 * k + 1] = v.y; x[4 * k + 2] = v.z; x[4 * k + 3] = v.w;
     }
-    if (DELTA) {
-      // last byte of the previous block: logical unit 3 of block t - 1
-      uint32_t prev = t ? in[16 * (4 * (t - 1) + ((3u + ((t - 1) >> 1)) & 3u)) + 15] : 0u;
-#pragma unroll
-      for (int i = 0; i < 16; i++) {
-        const uint32_t cur = x[i];
-        x[i] = __vsub4(cur, (cur << 8) | prev);
-        prev = cur >> 24;
-      }
-    }
+    // last byte of the previous block: logical unit 3 of block t - 1
+    if (DELTA && t) prevw = (uint32_t)in[16 * (4 * (t - 1) + ((3u + ((t - 1) >> 1)) & 3u)) + 15] << 24;
   }
-  // word bitmap: W = 2 -> 32 words (one bit each, 4 bitmap bytes); W = 1 -> 64 bytes (8 bitmap bytes)
+  // A byte of DELTA_1's output is zero exactly when the byte equals the one before
+  // it, so the bitmaps only need x ^ (x shifted by one byte); the differences
+  // themselves are formed when a compressible chunk's elements are written.
+  // Word bitmap: W = 2 -> 32 words (one bit each, 4 bitmap bytes); W = 1 -> 64
+  // bytes (8 bitmap bytes).
   uint32_t blo = 0, bhi = 0;
 #pragma unroll
   for (int i = 0; i < 16; i++) {
+    const uint32_t e = DELTA ? x[i] ^ __byte_perm(i ? x[i - 1] : prevw, x[i], 0x6543) : x[i];
     if (W == 2) {
-      blo |= (uint32_t)((x[i] & 0xffffu) != 0u) << (2 * i);
-      blo |= (uint32_t)((x[i] >> 16) != 0u) << (2 * i + 1);
+      blo |= (uint32_t)((e & 0xffffu) != 0u) << (2 * i);
+      blo |= (uint32_t)((e >> 16) != 0u) << (2 * i + 1);
     } else {
 #pragma unroll
       for (int b = 0; b < 4; b++) {
-        const uint32_t bit = (uint32_t)(((x[i] >> (8 * b)) & 0xffu) != 0u);
+        const uint32_t bit = (uint32_t)(((e >> (8 * b)) & 0xffu) != 0u);
         if (i < 8) blo |= bit << (4 * i + b);
         else bhi |= bit << (4 * (i - 8) + b);
       }
@@ -705,6 +717,7 @@ __device__ uint32_t fast_delta_rze(const uint8_t *in, uint8_t *out, uint32_t n, 
   }
   const uint32_t totB = tot >> 16, totW = tot & 0xffffu;
   const uint32_t size = nb2 + totB + W * totW;
+  if (t == 0) publish_size(P, ticket, align16u(size < n ? size : n));  // before the compaction
   if (size >= n) return size;  // uniform: the chunk is stored raw
   const uint32_t ex = wb + sc - c;
   uint32_t rB = ex >> 16, rW = ex & 0xffffu;
@@ -719,6 +732,13 @@ __device__ uint32_t fast_delta_rze(const uint8_t *in, uint8_t *out, uint32_t n, 
 #pragma unroll
     for (int j = 0; j < 4; j++) nib |= (uint32_t)(((bhi >> (8 * j)) & 0xffu) != 0u) << (4 + j);
     if (active) out[t] = (uint8_t)nib;
+  }
+  if (DELTA) {  // byte-wise differences, mod 256 (no borrow crosses a byte)
+#pragma unroll
+    for (int i = 15; i >= 0; i--) {
+      const uint32_t a = x[i], b = __byte_perm(i ? x[i - 1] : prevw, x[i], 0x6543);
+      x[i] = ((a | 0x80808080u) - (b & 0x7f7f7f7fu)) ^ ((a ^ ~b) & 0x80808080u);
+    }
   }
   if (active) {
     uint8_t *oB = out + nb2, *oW = out + nb2 + totB;
@@ -754,15 +774,20 @@ struct FastSpec {
   uint32_t bit8, delta1, rze_w, pad;
 };
 
-__global__ void __launch_bounds__(FW, 3) kvc_lossless_enc_fast(const LosslessParams P, const FastSpec F) {
+__global__ void __launch_bounds__(FW, kFastCtasPerSm) kvc_lossless_enc_fast(const LosslessParams P, const FastSpec F) {
   extern __shared__ uint4 smem_u4[];
   const uint32_t cb = P.chunk_bytes, slot_bytes = cb + 64;
-  uint8_t *const IN = reinterpret_cast<uint8_t *>(smem_u4);  // input buffer
-  uint8_t *const ring = IN + slot_bytes;                       // slot s at ring + s * slot_bytes
+  uint8_t *const A = reinterpret_cast<uint8_t *>(smem_u4);  // transform output (swizzled)
+  uint8_t *const ring = A + slot_bytes;                      // slot s at ring + s * slot_bytes
   uint16_t *Bs = reinterpret_cast<uint16_t *>(ring + kRing * slot_bytes);                       // generic-path bitmap
   uint32_t *wsum = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(Bs) + cb / 8 + 64);  // scan words
-  __shared__ __align__(8) uint64_t s_full[kRing], s_empty[kRing];
-  __shared__ uint32_t s_meta[kRing][2];  // ticket, table word (size | raw bit)
+  // Chunk k of this CTA lives in slot k % kRing: loaded there, encoded over itself
+  // when it compresses, copied out from there either way.  tick[j]: the ticket of
+  // chunk k (k % 2kRing == j) is announced, a value >= n_chunks meaning "no more
+  // chunks"; full[s]: the slot holds the chunk's stored bytes; empty[s]: the
+  // publisher is done with the slot.
+  __shared__ __align__(8) uint64_t s_tick[2 * kRing], s_full[kRing], s_empty[kRing];
+  __shared__ uint32_t s_ticket[2 * kRing], s_word[kRing], s_from_payload[kRing];
   __shared__ uint32_t s_t;
   const uint32_t nc = P.n_chunks;
   uint32_t *ticket_ctr = P.ctrl + kCtrlTicket;
@@ -771,6 +796,7 @@ __global__ void __launch_bounds__(FW, 3) kvc_lossless_enc_fast(const LosslessPar
       mbar_init(&s_full[s], 1);
       mbar_init(&s_empty[s], 1);
     }
+    for (int j = 0; j < 2 * kRing; j++) mbar_init(&s_tick[j], 1);
     s_t = atomicAdd(ticket_ctr, 1u);
   }
   __syncthreads();
@@ -778,18 +804,25 @@ __global__ void __launch_bounds__(FW, 3) kvc_lossless_enc_fast(const LosslessPar
   if (threadIdx.x >= FT) {  // ---- publisher warp
     const int lane = threadIdx.x & 31;
     for (uint32_t k = 0;; k++) {
-      const uint32_t s = k % kRing;
+      const uint32_t j = k % (2 * kRing), s = k % kRing;
+      if (!mbar_wait(&s_tick[j], (k / (2 * kRing)) & 1u)) {
+        if (lane == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
+        break;
+      }
+      const uint32_t t = s_ticket[j];
+      if (t >= nc) break;
+      // the predecessors' sizes do not depend on this chunk: walk back while
+      // the workers are still encoding it
+      const uint64_t excl = t ? lookback_excl(P, t) : 0ull;
       if (!mbar_wait(&s_full[s], (k / kRing) & 1u)) {
         if (lane == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
         break;
       }
-      const uint32_t t = s_meta[s][0], word = s_meta[s][1];
-      if (t == kEndTicket) break;
-      const bool raw = (word >> 31) != 0;
+      const uint32_t word = s_word[s];
       const uint32_t asz = align16u(word & 0x7fffffffu);
-      const uint64_t excl = lookback_warp(P, t, asz, false);
       const uint64_t dst = P.data_start + excl;
       if (lane == 0) {
+        if (t && (int64_t)t != P.skip_ticket) st_word64(P.state + t, kFlagIncl | (excl + asz));
         if (dst + asz > P.stream_cap) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CAPACITY);
         reinterpret_cast<uint32_t *>(P.stream + KVC_HEADER_BYTES)[t] = word;
         if (t == nc - 1) {
@@ -799,53 +832,65 @@ __global__ void __launch_bounds__(FW, 3) kvc_lossless_enc_fast(const LosslessPar
         }
       }
       if (dst + asz <= P.stream_cap) {
-        uint4 *o = reinterpret_cast<uint4 *>(P.stream + dst);
-        if (raw) {
+        if (s_from_payload[s]) {  // a raw chunk whose slot the generic stages overwrote
+          uint4 *o = reinterpret_cast<uint4 *>(P.stream + dst);
           const uint4 *g = reinterpret_cast<const uint4 *>(P.payload + (uint64_t)t * cb);
           for (uint32_t i = lane; i < asz / 16; i += 32) o[i] = __ldg(g + i);
-        } else {
-          const uint4 *sm = reinterpret_cast<const uint4 *>(ring + s * slot_bytes);
-#pragma unroll 4
-          for (uint32_t i = lane; i < asz / 16; i += 32) o[i] = sm[i];
+        } else if (lane == 0) {
+          // one bulk copy from the slot; the slot is free once it has been read
+          asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(P.stream + dst),
+                       "r"(smem_addr(ring + s * slot_bytes)), "r"(asz)
+                       : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[s]);
     }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     return;
   }
 
   // ---- workers
   uint32_t t = s_t;
-  if (t < nc) issue_chunk_load(P, t, IN);
+  if (threadIdx.x == 0) {
+    s_ticket[0] = t;
+    mbar_arrive(&s_tick[0]);
+  }
+  if (t < nc) issue_chunk_load(P, t, ring);
   cp_async_commit();
-  uint32_t k = 0;
-  for (; t < nc; k++) {
-    const uint32_t s = k % kRing;
-    uint8_t *const A = ring + s * slot_bytes;
-    if (threadIdx.x == 0 && k >= kRing && !mbar_wait(&s_empty[s], (k / kRing - 1) & 1u))
-      atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
+  for (uint32_t k = 0; t < nc; k++) {
+    const uint32_t s = k % kRing, s1 = (k + 1) % kRing, jn = (k + 1) % (2 * kRing);
+    uint8_t *const S = ring + s * slot_bytes;
     cp_async_wait<0>();
     bsync<FT>();
 
     const uint64_t off = (uint64_t)t * cb;
     const uint32_t n = (uint32_t)min((uint64_t)cb, P.payload_bytes - off);
     uint32_t size = n, tn;
-    bool raw;
+    bool raw, from_payload = false;
     if (fast_len(n)) {
-      if (threadIdx.x == 0) s_t = atomicAdd(ticket_ctr, 1u);
-      if (F.bit8) fast_transform<true>(IN, A, n);
-      else fast_transform<false>(IN, A, n);
+      if (threadIdx.x == 0) {  // the next chunk: announced to the publisher at once, loaded after the transform
+        s_t = s_ticket[jn] = atomicAdd(ticket_ctr, 1u);
+        mbar_arrive(&s_tick[jn]);
+        if (k + 1 >= kRing && !mbar_wait(&s_empty[s1], ((k + 1) / kRing - 1) & 1u))
+          atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
+      }
+      if (F.bit8) fast_transform<true>(S, A, n);
+      else fast_transform<false>(S, A, n);
       tn = s_t;
-      if (tn < nc) issue_chunk_load(P, tn, IN);
+      if (tn < nc) issue_chunk_load(P, tn, ring + s1 * slot_bytes);
       cp_async_commit();
       uint32_t rs;
-      if (F.rze_w == 2) rs = F.delta1 ? fast_delta_rze<2, true>(A, A, n, wsum) : fast_delta_rze<2, false>(A, A, n, wsum);
-      else rs = F.delta1 ? fast_delta_rze<1, true>(A, A, n, wsum) : fast_delta_rze<1, false>(A, A, n, wsum);
-      raw = rs >= n;  // stored raw: the publisher copies the chunk from the payload
+      if (F.rze_w == 2)
+        rs = F.delta1 ? fast_delta_rze<2, true>(A, S, n, wsum, P, t) : fast_delta_rze<2, false>(A, S, n, wsum, P, t);
+      else
+        rs = F.delta1 ? fast_delta_rze<1, true>(A, S, n, wsum, P, t) : fast_delta_rze<1, false>(A, S, n, wsum, P, t);
+      raw = rs >= n;  // stored raw: the slot still holds the chunk as loaded
       if (!raw) size = rs;
     } else {
-      uint8_t *cur_b = IN, *nxt_b = A;
+      uint8_t *cur_b = S, *nxt_b = A;
       for (uint32_t st = 0; st + 1 < P.n_stages; st++) {
         const uint32_t kind = P.kind[st], prm = P.param[st];
         if (kind == KVC_ST_TUPL) tupl_encode<FT>(cur_b, nxt_b, n, prm);
@@ -857,34 +902,36 @@ __global__ void __launch_bounds__(FW, 3) kvc_lossless_enc_fast(const LosslessPar
       raw = rs >= n;
       if (!raw) {
         size = rs;
-        if (nxt_b != A) {
+        if (nxt_b != S) {
           for (uint32_t i = threadIdx.x; i < align16u(rs) / 16; i += FT)
-            reinterpret_cast<uint4 *>(A)[i] = reinterpret_cast<const uint4 *>(nxt_b)[i];
+            reinterpret_cast<uint4 *>(S)[i] = reinterpret_cast<const uint4 *>(nxt_b)[i];
         }
+      } else {
+        from_payload = P.n_stages > 1;  // the stages wrote over the slot
       }
-      if (threadIdx.x == 0) s_t = atomicAdd(ticket_ctr, 1u);
+      if (threadIdx.x == 0) {
+        publish_size(P, t, align16u(size));
+        s_t = s_ticket[jn] = atomicAdd(ticket_ctr, 1u);
+        mbar_arrive(&s_tick[jn]);
+        if (k + 1 >= kRing && !mbar_wait(&s_empty[s1], ((k + 1) / kRing - 1) & 1u))
+          atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
+      }
       bsync<FT>();
       tn = s_t;
-      if (tn < nc) issue_chunk_load(P, tn, IN);
+      if (tn < nc) issue_chunk_load(P, tn, ring + s1 * slot_bytes);
       cp_async_commit();
     }
     const uint32_t asz = align16u(size);
-    if (!raw && threadIdx.x < asz - size) A[size + threadIdx.x] = 0;
+    if (!raw && threadIdx.x < asz - size) S[size + threadIdx.x] = 0;
     if (threadIdx.x == 0) {
-      if ((int64_t)t != P.skip_ticket) st_word64(P.state + t, (t == 0 ? kFlagIncl : kFlagAgg) | asz);
-      s_meta[s][0] = t;
-      s_meta[s][1] = size | (raw ? 0x80000000u : 0u);
+      s_word[s] = size | (raw ? 0x80000000u : 0u);
+      s_from_payload[s] = from_payload;
     }
+    // the publisher reads the slot through the bulk-copy (async) proxy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     bsync<FT>();
     if (threadIdx.x == 0) mbar_arrive(&s_full[s]);
     t = tn;
-  }
-  if (threadIdx.x == 0) {  // tell the publisher to stop
-    const uint32_t s = k % kRing;
-    if (k >= kRing && !mbar_wait(&s_empty[s], (k / kRing - 1) & 1u))
-      atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
-    s_meta[s][0] = kEndTicket;
-    mbar_arrive(&s_full[s]);
   }
   cp_async_wait<0>();
 }
