@@ -272,6 +272,22 @@ __device__ __forceinline__ float fmax3_n(float a, float b, float c) {
   asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+// Element-wise minimum / maximum of two packed 16-bit pairs (bf16x2 or f16x2),
+// NaN-propagating; exact, like the binary32 versions on the widened values.
+template <bool BF16>
+__device__ __forceinline__ uint32_t pmin2_n(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if (BF16) asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else asm("min.NaN.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <bool BF16>
+__device__ __forceinline__ uint32_t pmax2_n(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if (BF16) asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 __device__ __forceinline__ bool finite2(float a, float b) { return fabsf(a) <= 3.402823466e38f && fabsf(b) <= 3.402823466e38f; }
 
 // ---------------------------------------------------------------------------
@@ -309,6 +325,18 @@ __device__ __forceinline__ float2 qfast2(float2 y, float2 z2, float2 r2, bool &b
   const float2 d = sub2(p, k);
   const float thr = tie_threshold<BITS>();
   bad |= !(fabsf(d.x) < thr) || !(fabsf(d.y) < thr);
+  return u;
+}
+
+// qfast2 that keeps the largest |p - rint(p)| seen in dm instead of a flag: the
+// pair is safe while dm < tie_threshold<BITS>() (a NaN dm fails that test too).
+__device__ __forceinline__ float2 qfast2m(float2 y, float2 z2, float2 r2, float &dm) {
+  const float2 t = sub2(y, z2);
+  const float2 p = mul2(t, r2);
+  const float2 u = add2(p, bcast2(kRintMagic));
+  const float2 k = sub2(u, bcast2(kRintMagic));
+  const float2 d = sub2(p, k);
+  dm = fmax3_n(fabsf(d.x), fabsf(d.y), dm);
   return u;
 }
 

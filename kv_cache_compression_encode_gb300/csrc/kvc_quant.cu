@@ -508,116 +508,50 @@ __global__ void __launch_bounds__(kThreads) kvc_enc_tile(const QuantParams P) {
 // ---------------------------------------------------------------------------
 // key tile, groups over tokens (the key default): kvc_enc_ktile
 //
-// Per (layer, head, 128-token) tile, 256 threads:
-//  A  each thread reads 8 rows x 8 channels of the raw tile from the stage buffer
-//     (filled by cp.async during the previous tile), takes the smoothing
-//     statistics, applies the smoothing and stores x' into Y;
-//  C  (Hadamard) a lane owns 32 consecutive channels of a row and runs the
-//     butterfly strides 1..16 in registers;
-//  D  a thread owns channels {c, c+32, c+64, c+96} x 16 tokens: strides 32 and 64
-//     in registers, normalization, per-channel group statistics (combined across
-//     the token segments through shared memory), quantization and packing of
-//     its 16 codes per channel straight into the channel's record.
-// Y has no padding: float4 chunk q of part p (32 channels) of row r sits at
-// chunk 8p + ((q + p + 4(r & 1)) & 7), which keeps the row pass, the column pass
-// and the phase-A stores free of bank conflicts.
+// Per (layer, head, 128-token) tile, 512 threads, four barriers:
+//  A  (smoothing only) warp w takes channel octet w over all 128 rows of the
+//     stage (lane l: rows l + 32i).  The per-channel minima and maxima run on
+//     the packed 16-bit pairs and are reduced across the warp by a halving
+//     butterfly; one lane per channel turns them into the smoothing parameters
+//     (sign folded into the power-of-two scale) in a shared table.
+//  C  thread (row r, part p) reads its 32 channels of row r from the stage and
+//     smooths them (or flips their signs); the stage is then free for the next
+//     tile's cp.async.  The Hadamard butterflies run with strides 1..16 in
+//     registers and strides 32 and 64 with the lanes holding the row's other
+//     parts (shuffles); the scaled row goes to the fp32 tile Y.
+//  D  thread (channel c, quarter q) takes rows 32q..32q+31 of channel c from Y:
+//     group minimum and maximum in registers plus one or two shuffles (groups
+//     of 64 or 128 tokens), the group parameters, its 32 codes (packed by
+//     integer multiply-adds), one store into the channel's record.
+// Stage: 16-byte chunk k of row r sits at chunk k ^ (r & 7) ^ ((k >> 2) & 2).
+// Y: float4 column k of row r sits at k ^ (r & 1) ^ (((k >> 3) & 3) << 1) ^
+// (((r >> 5) & 3) << 1).  With these, the cp.async writes, the A and C reads of
+// the stage, the C writes and the D reads of Y are all free of bank conflicts.
 // ---------------------------------------------------------------------------
-constexpr size_t kKtileSmem = (size_t)128 * 128 * 4 + 128 * 256 + 2 * 8 * 128 * 4 + 2 * 128 * 4;
+constexpr int kKT = 512;
+constexpr int kTabStride = 36;  // floats per 32-channel part in the parameter tables (spreads the parts over banks)
+constexpr size_t kKtileSmem = (size_t)128 * 128 * 4 + 128 * 256 + 2 * 4 * kTabStride * 4;
 
-__device__ __forceinline__ int kchunk(int lc, int r) {
-  const int p = lc >> 3, q = lc & 7;
-  return 8 * p + ((q + p + 4 * (r & 1)) & 7);
+__device__ __forceinline__ uint32_t stage_chunk(uint32_t k, uint32_t r) { return k ^ (r & 7u) ^ ((k >> 2) & 2u); }
+__device__ __forceinline__ uint32_t ycol4(uint32_t k, uint32_t r) {
+  return k ^ (r & 1u) ^ (((k >> 3) & 3u) << 1) ^ (((r >> 5) & 3u) << 1);
 }
-__device__ __forceinline__ int kcol(int col, int r) { return 4 * kchunk(col >> 2, r) + (col & 3); }
 
 __device__ __forceinline__ void cp_async16_q(void *smem, const void *gmem) {
-  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit_q() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all_q() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-// Copy the raw rows of `tile` this thread will read in phase A (rows rg + 16i,
-// 16-byte chunk c8) into the stage buffer; absent rows are zero-filled.
-__device__ __forceinline__ void ktile_issue(const QuantParams &P, uint32_t tile, uint8_t *stage, int rg, int c8,
-                                            uint32_t &flags) {
-  const uint32_t n_sb = P.n_sb, H = P.g.H;
-  const uint32_t sb = tile % n_sb, lh = tile / n_sb, h = lh % H, l = lh / H;
+// Thread (rg = tid / 16, k = tid % 16) copies chunk k of rows rg + 32i (i < 4) of
+// `tile` into the stage; rows past the end of the tensor are left as they are
+// (no phase reads them), a bad page is zero-filled and flagged.
+__device__ __forceinline__ void ktile_issue(const QuantParams &P, uint32_t sb, uint32_t h, uint32_t l, uint8_t *stage,
+                                            int rg, int k, uint32_t &flags) {
   const uint32_t t0 = sb * kSmoothBlock, nvalid = min((uint32_t)kSmoothBlock, P.g.T - t0);
-  const uint8_t *lbase = static_cast<const uint8_t *>(P.layers[l]);
-#pragma unroll
-  for (int i = 0; i < 8; i++) {
-    const uint32_t r = rg + 16 * i;
-    uint8_t *dst = stage + r * 256 + 16 * c8;
-    if (r < nvalid) {
-      const uint64_t ro = row_offset(P.g, t0 + r);
-      if (ro == ~0ull) {
-        flags |= KVC_FLAG_BAD_PAGE;
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
-      } else {
-        cp_async16_q(dst, lbase + ro + (size_t)(h * kHeadDim + 8 * c8) * 2);
-      }
-    }
-  }
-  cp_async_commit_q();
-}
-
-// 16 codes (BITS each) -> the channel's 2*BITS bytes inside its record.
-template <int BITS>
-__device__ __forceinline__ void store_code_words(uint8_t *dst, const uint32_t (&w)[(16 * BITS + 31) / 32]) {
-  if constexpr (BITS == 2) {
-    *reinterpret_cast<uint32_t *>(dst) = w[0];
-  } else if constexpr (BITS == 4) {
-    *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
-  } else if constexpr (BITS == 8) {
-    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-  } else {  // 48 bits, 2-byte aligned
-    uint16_t *d16 = reinterpret_cast<uint16_t *>(dst);
-    d16[0] = (uint16_t)w[0];
-    d16[1] = (uint16_t)(w[0] >> 16);
-    d16[2] = (uint16_t)w[1];
-  }
-}
-
-// In-lane butterflies of 32 channels held as 16 pairs: stride 1 within pairs, 2..16 between pairs.
-__device__ __forceinline__ void fwht32_pairs(float2 (&w)[16]) {
-#pragma unroll
-  for (int i = 0; i < 16; i++) {
-    const float a = w[i].x, b = w[i].y;
-    w[i] = make_float2(__fadd_rn(a, b), __fsub_rn(a, b));
-  }
-#pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 16; i++)
-      if ((i & h) == 0) {
-        const float2 a = w[i], b = w[i + h];
-        w[i] = add2(a, b);
-        w[i + h] = sub2(a, b);
-      }
-  }
-}
-
-// Key tile with 512 threads (kvc_enc_ktile): per (layer, head, 128-token) tile
-//  A  thread (rg = tid/16, c8 = tid%16) takes rows rg + 32i (i < 4) x 8 channels
-//     from the stage buffer; smoothing statistics combine through the idle tile
-//     buffer; the smoothed rows (signs folded into the power-of-two scale) go to Y;
-//  C  one row per lane quarter-warp: butterfly strides 1..16 in registers;
-//  D  thread (cq = lane, rs = warp) takes channels {cq + 32k} x rows 8rs .. 8rs+7:
-//     strides 32/64 and the normalization in registers, per-channel statistics of
-//     its 8 rows; one thread per (group, channel) then turns the segment partials
-//     into the group's parameters (written once to a shared table and to the
-//     metadata section); every thread quantizes and packs its 8 codes per channel.
-constexpr int kKT = 512;
-constexpr size_t kKtile3Smem = (size_t)128 * 128 * 4 + 128 * 256 + 4 * 128 * 16 + 2 * 128 * 4;
-
-__device__ __forceinline__ void ktile3_issue(const QuantParams &P, uint32_t tile, uint8_t *stage, int rg, int c8,
-                                             uint32_t &flags) {
-  const uint32_t n_sb = P.n_sb, H = P.g.H;
-  const uint32_t sb = tile % n_sb, lh = tile / n_sb, h = lh % H, l = lh / H;
-  const uint32_t t0 = sb * kSmoothBlock, nvalid = min((uint32_t)kSmoothBlock, P.g.T - t0);
-  const uint8_t *lbase = static_cast<const uint8_t *>(P.layers[l]) + (size_t)(h * kHeadDim + 8 * c8) * 2;
-  uint8_t *dst = stage + rg * 256 + 16 * c8;
+  const uint8_t *lbase = static_cast<const uint8_t *>(P.layers[l]) + (size_t)(h * kHeadDim + 8 * k) * 2;
+  uint8_t *dst = stage + rg * 256 + 16 * stage_chunk(k, rg);  // r & 7 is the same for rows rg + 32i
   if (!P.g.block_table) {
     const uint64_t ts = P.g.token_stride;
     const uint8_t *src = lbase + (uint64_t)(t0 + rg) * ts;
@@ -642,311 +576,325 @@ __device__ __forceinline__ void ktile3_issue(const QuantParams &P, uint32_t tile
   cp_async_commit_q();
 }
 
-template <int BITS>
-__device__ __forceinline__ void store_codes8(uint8_t *dst, uint32_t lo, uint32_t hi) {
-  if constexpr (BITS == 2) *reinterpret_cast<uint16_t *>(dst) = (uint16_t)lo;
-  else if constexpr (BITS == 4) *reinterpret_cast<uint32_t *>(dst) = lo;
-  else if constexpr (BITS == 8) *reinterpret_cast<uint2 *>(dst) = make_uint2(lo, hi);
-  else {
-    dst[0] = (uint8_t)lo;
-    dst[1] = (uint8_t)(lo >> 8);
-    dst[2] = (uint8_t)(lo >> 16);
+// In-lane butterflies of 32 channels held as 16 pairs: stride 1 within pairs, 2..16 between pairs.
+__device__ __forceinline__ void fwht32_pairs(float2 (&w)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; i++) {
+    const float a = w[i].x, b = w[i].y;
+    w[i] = make_float2(__fadd_rn(a, b), __fsub_rn(a, b));
+  }
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; i++)
+      if ((i & h) == 0) {
+        const float2 a = w[i], b = w[i + h];
+        w[i] = add2(a, b);
+        w[i + h] = sub2(a, b);
+      }
   }
 }
+
+// 32 codes (BITS each, 4*BITS bytes) into a record segment.
+template <int BITS>
+__device__ __forceinline__ void store_codes32(uint8_t *dst, const uint32_t (&cw)[BITS]) {
+  if constexpr (BITS == 2) {
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(cw[0], cw[1]);
+  } else if constexpr (BITS == 4) {
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  } else if constexpr (BITS == 8) {
+    reinterpret_cast<uint4 *>(dst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    reinterpret_cast<uint4 *>(dst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < BITS; i++) reinterpret_cast<uint32_t *>(dst)[i] = cw[i];
+  }
+}
+
+// Codes of 32 qfast2 sums (bits 0x4B400000 + code, the code in the low byte) into
+// BITS words, LSB first.  2 and 4 bits: the codes of a byte are gathered with
+// integer multiply-adds (the magic's low byte is 0, so the low byte of
+// u1 * 2^BITS + u0 is code0 | code1 << BITS), bytes into words by byte_perm.
+template <int BITS>
+__device__ __forceinline__ void pack_sums32(const uint32_t (&u)[32], uint32_t (&cw)[BITS]) {
+  if constexpr (BITS == 4 || BITS == 2 || BITS == 8) {
+    constexpr int per_byte = 8 / BITS;
+    uint32_t b[4 * BITS];  // one byte (in the low 8 bits) per 8 / BITS codes
+#pragma unroll
+    for (int i = 0; i < 4 * BITS; i++) {
+      uint32_t x = u[per_byte * i + per_byte - 1];
+#pragma unroll
+      for (int j = per_byte - 2; j >= 0; j--) x = x * (1u << BITS) + u[per_byte * i + j];
+      b[i] = x;
+    }
+#pragma unroll
+    for (int w = 0; w < BITS; w++)
+      cw[w] = __byte_perm(__byte_perm(b[4 * w], b[4 * w + 1], 0x0040), __byte_perm(b[4 * w + 2], b[4 * w + 3], 0x0040),
+                          0x5410);
+  } else {
+#pragma unroll
+    for (int i = 0; i < BITS; i++) cw[i] = 0u;
+#pragma unroll
+    for (int i = 0; i < 32; i++) put_code<BITS>(cw, i, u[i]);
+  }
+}
+
+// Tile coordinates, advanced by a fixed number of tiles without divisions.
+struct TilePos {
+  uint32_t sb, h, l;
+  __device__ __forceinline__ void init(uint32_t tile, uint32_t n_sb, uint32_t H) {
+    sb = tile % n_sb;
+    const uint32_t lh = tile / n_sb;
+    h = lh % H;
+    l = lh / H;
+  }
+  // step = dsb + n_sb * (dh + H * dl) tiles, with dsb < n_sb and dh < H
+  __device__ __forceinline__ void advance(uint32_t dsb, uint32_t dh, uint32_t dl, uint32_t n_sb, uint32_t H) {
+    sb += dsb;
+    uint32_t c = sb >= n_sb;
+    sb -= c ? n_sb : 0u;
+    h += dh + c;
+    c = h >= H;
+    h -= c ? H : 0u;
+    l += dl + c;
+  }
+};
 
 template <int BITS, bool HAD, bool BF16>
 __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P) {
   extern __shared__ float4 smem_f4[];
-  float *Y = reinterpret_cast<float *>(smem_f4);                       // [128][128] swizzled; also reduction space
-  uint8_t *stage = reinterpret_cast<uint8_t *>(Y + 128 * 128);          // [128][256] raw rows of the next tile
-  float4 *prm = reinterpret_cast<float4 *>(stage + 128 * 256);          // [4 groups][128] {z, r, s, meta}
-  float *mu_s = reinterpret_cast<float *>(prm + 4 * 128);
-  float *inv_s = mu_s + 128;
+  float *Y = reinterpret_cast<float *>(smem_f4);                     // [128][128] fp32, swizzled
+  uint8_t *stage = reinterpret_cast<uint8_t *>(Y + 128 * 128);        // [128][256 B] raw rows, swizzled
+  float *tab_mu = reinterpret_cast<float *>(stage + 128 * 256);       // [4 parts][kTabStride]
+  float *tab_inv = tab_mu + 4 * kTabStride;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr bool bf16 = BF16;
   const uint32_t H = P.g.H, T = P.g.T, n_sb = P.n_sb, G = P.group;
   const uint32_t n_tiles = P.g.L * H * n_sb;
-  const int rg = tid >> 4, c8 = tid & 15;
   const bool smooth = P.smooth != 0;
   uint32_t flags = 0;
 
-  // tile-invariant quantities
-  const int spg = (int)(G >> 3);                      // 8-row segments per group
-  const int tiles_groups = 128 / (int)G;              // token groups per tile
-  const int my_gi = (8 * warp) / (int)G;              // phase-D group of this warp's rows
-  const uint32_t rec_bytes = G * BITS / 8;
-  const uint32_t my_seg_off = (uint32_t)(((8 * warp) % (int)G) / 8) * BITS;
-  const int chA = kchunk(2 * c8, rg), chB = kchunk(2 * c8 + 1, rg);  // phase-A store chunks (rg parity fixed)
-  // phase-D column offsets: channel cq + 32k of an even / odd row
-  int coff[8];
-#pragma unroll
-  for (int k = 0; k < 4; k++) {
-    coff[2 * k] = kcol(lane + 32 * k, 0);
-    coff[2 * k + 1] = kcol(lane + 32 * k, 1);
-  }
+  // tile-invariant thread roles and offsets
+  const int rg = tid >> 4, kq = tid & 15;                  // cp.async: rows rg + 32i, chunk kq
+  const uint32_t a_chunk = stage_chunk(warp, lane);          // A: chunk `warp` of rows lane + 32i
+  const int cr = tid >> 2, cp = tid & 3;                   // C: row cr, channels 32cp .. 32cp + 31
+  const uint32_t c_xs = (cr & 7) ^ (cp & 2);               // C: stage chunk 4cp + i sits at (4cp + i) ^ c_xs
+  const uint32_t c_xy = ycol4(8 * cp, cr) & 7u;            // C: Y float4 column 8cp + j sits at 8cp + (j ^ c_xy)
+  const int dc = 8 * warp + (lane >> 2), dq = lane & 3;    // D: channel dc, rows 32dq .. 32dq + 31
+  const float *Yd0 = Y + 32 * dq * 128 + 4 * (int)ycol4(dc >> 2, 32 * dq) + (dc & 3);      // even rows
+  const float *Yd1 = Y + 32 * dq * 128 + 4 * (int)ycol4(dc >> 2, 32 * dq + 1) + (dc & 3);  // odd rows
+  const int tiles_groups = 128 / (int)G;
+  const uint32_t rec_bytes = G * BITS / 8, seg_off = (uint32_t)((32 * dq) % (int)G) * BITS / 8;
+  const bool d_first = ((32 * dq) % (int)G) == 0;          // D: the quarter that starts its group writes the metadata
+  // the persistent grid advances by gridDim.x tiles
+  const uint32_t step_lh = gridDim.x / n_sb, step_sb = gridDim.x % n_sb;
+  const uint32_t step_h = step_lh % H, step_l = step_lh / H;
 
   uint32_t tile = blockIdx.x;
-  if (tile < n_tiles) ktile3_issue(P, tile, stage, rg, c8, flags);
+  TilePos cur, nxt;
+  cur.init(tile < n_tiles ? tile : 0u, n_sb, H);
+  if (tile < n_tiles) ktile_issue(P, cur.sb, cur.h, cur.l, stage, rg, kq, flags);
   for (; tile < n_tiles; tile += gridDim.x) {
-    const uint32_t sb = tile % n_sb, lh = tile / n_sb;
-    const uint32_t t0 = sb * kSmoothBlock;
-    const uint32_t nvalid = min((uint32_t)kSmoothBlock, T - t0);
-
-    // ---- A
+    const uint32_t sb = cur.sb, lh = cur.l * H + cur.h;
+    const uint32_t nvalid = min((uint32_t)kSmoothBlock, T - sb * kSmoothBlock);
+    nxt = cur;
+    nxt.advance(step_sb, step_h, step_l, n_sb, H);
     cp_async_wait_all_q();
-    float2 x[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const uint32_t r = rg + 32 * i;
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (r < nvalid) w = *reinterpret_cast<const uint4 *>(stage + r * 256 + 16 * c8);
-      x[i][0] = unpack_pair(w.x, bf16);
-      x[i][1] = unpack_pair(w.y, bf16);
-      x[i][2] = unpack_pair(w.z, bf16);
-      x[i][3] = unpack_pair(w.w, bf16);
-    }
-    if (tile + gridDim.x < n_tiles) ktile3_issue(P, tile + gridDim.x, stage, rg, c8, flags);
+    __syncthreads();  // the stage holds this tile; every thread is done with the previous Y
 
+    // ---- A: smoothing parameters.  Minima and maxima run on the packed 16-bit
+    // pairs (exact); lanes 8j..8j+7 end with pair j (channels 2j, 2j+1 of the octet).
     if (smooth) {
-      float mn[8], mx[8];
+      const uint32_t pinf = BF16 ? 0x7f807f80u : 0x7c007c00u, ninf = pinf | 0x80008000u;
+      uint32_t mn[4] = {pinf, pinf, pinf, pinf}, mx[4] = {ninf, ninf, ninf, ninf};
 #pragma unroll
-      for (int j = 0; j < 4; j++) {
-        mn[2 * j] = mx[2 * j] = x[0][j].x;
-        mn[2 * j + 1] = mx[2 * j + 1] = x[0][j].y;
-      }
-      if (nvalid == 128) {
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-          mn[2 * j] = fmin3_n(mn[2 * j], x[1][j].x, x[2][j].x);
-          mn[2 * j] = fmin_n(mn[2 * j], x[3][j].x);
-          mx[2 * j] = fmax3_n(mx[2 * j], x[1][j].x, x[2][j].x);
-          mx[2 * j] = fmax_n(mx[2 * j], x[3][j].x);
-          mn[2 * j + 1] = fmin3_n(mn[2 * j + 1], x[1][j].y, x[2][j].y);
-          mn[2 * j + 1] = fmin_n(mn[2 * j + 1], x[3][j].y);
-          mx[2 * j + 1] = fmax3_n(mx[2 * j + 1], x[1][j].y, x[2][j].y);
-          mx[2 * j + 1] = fmax_n(mx[2 * j + 1], x[3][j].y);
+      for (int i = 0; i < 4; i++) {
+        const int r = lane + 32 * i;
+        if (r < (int)nvalid) {
+          const uint4 u = *reinterpret_cast<const uint4 *>(stage + r * 256 + 16 * a_chunk);
+          mn[0] = pmin2_n<BF16>(mn[0], u.x); mx[0] = pmax2_n<BF16>(mx[0], u.x);
+          mn[1] = pmin2_n<BF16>(mn[1], u.y); mx[1] = pmax2_n<BF16>(mx[1], u.y);
+          mn[2] = pmin2_n<BF16>(mn[2], u.z); mx[2] = pmax2_n<BF16>(mx[2], u.z);
+          mn[3] = pmin2_n<BF16>(mn[3], u.w); mx[3] = pmax2_n<BF16>(mx[3], u.w);
         }
-      } else {
-#pragma unroll
-        for (int i = 1; i < 4; i++)
-          if (rg + 32 * i < (int)nvalid)
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-              mn[2 * j] = fmin_n(mn[2 * j], x[i][j].x);
-              mx[2 * j] = fmax_n(mx[2 * j], x[i][j].x);
-              mn[2 * j + 1] = fmin_n(mn[2 * j + 1], x[i][j].y);
-              mx[2 * j + 1] = fmax_n(mx[2 * j + 1], x[i][j].y);
-            }
       }
-      const bool mine = rg < (int)nvalid, other = (rg ^ 1) < (int)nvalid;
+      // halving butterfly (offsets 16, 8), then the rest of the lanes (4, 2, 1)
 #pragma unroll
-      for (int j = 0; j < 8; j++) {
-        const float oa = __shfl_xor_sync(kFull, mn[j], 16), ob = __shfl_xor_sync(kFull, mx[j], 16);
-        if (!mine) { mn[j] = oa; mx[j] = ob; }
-        else if (other) { mn[j] = fmin_n(mn[j], oa); mx[j] = fmax_n(mx[j], ob); }
-      }
-      float *red = Y;  // [16 warps][128] minima, then maxima
-      if (lane < 16) {
-        reinterpret_cast<float4 *>(red + warp * 128 + 8 * c8)[0] = make_float4(mn[0], mn[1], mn[2], mn[3]);
-        reinterpret_cast<float4 *>(red + warp * 128 + 8 * c8)[1] = make_float4(mn[4], mn[5], mn[6], mn[7]);
-        reinterpret_cast<float4 *>(red + 2048 + warp * 128 + 8 * c8)[0] = make_float4(mx[0], mx[1], mx[2], mx[3]);
-        reinterpret_cast<float4 *>(red + 2048 + warp * 128 + 8 * c8)[1] = make_float4(mx[4], mx[5], mx[6], mx[7]);
-      }
-      __syncthreads();
-      if (tid < 128) {
-        float a = red[tid], b = red[2048 + tid];
-        for (int k = 1; k < 16; k++) {
-          if (2 * k < (int)nvalid) {  // warp k holds rows 2k, 2k+1, 2k+32, ...
-            a = fmin_n(a, red[k * 128 + tid]);
-            b = fmax_n(b, red[2048 + k * 128 + tid]);
-          }
+      for (int s = 0; s < 2; s++) {
+        const int o = 16 >> s, half = 2 >> s;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; i++) {
+          const uint32_t sn = up ? mn[i] : mn[i + half], sx = up ? mx[i] : mx[i + half];
+          const uint32_t kn = up ? mn[i + half] : mn[i], kx = up ? mx[i + half] : mx[i];
+          mn[i] = pmin2_n<BF16>(kn, __shfl_xor_sync(kFull, sn, o));
+          mx[i] = pmax2_n<BF16>(kx, __shfl_xor_sync(kFull, sx, o));
         }
+      }
+#pragma unroll
+      for (int o = 4; o >= 1; o >>= 1) {
+        mn[0] = pmin2_n<BF16>(mn[0], __shfl_xor_sync(kFull, mn[0], o));
+        mx[0] = pmax2_n<BF16>(mx[0], __shfl_xor_sync(kFull, mx[0], o));
+      }
+      if ((lane & 3) == 0) {
+        const int hi = (lane >> 2) & 1;  // lane 8j: channel 2j, lane 8j + 4: channel 2j + 1
+        const int ch = 8 * warp + 2 * (lane >> 3) + hi;
+        const float2 fa = unpack_pair(mn[0], BF16), fb = unpack_pair(mx[0], BF16);
+        float a = hi ? fa.y : fa.x, b = hi ? fb.y : fb.x;
+        if (a != a) a = __int_as_float(0x7fffffff);  // one NaN for every input NaN
+        if (b != b) b = __int_as_float(0x7fffffff);
         if (!finite2(a, b)) flags |= KVC_FLAG_NONFINITE;
         float mu, inv;
         uint32_t mub;
         int e;
         smooth_params(a, b, mu, inv, mub, e, flags);
-        if (HAD && ((P.sign[tid >> 5] >> (tid & 31)) & 1u)) inv = -inv;  // sign folded into the exact scale
-        mu_s[tid] = mu;
-        inv_s[tid] = inv;
-        const size_t cell = ((size_t)lh * n_sb + sb) * kHeadDim + tid;
+        if (HAD && ((P.sign[ch >> 5] >> (ch & 31)) & 1u)) inv = -inv;  // sign folded into the exact scale
+        tab_mu[kTabStride * (ch >> 5) + (ch & 31)] = mu;
+        tab_inv[kTabStride * (ch >> 5) + (ch & 31)] = inv;
+        const size_t cell = ((size_t)lh * n_sb + sb) * kHeadDim + ch;
         reinterpret_cast<uint16_t *>(P.mu)[cell] = (uint16_t)mub;
         P.ex[cell] = (int8_t)e;
       }
       __syncthreads();
-      const float4 m0 = reinterpret_cast<const float4 *>(mu_s + 8 * c8)[0];
-      const float4 m1 = reinterpret_cast<const float4 *>(mu_s + 8 * c8)[1];
-      const float4 s0 = reinterpret_cast<const float4 *>(inv_s + 8 * c8)[0];
-      const float4 s1 = reinterpret_cast<const float4 *>(inv_s + 8 * c8)[1];
-      const float2 m[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
-                           make_float2(m1.z, m1.w)};
-      const float2 iv[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
-                            make_float2(s1.z, s1.w)};
-#pragma unroll
-      for (int i = 0; i < 4; i++)
-#pragma unroll
-        for (int j = 0; j < 4; j++) x[i][j] = mul2(sub2(x[i][j], m[j]), iv[j]);
-      if (nvalid < 128) {
-#pragma unroll
-        for (int i = 0; i < 4; i++)
-          if (rg + 32 * i >= (int)nvalid)
-#pragma unroll
-            for (int j = 0; j < 4; j++) x[i][j] = make_float2(0.0f, 0.0f);
-      }
     }
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-      float4 *row = reinterpret_cast<float4 *>(Y + (rg + 32 * i) * 128);
-      row[chA] = make_float4(x[i][0].x, x[i][0].y, x[i][1].x, x[i][1].y);
-      row[chB] = make_float4(x[i][2].x, x[i][2].y, x[i][3].x, x[i][3].y);
-    }
-    __syncthreads();
 
-    // ---- C
-    if (HAD) {
-      const int part = lane & 3, r = warp * 8 + (lane >> 2);
-      float4 *row = reinterpret_cast<float4 *>(Y + r * 128) + 8 * part;
-      const int rot = (part + 4 * (r & 1)) & 7;
+    // ---- C: row pass
+    {
       float2 w[16];
+      const bool live = cr < (int)nvalid;
 #pragma unroll
-      for (int q = 0; q < 8; q++) {
-        const float4 a = row[(q + rot) & 7];
-        w[2 * q] = make_float2(a.x, a.y);
-        w[2 * q + 1] = make_float2(a.z, a.w);
+      for (int i = 0; i < 4; i++) {
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (live) u = *reinterpret_cast<const uint4 *>(stage + cr * 256 + 16 * ((4 * cp + i) ^ c_xs));
+        w[4 * i] = unpack_pair(u.x, BF16);
+        w[4 * i + 1] = unpack_pair(u.y, BF16);
+        w[4 * i + 2] = unpack_pair(u.z, BF16);
+        w[4 * i + 3] = unpack_pair(u.w, BF16);
       }
-      if (!smooth) {
-        const uint32_t sbits = P.sign[part];
+      __syncthreads();  // every row has been read: the stage takes the next tile
+      if (tile + gridDim.x < n_tiles) ktile_issue(P, nxt.sb, nxt.h, nxt.l, stage, rg, kq, flags);
+      if (smooth) {
+        const float4 *tm = reinterpret_cast<const float4 *>(tab_mu + kTabStride * cp);
+        const float4 *ti = reinterpret_cast<const float4 *>(tab_inv + kTabStride * cp);
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+          const float4 m = tm[k], iv = ti[k];
+          w[2 * k] = mul2(sub2(w[2 * k], make_float2(m.x, m.y)), make_float2(iv.x, iv.y));
+          w[2 * k + 1] = mul2(sub2(w[2 * k + 1], make_float2(m.z, m.w)), make_float2(iv.z, iv.w));
+        }
+        if (nvalid < 128 && !live) {  // rows past the end stay 0 (only the last tile has any)
+#pragma unroll
+          for (int k = 0; k < 16; k++) w[k] = make_float2(0.0f, 0.0f);
+        }
+      } else if (HAD) {
+        const uint32_t sbits = P.sign[cp];
 #pragma unroll
         for (int i = 0; i < 16; i++) {
           w[i].x = __uint_as_float(__float_as_uint(w[i].x) ^ (((sbits >> (2 * i)) & 1u) << 31));
           w[i].y = __uint_as_float(__float_as_uint(w[i].y) ^ (((sbits >> (2 * i + 1)) & 1u) << 31));
         }
       }
-      fwht32_pairs(w);
+      if (HAD) {
+        fwht32_pairs(w);
+        const float2 s32 = bcast2((cp & 1) ? -1.0f : 1.0f), s64 = bcast2((cp & 2) ? -1.0f : 1.0f);
 #pragma unroll
-      for (int q = 0; q < 8; q++) row[(q + rot) & 7] = make_float4(w[2 * q].x, w[2 * q].y, w[2 * q + 1].x, w[2 * q + 1].y);
-      __syncthreads();
-    }
-
-    // ---- D1: 8 rows x 4 channels into registers, strides 32 / 64, per-channel partials
-    const int cq = lane, rs = warp;
-    const int nv = (int)nvalid - 8 * rs;
-    float2 v[4][4];
-    {
-      const float *Yr = Y + 8 * rs * 128;
+        for (int i = 0; i < 16; i++) {  // stride 32: the partner part is lane ^ 1
+          const float2 x = make_float2(__shfl_xor_sync(kFull, w[i].x, 1), __shfl_xor_sync(kFull, w[i].y, 1));
+          w[i] = __ffma2_rn(w[i], s32, x);  // lower channel: own + other; upper: other - own
+        }
 #pragma unroll
-      for (int i = 0; i < 4; i++)
+        for (int i = 0; i < 16; i++) {  // stride 64: the partner part is lane ^ 2
+          const float2 x = make_float2(__shfl_xor_sync(kFull, w[i].x, 2), __shfl_xor_sync(kFull, w[i].y, 2));
+          w[i] = __ffma2_rn(w[i], s64, x);
+        }
+        const float2 c2 = bcast2(hadamard_scale());
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-          v[k][i] = make_float2(Yr[2 * i * 128 + coff[2 * k]], Yr[(2 * i + 1) * 128 + coff[2 * k + 1]]);
-    }
-    if (HAD) {
-      const float2 c2 = bcast2(hadamard_scale());
-#pragma unroll
-      for (int i = 0; i < 4; i++) {
-        const float2 a0 = add2(v[0][i], v[1][i]), a1 = sub2(v[0][i], v[1][i]);
-        const float2 a2 = add2(v[2][i], v[3][i]), a3 = sub2(v[2][i], v[3][i]);
-        v[0][i] = mul2(add2(a0, a2), c2);
-        v[2][i] = mul2(sub2(a0, a2), c2);
-        v[1][i] = mul2(add2(a1, a3), c2);
-        v[3][i] = mul2(sub2(a1, a3), c2);
+        for (int i = 0; i < 16; i++) w[i] = mul2(w[i], c2);
       }
-    }
-    float pmn[4], pmx[4];
+      float4 *yrow = reinterpret_cast<float4 *>(Y + cr * 128) + 8 * cp;
 #pragma unroll
-    for (int k = 0; k < 4; k++) {
-      if (nv >= 8) {
-        pmn[k] = fmin3_n(fmin_n(v[k][0].x, v[k][0].y), v[k][1].x, v[k][1].y);
-        pmx[k] = fmax3_n(fmax_n(v[k][0].x, v[k][0].y), v[k][1].x, v[k][1].y);
-        pmn[k] = fmin3_n(fmin3_n(pmn[k], v[k][2].x, v[k][2].y), v[k][3].x, v[k][3].y);
-        pmx[k] = fmax3_n(fmax3_n(pmx[k], v[k][2].x, v[k][2].y), v[k][3].x, v[k][3].y);
+      for (int j = 0; j < 8; j++) yrow[j ^ c_xy] = make_float4(w[2 * j].x, w[2 * j].y, w[2 * j + 1].x, w[2 * j + 1].y);
+    }
+    __syncthreads();
+
+    // ---- D: column pass
+    {
+      const int nv = (int)nvalid - 32 * dq;
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; i++) v[i] = ((i & 1) ? Yd1 : Yd0)[i * 128];
+      float mn, mx;
+      if (nv >= 32) {
+        mn = fmin3_n(v[0], v[1], v[2]);
+        mx = fmax3_n(v[0], v[1], v[2]);
+#pragma unroll
+        for (int i = 3; i < 31; i += 2) {
+          mn = fmin3_n(mn, v[i], v[i + 1]);
+          mx = fmax3_n(mx, v[i], v[i + 1]);
+        }
+        mn = fmin_n(mn, v[31]);
+        mx = fmax_n(mx, v[31]);
       } else {
-        pmn[k] = pmx[k] = v[k][0].x;
+        mn = __int_as_float(0x7f800000);
+        mx = __int_as_float(0xff800000);
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-          if (2 * i < nv) { pmn[k] = fmin_n(pmn[k], v[k][i].x); pmx[k] = fmax_n(pmx[k], v[k][i].x); }
-          if (2 * i + 1 < nv) { pmn[k] = fmin_n(pmn[k], v[k][i].y); pmx[k] = fmax_n(pmx[k], v[k][i].y); }
+        for (int i = 0; i < 32; i++)
+          if (i < nv) {
+            mn = fmin_n(mn, v[i]);
+            mx = fmax_n(mx, v[i]);
+          }
+      }
+      for (int o = 1; o < (int)G / 32; o <<= 1) {  // the group's other quarters are lanes ^ 1 (and ^ 2)
+        mn = fmin_n(mn, __shfl_xor_sync(kFull, mn, o));
+        mx = fmax_n(mx, __shfl_xor_sync(kFull, mx, o));
+      }
+      const uint32_t tg = sb * tiles_groups + (32 * dq) / (int)G;
+      const bool active = tg < P.n_tg;  // a quarter past the end of an existing group still writes its (zero) codes
+      float sc = 0.0f, z = 0.0f, rr = 0.0f;
+      uint32_t meta = 0, fl = 0;
+      if (active) {
+        if (!finite2(mn, mx)) flags |= KVC_FLAG_NONFINITE;
+        meta = quant_params<BITS>(mn, mx, sc, z, rr, fl);
+        flags |= fl;
+      }
+      uint32_t cw[BITS];
+      float dm = 0.0f;
+      {
+        const float2 z2 = bcast2(z), r2 = bcast2(rr);
+        uint32_t u[32];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+          const float2 s2 = qfast2m(make_float2(v[2 * i], v[2 * i + 1]), z2, r2, dm);
+          u[2 * i] = __float_as_uint(s2.x);
+          u[2 * i + 1] = __float_as_uint(s2.y);
+        }
+        pack_sums32<BITS>(u, cw);
+      }
+      // a near-tie or a saturated group takes the exact path
+      const bool bad = active && (fl != 0 || !(dm < tie_threshold<BITS>()));
+      if (__any_sync(kFull, bad)) {
+        if (bad) {
+#pragma unroll
+          for (int i = 0; i < BITS; i++) cw[i] = 0u;
+#pragma unroll
+          for (int i = 0; i < 32; i++) put_code<BITS>(cw, i, qexact<BITS>(v[i], z, sc));
         }
       }
-    }
-    __syncthreads();  // every thread has read Y: its space holds the partials now
-    float *red = Y;   // [16 segments][128] minima at 0, maxima at 2048
+      if (nv < 32) {  // codes of rows past the end are 0
+        const int keep = (nv > 0 ? nv : 0) * BITS;
 #pragma unroll
-    for (int k = 0; k < 4; k++) {
-      red[rs * 128 + cq + 32 * k] = pmn[k];
-      red[2048 + rs * 128 + cq + 32 * k] = pmx[k];
-    }
-    __syncthreads();
-
-    // ---- D2: one thread per (group, channel) of the tile
-    {
-      const int nseg_valid = (int)((nvalid + 7) / 8);
-      const uint32_t tg_base = sb * tiles_groups;    // first token group of the tile
-      for (int j = tid; j < tiles_groups * 128; j += kKT) {
-        const int gi = j >> 7, ch = j & 127;
-        const int s0 = gi * spg;
-        const uint32_t tg = tg_base + gi;
-        if (s0 < nseg_valid && tg < P.n_tg) {
-          float a = red[s0 * 128 + ch], b = red[2048 + s0 * 128 + ch];
-          const int ns = min(spg, nseg_valid - s0);
-          for (int sg = 1; sg < ns; sg++) {
-            a = fmin_n(a, red[(s0 + sg) * 128 + ch]);
-            b = fmax_n(b, red[2048 + (s0 + sg) * 128 + ch]);
-          }
-          if (!finite2(a, b)) flags |= KVC_FLAG_NONFINITE;
-          float sc, z, rr;
-          uint32_t fl = 0;
-          const uint32_t meta = quant_params<BITS>(a, b, sc, z, rr, fl);
-          flags |= fl;
-          // a saturated group (fl != 0) is marked by r = NaN: its codes take the exact path
-          prm[gi * 128 + ch] = make_float4(z, fl ? __int_as_float(0x7fc00000) : rr, sc, __uint_as_float(meta));
-          const size_t g = ((size_t)lh * P.n_tg + tg) * kHeadDim + ch;
-          *reinterpret_cast<uint32_t *>(P.meta + g * 4) = meta;
+        for (int i = 0; i < BITS; i++) {
+          const int lo = 32 * i;
+          if (keep <= lo) cw[i] = 0u;
+          else if (keep < lo + 32) cw[i] &= (1u << (keep - lo)) - 1u;
         }
       }
-    }
-    __syncthreads();
-
-    // ---- D3: codes
-    {
-      const uint32_t tg = sb * tiles_groups + my_gi;
-      if (tg < P.n_tg) {  // a segment past the end of an existing group still writes its (zero) codes
-        const int gi = my_gi;
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          const int ch = cq + 32 * k;
-          const float4 pp = prm[gi * 128 + ch];
-          const float z = pp.x, rr = pp.y, sc = pp.z;
-          bool bad = false;
-          uint32_t cw[2] = {0u, 0u};
-          const float2 z2 = bcast2(z), r2 = bcast2(rr);
-#pragma unroll
-          for (int i = 0; i < 4; i++) {
-            const float2 u = qfast2<BITS>(v[k][i], z2, r2, bad);
-            put_code<BITS>(cw, 2 * i, __float_as_uint(u.x));
-            put_code<BITS>(cw, 2 * i + 1, __float_as_uint(u.y));
-          }
-          if (__any_sync(kFull, bad)) {
-            if (bad) {
-              cw[0] = cw[1] = 0u;
-#pragma unroll
-              for (int i = 0; i < 4; i++) {
-                put_code<BITS>(cw, 2 * i, qexact<BITS>(v[k][i].x, z, sc));
-                put_code<BITS>(cw, 2 * i + 1, qexact<BITS>(v[k][i].y, z, sc));
-              }
-            }
-          }
-          if (nv < 8) {  // codes of rows past the end are 0
-            const int keep = (nv > 0 ? nv : 0) * BITS;
-            if (keep < 32) { cw[0] &= (1u << keep) - 1u; cw[1] = 0u; }
-            else if (keep < 64) cw[1] &= (1u << (keep - 32)) - 1u;
-          }
-          const size_t g = ((size_t)lh * P.n_tg + tg) * kHeadDim + ch;
-          store_codes8<BITS>(P.codes + g * rec_bytes + my_seg_off, cw[0], cw[1]);
-        }
+      if (active) {
+        const size_t g = ((size_t)lh * P.n_tg + tg) * kHeadDim + dc;
+        if (d_first) *reinterpret_cast<uint32_t *>(P.meta + g * 4) = meta;
+        store_codes32<BITS>(P.codes + g * rec_bytes + seg_off, cw);
       }
     }
-    __syncthreads();
+    cur = nxt;
   }
   cp_async_wait_all_q();
   if (flags) atomicOr(P.status, flags);
@@ -1108,10 +1056,10 @@ static int dispatch(const QuantParams &p, bool had, bool enc, int sm, void *st, 
     if (p.axis == KVC_AXIS_OVER_TOKENS) {
       *name = "kvc_enc_ktile";
       if (p.g.bf16)
-        return had ? run(kvc_enc_ktile<BITS, true, true>, true, p, sm, st, units, kKtile3Smem, kKT)
-                   : run(kvc_enc_ktile<BITS, false, true>, true, p, sm, st, units, kKtile3Smem, kKT);
-      return had ? run(kvc_enc_ktile<BITS, true, false>, true, p, sm, st, units, kKtile3Smem, kKT)
-                 : run(kvc_enc_ktile<BITS, false, false>, true, p, sm, st, units, kKtile3Smem, kKT);
+        return had ? run(kvc_enc_ktile<BITS, true, true>, true, p, sm, st, units, kKtileSmem, kKT)
+                   : run(kvc_enc_ktile<BITS, false, true>, true, p, sm, st, units, kKtileSmem, kKT);
+      return had ? run(kvc_enc_ktile<BITS, true, false>, true, p, sm, st, units, kKtileSmem, kKT)
+                 : run(kvc_enc_ktile<BITS, false, false>, true, p, sm, st, units, kKtileSmem, kKT);
     }
     if (tile) {
       *name = "kvc_enc_tile";
