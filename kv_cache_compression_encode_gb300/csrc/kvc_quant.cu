@@ -508,12 +508,13 @@ __global__ void __launch_bounds__(kThreads) kvc_enc_tile(const QuantParams P) {
 // ---------------------------------------------------------------------------
 // key tile, groups over tokens (the key default): kvc_enc_ktile
 //
-// Per (layer, head, 128-token) tile, 512 threads, four barriers:
+// Per (layer, head, 128-token) tile, 512 threads, five barriers (three without smoothing):
 //  A  (smoothing only) warp w takes channel octet w over all 128 rows of the
 //     stage (lane l: rows l + 32i).  The per-channel minima and maxima run on
 //     the packed 16-bit pairs and are reduced across the warp by a halving
-//     butterfly; one lane per channel turns them into the smoothing parameters
-//     (sign folded into the power-of-two scale) in a shared table.
+//     butterfly; then four warps, one lane per channel, turn them into the
+//     smoothing parameters (sign folded into the power-of-two scale) in a
+//     shared table.
 //  C  thread (row r, part p) reads its 32 channels of row r from the stage and
 //     smooths them (or flips their signs); the stage is then free for the next
 //     tile's cp.async.  The Hadamard butterflies run with strides 1..16 in
@@ -545,8 +546,8 @@ __device__ __forceinline__ void cp_async_commit_q() { asm volatile("cp.async.com
 __device__ __forceinline__ void cp_async_wait_all_q() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Thread (rg = tid / 16, k = tid % 16) copies chunk k of rows rg + 32i (i < 4) of
-// `tile` into the stage; rows past the end of the tensor are left as they are
-// (no phase reads them), a bad page is zero-filled and flagged.
+// the tile (sb, h, l) into the stage; rows past the end of the tensor are left as
+// they are (no phase reads them), a bad page is zero-filled and flagged.
 __device__ __forceinline__ void ktile_issue(const QuantParams &P, uint32_t sb, uint32_t h, uint32_t l, uint8_t *stage,
                                             int rg, int k, uint32_t &flags) {
   const uint32_t t0 = sb * kSmoothBlock, nvalid = min((uint32_t)kSmoothBlock, P.g.T - t0);
@@ -555,9 +556,14 @@ __device__ __forceinline__ void ktile_issue(const QuantParams &P, uint32_t sb, u
   if (!P.g.block_table) {
     const uint64_t ts = P.g.token_stride;
     const uint8_t *src = lbase + (uint64_t)(t0 + rg) * ts;
+    if (nvalid == kSmoothBlock) {
 #pragma unroll
-    for (int i = 0; i < 4; i++)
-      if (rg + 32 * i < (int)nvalid) cp_async16_q(dst + i * 32 * 256, src + (uint64_t)i * 32 * ts);
+      for (int i = 0; i < 4; i++) cp_async16_q(dst + i * 32 * 256, src + (uint64_t)i * 32 * ts);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; i++)
+        if (rg + 32 * i < (int)nvalid) cp_async16_q(dst + i * 32 * 256, src + (uint64_t)i * 32 * ts);
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < 4; i++) {
@@ -735,11 +741,18 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P) {
         mn[0] = pmin2_n<BF16>(mn[0], __shfl_xor_sync(kFull, mn[0], o));
         mx[0] = pmax2_n<BF16>(mx[0], __shfl_xor_sync(kFull, mx[0], o));
       }
+      float *st = Y;  // the statistics of channel c at st[c] (minimum) and st[128 + c] (maximum)
       if ((lane & 3) == 0) {
         const int hi = (lane >> 2) & 1;  // lane 8j: channel 2j, lane 8j + 4: channel 2j + 1
         const int ch = 8 * warp + 2 * (lane >> 3) + hi;
         const float2 fa = unpack_pair(mn[0], BF16), fb = unpack_pair(mx[0], BF16);
-        float a = hi ? fa.y : fa.x, b = hi ? fb.y : fb.x;
+        st[ch] = hi ? fa.y : fa.x;
+        st[128 + ch] = hi ? fb.y : fb.x;
+      }
+      __syncthreads();
+      if (warp < 4) {  // one lane per channel turns the statistics into the smoothing parameters
+        const int ch = 32 * warp + lane;
+        float a = st[ch], b = st[128 + ch];
         if (a != a) a = __int_as_float(0x7fffffff);  // one NaN for every input NaN
         if (b != b) b = __int_as_float(0x7fffffff);
         if (!finite2(a, b)) flags |= KVC_FLAG_NONFINITE;
@@ -747,9 +760,9 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P) {
         uint32_t mub;
         int e;
         smooth_params(a, b, mu, inv, mub, e, flags);
-        if (HAD && ((P.sign[ch >> 5] >> (ch & 31)) & 1u)) inv = -inv;  // sign folded into the exact scale
-        tab_mu[kTabStride * (ch >> 5) + (ch & 31)] = mu;
-        tab_inv[kTabStride * (ch >> 5) + (ch & 31)] = inv;
+        if (HAD && ((P.sign[warp] >> lane) & 1u)) inv = -inv;  // sign folded into the exact scale
+        tab_mu[kTabStride * warp + lane] = mu;
+        tab_inv[kTabStride * warp + lane] = inv;
         const size_t cell = ((size_t)lh * n_sb + sb) * kHeadDim + ch;
         reinterpret_cast<uint16_t *>(P.mu)[cell] = (uint16_t)mub;
         P.ex[cell] = (int8_t)e;
