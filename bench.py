@@ -150,6 +150,7 @@ def kernel_bytes(plan, w, name: str, stream_bytes: int) -> int:
         "kvc_enc_ktile": raw_tensor + k_out,
         "kvc_enc_rows": raw_tensor + v_out,
         "kvc_dec_tile": raw_tensor + k_out,
+        "kvc_dec_ktile": raw_tensor + k_out,
         "kvc_dec_rows": raw_tensor + v_out,
         "kvc_lossless_enc": Q + stream_bytes,
         "kvc_lossless_dec": stream_bytes + Q,

@@ -914,6 +914,283 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P) {
 }
 
 // ---------------------------------------------------------------------------
+// key tile decode, groups over tokens (the key default): kvc_dec_ktile
+//
+// Per (layer, head, 128-token) tile, 128 threads (three CTAs per SM), two
+// barriers, no shuffles:
+//  D  thread c: the 128 codes of channel c (loaded a tile ahead) become floats
+//     through the exponent field (0x4B000000 | code is 2^23 + code, so one exact
+//     subtraction per pair leaves the code), are dequantized with one packed
+//     fma per pair and go down column c of the fp32 tile Y;
+//  C  thread r: all 128 channels of row r in registers: the inverse Hadamard
+//     transform (strides 1..64, then the scale), the signs and the smoothing
+//     undone by one packed fma per pair (sign folded into the power-of-two
+//     scale), rounding to the element type, the 256-byte row stored.
+// Each thread cp.asyncs its next tile's codes and metadata into its own slots of
+// shared buffers while C runs.
+// Y: float4 column k of row r sits at k ^ (r & 31), so a warp's column writes
+// (one row, 32 channels) and row reads (32 rows, one float4 column) are free of
+// bank conflicts.
+// ---------------------------------------------------------------------------
+constexpr int kKD = 128;
+
+// 32 codes (BITS each, LSB first) -> 16 float pairs, exactly.
+template <int BITS>
+__device__ __forceinline__ void codes_to_f2(const uint32_t (&w)[BITS], float2 (&q)[16]) {
+  constexpr uint32_t kE = 0x4B000000u;  // the bits of 2^23
+  uint32_t b[32];
+  if constexpr (BITS == 4) {
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      const uint32_t lo = w[k] & 0x0F0F0F0Fu, hi = (w[k] >> 4) & 0x0F0F0F0Fu;  // byte j: codes 8k+2j, 8k+2j+1
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        b[8 * k + 2 * j] = __byte_perm(lo, kE, 0x7440u | j);
+        b[8 * k + 2 * j + 1] = __byte_perm(hi, kE, 0x7440u | j);
+      }
+    }
+  } else if constexpr (BITS == 8) {
+#pragma unroll
+    for (int k = 0; k < 8; k++)
+#pragma unroll
+      for (int j = 0; j < 4; j++) b[4 * k + j] = __byte_perm(w[k], kE, 0x7440u | j);
+  } else if constexpr (BITS == 2) {
+#pragma unroll
+    for (int k = 0; k < 2; k++)
+#pragma unroll
+      for (int f = 0; f < 4; f++) {
+        const uint32_t m = (w[k] >> (2 * f)) & 0x03030303u;  // byte j: code 16k + 4j + f
+#pragma unroll
+        for (int j = 0; j < 4; j++) b[16 * k + 4 * j + f] = __byte_perm(m, kE, 0x7440u | j);
+      }
+  } else {
+    uint32_t c[32];
+    unpack32<BITS>(w, c);
+#pragma unroll
+    for (int i = 0; i < 32; i++) b[i] = c[i] | kE;
+  }
+  const float2 e2 = bcast2(8388608.0f);
+#pragma unroll
+  for (int i = 0; i < 16; i++) q[i] = sub2(make_float2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1])), e2);
+}
+
+// The D-phase inputs of a tile for channel c, copied by thread c into its own
+// slots of the shared buffers (so only thread c reads them, after its own
+// cp.async wait): its codes over the tile's 128 rows (16*BITS bytes: a segment of
+// each of the tile's 128 / G token-group records) at cbuf + 16*BITS*c, and the
+// group metadata words at mbuf[128 gi + c].  Groups past the end are zero.
+template <int BITS>
+__device__ __forceinline__ void kdec_issue(const QuantParams &P, uint32_t sb, uint32_t lh, int c, uint8_t *cbuf,
+                                           uint32_t *mbuf) {
+  const uint32_t G = P.group, ng = 128 / G, rec = G * BITS / 8;
+  const size_t g0 = ((size_t)lh * P.n_tg + sb * ng) * kHeadDim + c;  // record of the tile's first group
+  uint8_t *dst = cbuf + 16 * BITS * c;
+  for (uint32_t gi = 0; gi < ng; gi++) {
+    const size_t g = g0 + (size_t)gi * kHeadDim;
+    if (sb * ng + gi < P.n_tg) {
+      const uint32_t m = (uint32_t)__cvta_generic_to_shared(mbuf + 128 * gi + c);
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(m), "l"(P.meta + g * 4) : "memory");
+      const uint8_t *src = P.codes + g * rec;
+      if ((rec & 15) == 0) {
+        for (uint32_t o = 0; o < rec; o += 16) cp_async16_q(dst + gi * rec + o, src + o);
+      } else {
+        for (uint32_t o = 0; o < rec; o += 4) {
+          const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst + gi * rec + o);
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src + o) : "memory");
+        }
+      }
+    } else {
+      mbuf[128 * gi + c] = 0u;
+      for (uint32_t o = 0; o < rec; o += 4) *reinterpret_cast<uint32_t *>(dst + gi * rec + o) = 0u;
+    }
+  }
+  cp_async_commit_q();
+}
+
+template <int BITS>
+constexpr size_t kdec_smem(uint32_t G) {
+  return (size_t)128 * 128 * 4 + 64 * 16 + 16 * BITS * 128 + 4 * 128 * (128 / G);
+}
+
+// D phase of kvc_dec_ktile for one tile: column `tid` of Y from this thread's
+// code and metadata slots, the smoothing table entry of channel `tid`.
+template <int BITS, bool HAD>
+__device__ __forceinline__ void kdec_columns(const QuantParams &P, float *Y, float4 *tab, const uint8_t *cbuf,
+                                             const uint32_t *mbuf, bool smooth, uint32_t mub, int ex) {
+  const int tid = threadIdx.x, kc = tid >> 2;
+  const uint32_t G = P.group;
+  float *Yc = Y + (tid & 3);  // element (row i, channel tid) at Yc + 128 i + 4 (kc ^ (i & 31))
+  uint32_t cw[4 * BITS];
+  const uint32_t *cs = reinterpret_cast<const uint32_t *>(cbuf + 16 * BITS * tid);
+  if constexpr (BITS == 3) {
+#pragma unroll
+    for (int k = 0; k < 12; k++) cw[k] = cs[k];
+  } else {
+#pragma unroll
+    for (int k = 0; k < BITS; k++) {
+      const uint4 a = reinterpret_cast<const uint4 *>(cs)[k];
+      cw[4 * k] = a.x; cw[4 * k + 1] = a.y; cw[4 * k + 2] = a.z; cw[4 * k + 3] = a.w;
+    }
+  }
+  const uint32_t ng = 128 / G;
+  uint32_t meta[4];
+#pragma unroll
+  for (uint32_t gi = 0; gi < 4; gi++) meta[gi] = gi < ng ? mbuf[128 * gi + tid] : 0u;
+  float2 qf[16];
+#pragma unroll
+  for (int seg = 0; seg < 4; seg++) {  // rows 32 seg .. 32 seg + 31
+    uint32_t w[BITS];
+#pragma unroll
+    for (int k = 0; k < BITS; k++) w[k] = cw[seg * BITS + k];
+    codes_to_f2<BITS>(w, qf);
+    const uint32_t gi = (uint32_t)(32 * seg) / G;
+    const uint32_t m = gi == 0 ? meta[0] : gi == 1 ? meta[1] : gi == 2 ? meta[2] : meta[3];
+    const float2 s2 = bcast2(__half2float(__ushort_as_half((unsigned short)(m & 0xffffu))));
+    const float2 z2 = bcast2(__half2float(__ushort_as_half((unsigned short)(m >> 16))));
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      const float2 y = __ffma2_rn(qf[i], s2, z2);
+      const int r0 = 32 * seg + 2 * i;
+      Yc[r0 * 128 + 4 * (kc ^ (r0 & 31))] = y.x;
+      Yc[(r0 + 1) * 128 + 4 * (kc ^ ((r0 + 1) & 31))] = y.y;
+    }
+  }
+  if (smooth) {
+    float sc = pow2i(ex < -126 ? -126 : ex);
+    if (HAD && ((P.sign[tid >> 5] >> (tid & 31)) & 1u)) sc = -sc;  // sign folded into the exact scale
+    float *t = reinterpret_cast<float *>(tab + (tid >> 1)) + (tid & 1);
+    t[0] = __half2float(__ushort_as_half((unsigned short)mub));
+    t[2] = sc;
+  }
+}
+
+template <int BITS, bool HAD, bool BF16>
+__global__ void __launch_bounds__(kKD, 3) kvc_dec_ktile(const QuantParams P) {
+  if (P.check_corrupt && (*(volatile uint32_t *)P.status & KVC_FLAG_CORRUPT)) return;
+  extern __shared__ float4 smem_f4[];
+  float *Y = reinterpret_cast<float *>(smem_f4);   // [128][128] fp32, swizzled
+  float4 *tab = smem_f4 + 128 * 128 / 4;           // pair j: {mu_2j, mu_2j+1, sc_2j, sc_2j+1}
+  uint8_t *cbuf = reinterpret_cast<uint8_t *>(tab + 64);                 // [128 channels][16*BITS] codes
+  uint32_t *mbuf = reinterpret_cast<uint32_t *>(cbuf + 16 * BITS * 128);  // [groups][128] metadata
+  const int tid = threadIdx.x;
+  const uint32_t H = P.g.H, T = P.g.T, n_sb = P.n_sb;
+  const uint32_t n_tiles = P.g.L * H * n_sb;
+  const bool smooth = P.smooth != 0;
+  uint32_t flags = 0;
+  const uint32_t step_lh = gridDim.x / n_sb, step_sb = gridDim.x % n_sb;
+  const uint32_t step_h = step_lh % H, step_l = step_lh / H;
+
+  uint32_t tile = blockIdx.x;
+  if (tile >= n_tiles) return;
+  TilePos cur, nxt;
+  cur.init(tile, n_sb, H);
+  uint32_t mub = 0;
+  int ex = 0;
+  kdec_issue<BITS>(P, cur.sb, cur.l * H + cur.h, tid, cbuf, mbuf);
+  if (smooth) {
+    const size_t cell = ((size_t)(cur.l * H + cur.h) * n_sb + cur.sb) * kHeadDim + tid;
+    mub = reinterpret_cast<const uint16_t *>(P.mu)[cell];
+    ex = P.ex[cell];
+  }
+  for (; tile < n_tiles; tile += gridDim.x) {
+    const uint32_t sb = cur.sb, l = cur.l, h = cur.h;
+    const uint32_t t0 = sb * kSmoothBlock, nvalid = min((uint32_t)kSmoothBlock, T - t0);
+    nxt = cur;
+    nxt.advance(step_sb, step_h, step_l, n_sb, H);
+
+    // ---- D: column tid
+    cp_async_wait_all_q();
+    kdec_columns<BITS, HAD>(P, Y, tab, cbuf, mbuf, smooth, mub, ex);
+    if (tile + gridDim.x < n_tiles) {  // this thread's slots are read: the next tile's inputs go there
+      kdec_issue<BITS>(P, nxt.sb, nxt.l * H + nxt.h, tid, cbuf, mbuf);
+      if (smooth) {
+        const size_t cell = ((size_t)(nxt.l * H + nxt.h) * n_sb + nxt.sb) * kHeadDim + tid;
+        mub = reinterpret_cast<const uint16_t *>(P.mu)[cell];
+        ex = P.ex[cell];
+      }
+    }
+    __syncthreads();
+
+    // ---- C: row tid
+    const int r = tid;
+    if (r < (int)nvalid) {
+      float2 v[64];  // v[j] = channels 2j, 2j+1
+      const float4 *yrow = reinterpret_cast<const float4 *>(Y + r * 128);
+#pragma unroll
+      for (int k = 0; k < 32; k++) {
+        const float4 a = yrow[k ^ (r & 31)];
+        v[2 * k] = make_float2(a.x, a.y);
+        v[2 * k + 1] = make_float2(a.z, a.w);
+      }
+      if (HAD) {
+#pragma unroll
+        for (int j = 0; j < 64; j++) {  // stride 1, inside each pair
+          const float a = v[j].x, b = v[j].y;
+          v[j] = make_float2(__fadd_rn(a, b), __fsub_rn(a, b));
+        }
+#pragma unroll
+        for (int hs = 1; hs < 64; hs <<= 1)  // strides 2 .. 64: pairs j and j + hs
+#pragma unroll
+          for (int j = 0; j < 64; j++)
+            if ((j & hs) == 0) {
+              const float2 a = v[j], b = v[j + hs];
+              v[j] = add2(a, b);
+              v[j + hs] = sub2(a, b);
+            }
+        const float2 c2 = bcast2(hadamard_scale());
+#pragma unroll
+        for (int j = 0; j < 64; j++) v[j] = mul2(v[j], c2);
+      }
+      if (smooth) {
+#pragma unroll
+        for (int j = 0; j < 64; j++) {
+          const float4 t = tab[j];
+          v[j] = __ffma2_rn(v[j], make_float2(t.z, t.w), make_float2(t.x, t.y));
+        }
+      } else if (HAD) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          const uint32_t sbits = P.sign[q];
+#pragma unroll
+          for (int i = 0; i < 16; i++) {
+            float2 &x = v[16 * q + i];
+            x.x = __uint_as_float(__float_as_uint(x.x) ^ (((sbits >> (2 * i)) & 1u) << 31));
+            x.y = __uint_as_float(__float_as_uint(x.y) ^ (((sbits >> (2 * i + 1)) & 1u) << 31));
+          }
+        }
+      }
+      const uint64_t ro = row_offset(P.g, t0 + r);
+      if (ro == ~0ull) {
+        flags |= KVC_FLAG_BAD_PAGE;
+      } else {
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.layers[l]) + ro + (size_t)h * kHeadDim * 2);
+#pragma unroll
+        for (int k = 0; k < 16; k++) {
+          uint32_t u[4];
+#pragma unroll
+          for (int i = 0; i < 4; i++) {
+            const float2 x = v[4 * k + i];
+            if (BF16) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(x.x, x.y);
+              u[i] = *reinterpret_cast<const uint32_t *>(&b2);
+            } else {
+              const __half2 h2 = __floats2half2_rn(x.x, x.y);
+              u[i] = *reinterpret_cast<const uint32_t *>(&h2);
+            }
+          }
+          dst[k] = make_uint4(u[0], u[1], u[2], u[3]);
+        }
+      }
+    }
+
+    __syncthreads();
+    cur = nxt;
+  }
+  cp_async_wait_all_q();
+  if (flags) atomicOr(P.status, flags);
+}
+
+// ---------------------------------------------------------------------------
 // tile: decode
 // ---------------------------------------------------------------------------
 template <int BITS, bool HAD>
@@ -1085,6 +1362,14 @@ static int dispatch(const QuantParams &p, bool had, bool enc, int sm, void *st, 
                  : run(kvc_enc_rows<BITS, false, true>, false, p, sm, st, units);
     return had ? run(kvc_enc_rows<BITS, true, false>, false, p, sm, st, units)
                : run(kvc_enc_rows<BITS, false, false>, false, p, sm, st, units);
+  }
+  if (p.axis == KVC_AXIS_OVER_TOKENS) {
+    *name = "kvc_dec_ktile";
+    if (p.g.bf16)
+      return had ? run(kvc_dec_ktile<BITS, true, true>, true, p, sm, st, units, kdec_smem<BITS>(p.group), kKD)
+                 : run(kvc_dec_ktile<BITS, false, true>, true, p, sm, st, units, kdec_smem<BITS>(p.group), kKD);
+    return had ? run(kvc_dec_ktile<BITS, true, false>, true, p, sm, st, units, kdec_smem<BITS>(p.group), kKD)
+               : run(kvc_dec_ktile<BITS, false, false>, true, p, sm, st, units, kdec_smem<BITS>(p.group), kKD);
   }
   if (tile) {
     *name = "kvc_dec_tile";
