@@ -9,6 +9,8 @@
 // channels: records [layer][token][head][channel group]; smoothing cells
 // [layer][head][128-token block][channel].  A record holds G codes of b bits,
 // least significant bit first.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -36,6 +38,10 @@ struct kvc_plan_s {
   uint8_t header[KVC_HEADER_BYTES];
   int sm_count;
   uint64_t launches;
+  // host-side tensor maps for the key-tile encoder's TMA loads, per tensor, and the
+  // layer pointers they were encoded for
+  TmaMaps *tm[2];
+  const void *tm_ptr[2][kTmaMaxLayers];
   // timing
   bool timing;
   int timing_cap;
@@ -206,6 +212,8 @@ extern "C" void kvc_plan_destroy(kvc_plan_t *plan) {
   if (!plan) return;
   timing_clear(plan);
   for (cudaEvent_t e : plan->pool) cudaEventDestroy(e);
+  delete plan->tm[0];
+  delete plan->tm[1];
   delete plan;
 }
 
@@ -332,6 +340,53 @@ static void fill_geom(const kvc_plan_s *P, const kvc_kv *kv, KvGeom &g) {
   g.pad_ = 0;
 }
 
+// ---------------------------------------------------------------------------
+// tensor maps for the key-tile encoder (cuTensorMapEncodeTiled through the
+// runtime's driver entry point; no link-time dependency on the driver library)
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Maps of tensor `t`'s layers (see TmaMaps), re-encoded only for layers whose
+// pointer changed since the last call.  nullptr when TMA cannot be used: too many
+// layers, no encoder, or a layout the maps do not describe.
+static const TmaMaps *tensor_maps(kvc_plan_s *P, int t, void *const *layers) {
+  const kvc_shape &sh = P->shape;
+  if (sh.layers > (uint32_t)kTmaMaxLayers || sh.token_stride % 16 != 0) return nullptr;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (!enc) return nullptr;
+  if (!P->tm[t]) {
+    P->tm[t] = new (std::nothrow) TmaMaps();
+    if (!P->tm[t]) return nullptr;
+    for (int l = 0; l < kTmaMaxLayers; l++) P->tm_ptr[t][l] = nullptr;
+  }
+  for (uint32_t l = 0; l < sh.layers; l++) {
+    if (P->tm_ptr[t][l] == layers[l]) continue;
+    const cuuint64_t dim[2] = {(cuuint64_t)sh.kv_heads * sh.head_dim, (cuuint64_t)sh.tokens};
+    const cuuint64_t stride[1] = {(cuuint64_t)sh.token_stride};
+    const cuuint32_t box[2] = {64, 128}, estride[2] = {1, 1};
+    const CUresult r = enc(&P->tm[t]->map[l], sh.dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           2, const_cast<void *>(layers[l]), dim, stride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      P->tm_ptr[t][l] = nullptr;
+      return nullptr;
+    }
+    P->tm_ptr[t][l] = layers[l];
+  }
+  return P->tm[t];
+}
+
 // One quantize / dequantize launch per tensor.
 static kvc_status run_quant(kvc_plan_s *P, const kvc_kv *kv, uint8_t *Q, void *ws, bool enc, bool check_corrupt,
                             cudaStream_t st) {
@@ -356,9 +411,12 @@ static kvc_status run_quant(kvc_plan_s *P, const kvc_kv *kv, uint8_t *Q, void *w
     q.ex = reinterpret_cast<int8_t *>(Q + P->off[5]);
     q.status = ctrl_of(ws) + kCtrlFlags;
     q.check_corrupt = check_corrupt;
+    const TmaMaps *maps = nullptr;
+    if (enc && q.axis == KVC_AXIS_OVER_TOKENS && !kv->block_table) maps = tensor_maps(P, tensor, src);
+    q.tma = maps != nullptr;
     Bracket br(P, st);
     const char *name = "";
-    const int rc = enc ? launch_quantize(q, P->sm_count, st, &P->launches, &name)
+    const int rc = enc ? launch_quantize(q, maps, P->sm_count, st, &P->launches, &name)
                        : launch_dequantize(q, P->sm_count, st, &P->launches, &name);
     br.done(name);
     if (rc) return KVC_ERR_CUDA;

@@ -8,6 +8,7 @@
 // decode: chunk byte offsets), then (256-aligned) the quantized payload when
 // lossless stages are on.
 #pragma once
+#include <cuda.h>
 #include <stdint.h>
 
 #include "../../include/kvc.h"
@@ -47,6 +48,17 @@ struct QuantParams {
   uint32_t *status;              // workspace status word
   uint32_t check_corrupt;        // dequantize: skip when the status word carries CORRUPT
   uint32_t hadamard;             // randomized Hadamard on
+  uint32_t tma;                  // key-tile encoder: tiles arrive through the tensor maps (TmaMaps)
+};
+
+// Tensor maps of one tensor's layers for the key-tile encoder's TMA loads: rank 2
+// (H*128 channels innermost, T tokens; row stride = token stride), box 64
+// channels x 128 tokens, 128-byte swizzle, rows past T read as zero.  Passed as a
+// kernel parameter, so at most kTmaMaxLayers layers (beyond that the encoder
+// loads with cp.async).
+constexpr int kTmaMaxLayers = 128;
+struct TmaMaps {
+  CUtensorMap map[kTmaMaxLayers];
 };
 
 // Prologue: reset workspace words, write the stream header.
@@ -89,7 +101,8 @@ struct LosslessParams {
 };
 
 // Launchers (return cudaError_t as int).  `occ_grid` = resident-grid size to use.
-int launch_quantize(const QuantParams &p, int sm_count, void *stream, uint64_t *launches, const char **name);
+int launch_quantize(const QuantParams &p, const TmaMaps *maps, int sm_count, void *stream, uint64_t *launches,
+                    const char **name);
 int launch_dequantize(const QuantParams &p, int sm_count, void *stream, uint64_t *launches, const char **name);
 int launch_prologue(const PrologueParams &p, void *stream);
 int launch_lossless_encode(const LosslessParams &p, int sm_count, void *stream);

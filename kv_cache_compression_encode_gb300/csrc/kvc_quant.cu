@@ -524,16 +524,22 @@ __global__ void __launch_bounds__(kThreads) kvc_enc_tile(const QuantParams P) {
 //     group minimum and maximum in registers plus one or two shuffles (groups
 //     of 64 or 128 tokens), the group parameters, its 32 codes (packed by
 //     integer multiply-adds), one store into the channel's record.
-// Stage: 16-byte chunk k of row r sits at chunk k ^ (r & 7) ^ ((k >> 2) & 2).
+// Stage: the tile as two boxes of 64 channels x 128 rows (16 KiB each, rows of
+// 128 bytes), each with the TMA 128-byte swizzle: 16-byte chunk k (0..15) of row
+// r sits at byte (k >> 3) * 16384 + 128 r + 16 ((k & 7) ^ (r & 7)).
 // Y: float4 column k of row r sits at k ^ (r & 1) ^ (((k >> 3) & 3) << 1) ^
-// (((r >> 5) & 3) << 1).  With these, the cp.async writes, the A and C reads of
-// the stage, the C writes and the D reads of Y are all free of bank conflicts.
+// (((r >> 5) & 3) << 1).  With these, the loads into the stage, the A and C reads
+// of the stage (C: two-way at most), the C writes and the D reads of Y are free of
+// bank conflicts.
 // ---------------------------------------------------------------------------
 constexpr int kKT = 512;
 constexpr int kTabStride = 36;  // floats per 32-channel part in the parameter tables (spreads the parts over banks)
-constexpr size_t kKtileSmem = (size_t)128 * 128 * 4 + 128 * 256 + 2 * 4 * kTabStride * 4;
+// 1 KiB slack for aligning the stage to the swizzle's 1 KiB period
+constexpr size_t kKtileSmem = 1024 + 128 * 256 + (size_t)128 * 128 * 4 + 2 * 4 * kTabStride * 4;
 
-__device__ __forceinline__ uint32_t stage_chunk(uint32_t k, uint32_t r) { return k ^ (r & 7u) ^ ((k >> 2) & 2u); }
+__device__ __forceinline__ uint32_t stage_off(uint32_t k, uint32_t r) {
+  return (k >> 3) * 16384u + 128u * r + 16u * ((k & 7u) ^ (r & 7u));
+}
 __device__ __forceinline__ uint32_t ycol4(uint32_t k, uint32_t r) {
   return k ^ (r & 1u) ^ (((k >> 3) & 3u) << 1) ^ (((r >> 5) & 3u) << 1);
 }
@@ -545,6 +551,34 @@ __device__ __forceinline__ void cp_async16_q(void *smem, const void *gmem) {
 __device__ __forceinline__ void cp_async_commit_q() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all_q() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+// The tile's two boxes by TMA (one thread): the mbarrier expects their 32 KiB.
+__device__ __forceinline__ void ktile_tma(const CUtensorMap *map, uint32_t h, uint32_t t0, uint8_t *stage,
+                                          uint64_t *bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+               "r"(32768u)
+               : "memory");
+#pragma unroll
+  for (int b = 0; b < 2; b++)
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(stage + b * 16384)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"((int)(h * kHeadDim + 64 * b)), "r"((int)t0), "r"(smem_u32(bar))
+        : "memory");
+}
+// Bounded wait for phase `par` of the stage barrier; false when it ran out.
+__device__ __forceinline__ bool ktile_wait(uint64_t *bar, uint32_t par) {
+  for (uint32_t i = 0; i < (1u << 22); i++) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done)
+                 : "r"(smem_u32(bar)), "r"(par)
+                 : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
 // Thread (rg = tid / 16, k = tid % 16) copies chunk k of rows rg + 32i (i < 4) of
 // the tile (sb, h, l) into the stage; rows past the end of the tensor are left as
 // they are (no phase reads them), a bad page is zero-filled and flagged.
@@ -552,17 +586,17 @@ __device__ __forceinline__ void ktile_issue(const QuantParams &P, uint32_t sb, u
                                             int rg, int k, uint32_t &flags) {
   const uint32_t t0 = sb * kSmoothBlock, nvalid = min((uint32_t)kSmoothBlock, P.g.T - t0);
   const uint8_t *lbase = static_cast<const uint8_t *>(P.layers[l]) + (size_t)(h * kHeadDim + 8 * k) * 2;
-  uint8_t *dst = stage + rg * 256 + 16 * stage_chunk(k, rg);  // r & 7 is the same for rows rg + 32i
+  uint8_t *dst = stage + stage_off(k, rg);  // rows rg + 32i: + 4096 i
   if (!P.g.block_table) {
     const uint64_t ts = P.g.token_stride;
     const uint8_t *src = lbase + (uint64_t)(t0 + rg) * ts;
     if (nvalid == kSmoothBlock) {
 #pragma unroll
-      for (int i = 0; i < 4; i++) cp_async16_q(dst + i * 32 * 256, src + (uint64_t)i * 32 * ts);
+      for (int i = 0; i < 4; i++) cp_async16_q(dst + i * 4096, src + (uint64_t)i * 32 * ts);
     } else {
 #pragma unroll
       for (int i = 0; i < 4; i++)
-        if (rg + 32 * i < (int)nvalid) cp_async16_q(dst + i * 32 * 256, src + (uint64_t)i * 32 * ts);
+        if (rg + 32 * i < (int)nvalid) cp_async16_q(dst + i * 4096, src + (uint64_t)i * 32 * ts);
     }
   } else {
 #pragma unroll
@@ -572,9 +606,9 @@ __device__ __forceinline__ void ktile_issue(const QuantParams &P, uint32_t sb, u
         const uint64_t ro = row_offset(P.g, t0 + r);
         if (ro == ~0ull) {
           flags |= KVC_FLAG_BAD_PAGE;
-          *reinterpret_cast<uint4 *>(dst + i * 32 * 256) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4 *>(dst + i * 4096) = make_uint4(0u, 0u, 0u, 0u);
         } else {
-          cp_async16_q(dst + i * 32 * 256, lbase + ro);
+          cp_async16_q(dst + i * 4096, lbase + ro);
         }
       }
     }
@@ -667,11 +701,13 @@ struct TilePos {
 };
 
 template <int BITS, bool HAD, bool BF16>
-__global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P) {
+__global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P, const __grid_constant__ TmaMaps M) {
   extern __shared__ float4 smem_f4[];
-  float *Y = reinterpret_cast<float *>(smem_f4);                     // [128][128] fp32, swizzled
-  uint8_t *stage = reinterpret_cast<uint8_t *>(Y + 128 * 128);        // [128][256 B] raw rows, swizzled
-  float *tab_mu = reinterpret_cast<float *>(stage + 128 * 256);       // [4 parts][kTabStride]
+  __shared__ __align__(8) uint64_t stage_bar;
+  uint8_t *stage = reinterpret_cast<uint8_t *>(smem_f4);
+  stage += (1024u - (smem_u32(stage) & 1023u)) & 1023u;                // [2 boxes][128 rows][128 B], TMA swizzle
+  float *Y = reinterpret_cast<float *>(stage + 128 * 256);             // [128][128] fp32, swizzled
+  float *tab_mu = Y + 128 * 128;                                       // [4 parts][kTabStride]
   float *tab_inv = tab_mu + 4 * kTabStride;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t H = P.g.H, T = P.g.T, n_sb = P.n_sb, G = P.group;
@@ -681,9 +717,9 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P) {
 
   // tile-invariant thread roles and offsets
   const int rg = tid >> 4, kq = tid & 15;                  // cp.async: rows rg + 32i, chunk kq
-  const uint32_t a_chunk = stage_chunk(warp, lane);          // A: chunk `warp` of rows lane + 32i
+  const uint32_t a_off = stage_off(warp, lane);             // A: chunk `warp` of rows lane + 32i: + 4096 i
   const int cr = tid >> 2, cp = tid & 3;                   // C: row cr, channels 32cp .. 32cp + 31
-  const uint32_t c_xs = (cr & 7) ^ (cp & 2);               // C: stage chunk 4cp + i sits at (4cp + i) ^ c_xs
+  const uint32_t c_off = stage_off(4 * cp, cr);             // C: chunk 4cp + i of row cr at c_off ^ 16 i
   const uint32_t c_xy = ycol4(8 * cp, cr) & 7u;            // C: Y float4 column 8cp + j sits at 8cp + (j ^ c_xy)
   const int dc = 8 * warp + (lane >> 2), dq = lane & 3;    // D: channel dc, rows 32dq .. 32dq + 31
   const float *Yd0 = Y + 32 * dq * 128 + 4 * (int)ycol4(dc >> 2, 32 * dq) + (dc & 3);      // even rows
@@ -695,16 +731,27 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P) {
   const uint32_t step_lh = gridDim.x / n_sb, step_sb = gridDim.x % n_sb;
   const uint32_t step_h = step_lh % H, step_l = step_lh / H;
 
+  const bool tma = P.tma != 0;
+  if (tma && tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&stage_bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
   uint32_t tile = blockIdx.x;
   TilePos cur, nxt;
   cur.init(tile < n_tiles ? tile : 0u, n_sb, H);
-  if (tile < n_tiles) ktile_issue(P, cur.sb, cur.h, cur.l, stage, rg, kq, flags);
-  for (; tile < n_tiles; tile += gridDim.x) {
+  if (tile < n_tiles) {
+    if (!tma) ktile_issue(P, cur.sb, cur.h, cur.l, stage, rg, kq, flags);
+    else if (tid == 0) ktile_tma(&M.map[cur.l], cur.h, cur.sb * kSmoothBlock, stage, &stage_bar);
+  }
+  for (uint32_t it = 0; tile < n_tiles; tile += gridDim.x, it++) {
     const uint32_t sb = cur.sb, lh = cur.l * H + cur.h;
     const uint32_t nvalid = min((uint32_t)kSmoothBlock, T - sb * kSmoothBlock);
     nxt = cur;
     nxt.advance(step_sb, step_h, step_l, n_sb, H);
-    cp_async_wait_all_q();
+    if (!tma) cp_async_wait_all_q();
+    else if (!ktile_wait(&stage_bar, it & 1u)) flags |= KVC_FLAG_TIMEOUT;
     __syncthreads();  // the stage holds this tile; every thread is done with the previous Y
 
     // ---- A: smoothing parameters.  Minima and maxima run on the packed 16-bit
@@ -716,7 +763,7 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P) {
       for (int i = 0; i < 4; i++) {
         const int r = lane + 32 * i;
         if (r < (int)nvalid) {
-          const uint4 u = *reinterpret_cast<const uint4 *>(stage + r * 256 + 16 * a_chunk);
+          const uint4 u = *reinterpret_cast<const uint4 *>(stage + a_off + 4096 * i);
           mn[0] = pmin2_n<BF16>(mn[0], u.x); mx[0] = pmax2_n<BF16>(mx[0], u.x);
           mn[1] = pmin2_n<BF16>(mn[1], u.y); mx[1] = pmax2_n<BF16>(mx[1], u.y);
           mn[2] = pmin2_n<BF16>(mn[2], u.z); mx[2] = pmax2_n<BF16>(mx[2], u.z);
@@ -777,14 +824,21 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P) {
 #pragma unroll
       for (int i = 0; i < 4; i++) {
         uint4 u = make_uint4(0u, 0u, 0u, 0u);
-        if (live) u = *reinterpret_cast<const uint4 *>(stage + cr * 256 + 16 * ((4 * cp + i) ^ c_xs));
+        if (live) u = *reinterpret_cast<const uint4 *>(stage + (c_off ^ (16u * i)));
         w[4 * i] = unpack_pair(u.x, BF16);
         w[4 * i + 1] = unpack_pair(u.y, BF16);
         w[4 * i + 2] = unpack_pair(u.z, BF16);
         w[4 * i + 3] = unpack_pair(u.w, BF16);
       }
       __syncthreads();  // every row has been read: the stage takes the next tile
-      if (tile + gridDim.x < n_tiles) ktile_issue(P, nxt.sb, nxt.h, nxt.l, stage, rg, kq, flags);
+      if (tile + gridDim.x < n_tiles) {
+        if (!tma) {
+          ktile_issue(P, nxt.sb, nxt.h, nxt.l, stage, rg, kq, flags);
+        } else if (tid == 0) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the reads above before the async writes
+          ktile_tma(&M.map[nxt.l], nxt.h, nxt.sb * kSmoothBlock, stage, &stage_bar);
+        }
+      }
       if (smooth) {
         const float4 *tm = reinterpret_cast<const float4 *>(tab_mu + kTabStride * cp);
         const float4 *ti = reinterpret_cast<const float4 *>(tab_inv + kTabStride * cp);
@@ -1337,8 +1391,23 @@ static int run(K kernel, bool tile, const QuantParams &p, int sm_count, void *st
 
 static bool use_tile(const QuantParams &p) { return p.smooth || p.axis == KVC_AXIS_OVER_TOKENS; }
 
+// The key-tile encoder takes the tensor maps as a second (grid-constant) parameter.
+static const TmaMaps kNoMaps = {};
+template <typename K>
+static int run_ktile(K kernel, const QuantParams &p, const TmaMaps *maps, int sm_count, void *stream,
+                     uint64_t work_units) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kKtileSmem);
+  if (e != cudaSuccess) return (int)e;
+  uint64_t blocks = (uint64_t)sm_count * resident_blocks(kernel, kKtileSmem, kKT);
+  if (work_units < blocks) blocks = work_units;
+  if (blocks == 0) return 0;
+  kernel<<<(unsigned)blocks, kKT, kKtileSmem, (cudaStream_t)stream>>>(p, maps ? *maps : kNoMaps);
+  return (int)cudaGetLastError();
+}
+
 template <int BITS>
-static int dispatch(const QuantParams &p, bool had, bool enc, int sm, void *st, const char **name) {
+static int dispatch(const QuantParams &p, const TmaMaps *maps, bool had, bool enc, int sm, void *st,
+                    const char **name) {
   const bool tile = use_tile(p);
   const uint64_t rows = (uint64_t)p.g.L * p.g.T * p.g.H;
   const uint64_t units = tile ? (uint64_t)p.g.L * p.g.H * p.n_sb : (enc ? (rows + 127) / 128 : (rows + 63) / 64);
@@ -1346,10 +1415,10 @@ static int dispatch(const QuantParams &p, bool had, bool enc, int sm, void *st, 
     if (p.axis == KVC_AXIS_OVER_TOKENS) {
       *name = "kvc_enc_ktile";
       if (p.g.bf16)
-        return had ? run(kvc_enc_ktile<BITS, true, true>, true, p, sm, st, units, kKtileSmem, kKT)
-                   : run(kvc_enc_ktile<BITS, false, true>, true, p, sm, st, units, kKtileSmem, kKT);
-      return had ? run(kvc_enc_ktile<BITS, true, false>, true, p, sm, st, units, kKtileSmem, kKT)
-                 : run(kvc_enc_ktile<BITS, false, false>, true, p, sm, st, units, kKtileSmem, kKT);
+        return had ? run_ktile(kvc_enc_ktile<BITS, true, true>, p, maps, sm, st, units)
+                   : run_ktile(kvc_enc_ktile<BITS, false, true>, p, maps, sm, st, units);
+      return had ? run_ktile(kvc_enc_ktile<BITS, true, false>, p, maps, sm, st, units)
+                 : run_ktile(kvc_enc_ktile<BITS, false, false>, p, maps, sm, st, units);
     }
     if (tile) {
       *name = "kvc_enc_tile";
@@ -1381,25 +1450,27 @@ static int dispatch(const QuantParams &p, bool had, bool enc, int sm, void *st, 
              : run(kvc_dec_rows<BITS, false>, false, p, sm, st, units);
 }
 
-static int dispatch_bits(const QuantParams &p, bool enc, int sm, void *st, uint64_t *launches, const char **name) {
+static int dispatch_bits(const QuantParams &p, const TmaMaps *maps, bool enc, int sm, void *st, uint64_t *launches,
+                         const char **name) {
   const bool had = p.hadamard != 0;
   int rc;
   switch (p.bits) {
-    case 2: rc = dispatch<2>(p, had, enc, sm, st, name); break;
-    case 3: rc = dispatch<3>(p, had, enc, sm, st, name); break;
-    case 4: rc = dispatch<4>(p, had, enc, sm, st, name); break;
-    default: rc = dispatch<8>(p, had, enc, sm, st, name); break;
+    case 2: rc = dispatch<2>(p, maps, had, enc, sm, st, name); break;
+    case 3: rc = dispatch<3>(p, maps, had, enc, sm, st, name); break;
+    case 4: rc = dispatch<4>(p, maps, had, enc, sm, st, name); break;
+    default: rc = dispatch<8>(p, maps, had, enc, sm, st, name); break;
   }
   if (launches) ++*launches;
   return rc;
 }
 
-int launch_quantize(const QuantParams &p, int sm_count, void *stream, uint64_t *launches, const char **name) {
-  return dispatch_bits(p, true, sm_count, stream, launches, name);
+int launch_quantize(const QuantParams &p, const TmaMaps *maps, int sm_count, void *stream, uint64_t *launches,
+                    const char **name) {
+  return dispatch_bits(p, maps, true, sm_count, stream, launches, name);
 }
 
 int launch_dequantize(const QuantParams &p, int sm_count, void *stream, uint64_t *launches, const char **name) {
-  return dispatch_bits(p, false, sm_count, stream, launches, name);
+  return dispatch_bits(p, nullptr, false, sm_count, stream, launches, name);
 }
 
 }  // namespace kvc
