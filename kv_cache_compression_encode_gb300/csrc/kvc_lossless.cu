@@ -937,6 +937,137 @@ __global__ void __launch_bounds__(FW, kFastCtasPerSm) kvc_lossless_enc_fast(cons
 }
 
 // ---------------------------------------------------------------------------
+// Fast decode of one compressed chunk for the stage lists TUPL_8 [BIT_8]
+// [DELTA_1] RZE_w, n a multiple of 4 KiB: the inverse of the fast encoder's
+// register passes.  `in` (shared) holds the chunk's `size` stored bytes; thread
+// t < n/64 owns stream bytes 64t..64t+63:
+//  * RZE: its level-2 bits, one block scan for its place in the list of nonzero
+//    level-1 bytes, its level-1 bytes, a second scan for its place in the list of
+//    nonzero words, its words;
+//  * DELTA_1: byte-wise inclusive prefix sums inside its words (SWAR adds that
+//    keep carries inside each byte), a block scan of the per-thread sums;
+//  * the bytes go to `buf` (shared) swizzled like the encoder's transform output;
+//    thread beta then gathers the 64 bit-plane bytes of block beta, undoes the
+//    8x8 bit transposes and the 4x4 byte transposes (both are involutions) and
+//    stores the 64-byte block to `dst`.
+// The consistency checks are the generic decoder's: the level-1 list must fit in
+// the stored bytes and the sizes must add up exactly; otherwise false (uniform).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t badd4(uint32_t a, uint32_t b) {  // byte-wise a + b mod 256
+  return ((a & 0x7f7f7f7fu) + (b & 0x7f7f7f7fu)) ^ ((a ^ b) & 0x80808080u);
+}
+
+template <int W, bool DELTA, bool BIT8>
+__device__ bool fast_decode_chunk(const uint8_t *in, uint32_t size, uint32_t n, uint8_t *buf, uint8_t *dst,
+                                  uint32_t *tmp) {
+  const uint32_t nthr = n / 64, nb = n / (8 * W), nb2 = nb / 8;
+  const uint32_t t = threadIdx.x;
+  const bool active = t < nthr;
+  if (size < nb2) return false;
+  uint32_t l2 = 0;  // this thread's level-2 bits (W = 2: a nibble, W = 1: a byte)
+  if (active) l2 = W == 2 ? (in[t >> 1] >> (4 * (t & 1))) & 0xfu : in[t];
+  uint32_t totB;
+  uint32_t r = block_excl_scan<uint32_t, LT>(__popc(l2), tmp, totB);
+  if (nb2 + totB > size) return false;
+  uint32_t blo = 0, bhi = 0;  // element bits: W = 2 -> 32 in blo; W = 1 -> 64 in (bhi:blo)
+  if (active) {
+    const uint8_t *L1 = in + nb2;
+#pragma unroll
+    for (int k = 0; k < 8 / W; k++)
+      if ((l2 >> k) & 1u) {
+        const uint32_t b = L1[r++];
+        if (k < 4) blo |= b << (8 * k);
+        else bhi |= b << (8 * (k - 4));
+      }
+  }
+  uint32_t totW;
+  uint32_t e = block_excl_scan<uint32_t, LT>(__popc(blo) + __popc(bhi), tmp, totW);
+  if (nb2 + totB + W * totW != size) return false;
+  uint32_t x[16];
+#pragma unroll
+  for (int i = 0; i < 16; i++) x[i] = 0u;
+  if (active) {
+    const uint8_t *E = in + nb2 + totB;
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      if (W == 2) {
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++)
+          if ((blo >> (2 * i + hh)) & 1u) {
+            x[i] |= ((uint32_t)E[2 * e] | ((uint32_t)E[2 * e + 1] << 8)) << (16 * hh);
+            e++;
+          }
+      } else {
+        const uint32_t bits = i < 8 ? (blo >> (4 * i)) : (bhi >> (4 * (i - 8)));
+#pragma unroll
+        for (int b = 0; b < 4; b++)
+          if ((bits >> b) & 1u) x[i] |= (uint32_t)E[e++] << (8 * b);
+      }
+    }
+  }
+  if (DELTA) {
+    uint32_t run = 0;
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      uint32_t p = badd4(x[i], x[i] << 8);
+      p = badd4(p, p << 16);
+      p = badd4(p, run * 0x01010101u);
+      x[i] = p;
+      run = p >> 24;
+    }
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan<uint32_t, LT>(active ? run : 0u, tmp, tot) & 0xffu;
+#pragma unroll
+    for (int i = 0; i < 16; i++) x[i] = badd4(x[i], ex * 0x01010101u);
+  }
+  if (active) {
+    uint4 *d = reinterpret_cast<uint4 *>(buf) + 4 * t;
+    const uint32_t rot = (t >> 1) & 3u;
+#pragma unroll
+    for (int k = 0; k < 4; k++) d[(k + rot) & 3u] = make_uint4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+  }
+  bsync<LT>();
+  if (active) {
+    const uint32_t beta = t, m = n / 8, m8 = n / 64;
+    uint32_t L0[4], L1[4], H0[4], H1[4];
+    const uint32_t off8 = 64 * (beta >> 3) + 16 * (((beta >> 1) + (beta >> 4)) & 3u) + 8 * (beta & 1u);
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      uint32_t lo, hi;
+      if (BIT8) {
+        const uint8_t *ob = buf + swzb(j * m8 + beta);
+        lo = (uint32_t)ob[0] | ((uint32_t)ob[m] << 8) | ((uint32_t)ob[2 * m] << 16) | ((uint32_t)ob[3 * m] << 24);
+        hi = (uint32_t)ob[4 * m] | ((uint32_t)ob[5 * m] << 8) | ((uint32_t)ob[6 * m] << 16) | ((uint32_t)ob[7 * m] << 24);
+        bits8x8(lo, hi);
+      } else {
+        const uint2 v = *reinterpret_cast<const uint2 *>(buf + j * m + off8);
+        lo = v.x;
+        hi = v.y;
+      }
+      if (j < 4) {
+        L0[j] = lo;
+        L1[j] = hi;
+      } else {
+        H0[j - 4] = lo;
+        H1[j - 4] = hi;
+      }
+    }
+    uint32_t a[4], b[4], c[4], d[4];
+    byte_t4x4(L0[0], L0[1], L0[2], L0[3], a);  // a[i]: bytes 0..3 of tuple i
+    byte_t4x4(H0[0], H0[1], H0[2], H0[3], b);  // b[i]: bytes 4..7 of tuple i
+    byte_t4x4(L1[0], L1[1], L1[2], L1[3], c);  // tuples 4..7
+    byte_t4x4(H1[0], H1[1], H1[2], H1[3], d);
+    uint4 *o = reinterpret_cast<uint4 *>(dst + 64 * beta);
+    o[0] = make_uint4(a[0], b[0], a[1], b[1]);
+    o[1] = make_uint4(a[2], b[2], a[3], b[3]);
+    o[2] = make_uint4(c[0], d[0], c[1], d[1]);
+    o[3] = make_uint4(c[2], d[2], c[3], d[3]);
+  }
+  bsync<LT>();
+  return true;
+}
+
+// ---------------------------------------------------------------------------
 // Decode, step 1 (one CTA): check the header and the chunk table, compute the
 // chunk offsets.  Any inconsistency sets KVC_FLAG_CORRUPT.
 // ---------------------------------------------------------------------------
@@ -1015,7 +1146,7 @@ __global__ void __launch_bounds__(PT) kvc_decode_prepare(const LosslessParams P)
 // ---------------------------------------------------------------------------
 // Decode, step 2: one chunk per CTA iteration back into the payload.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(LT) kvc_lossless_dec(const LosslessParams P) {
+__global__ void __launch_bounds__(LT, 3) kvc_lossless_dec(const LosslessParams P, const FastSpec F) {
   if (*(volatile uint32_t *)(P.ctrl + kCtrlFlags) & KVC_FLAG_CORRUPT) return;
   extern __shared__ uint4 smem_u4[];
   uint8_t *bufA = reinterpret_cast<uint8_t *>(smem_u4);
@@ -1042,6 +1173,26 @@ __global__ void __launch_bounds__(LT) kvc_lossless_dec(const LosslessParams P) {
     }
     for (uint32_t i = threadIdx.x; i < align16u(size) / 16; i += LT) reinterpret_cast<uint4 *>(bufA)[i] = __ldg(src + i);
     __syncthreads();
+    if (F.rze_w != 0 && fast_len(n)) {
+      uint8_t *d8 = P.out_payload + off;
+      bool ok;
+      if (F.rze_w == 2) {
+        if (F.delta1) ok = F.bit8 ? fast_decode_chunk<2, true, true>(bufA, size, n, bufB, d8, tmp)
+                                  : fast_decode_chunk<2, true, false>(bufA, size, n, bufB, d8, tmp);
+        else ok = F.bit8 ? fast_decode_chunk<2, false, true>(bufA, size, n, bufB, d8, tmp)
+                         : fast_decode_chunk<2, false, false>(bufA, size, n, bufB, d8, tmp);
+      } else {
+        if (F.delta1) ok = F.bit8 ? fast_decode_chunk<1, true, true>(bufA, size, n, bufB, d8, tmp)
+                                  : fast_decode_chunk<1, true, false>(bufA, size, n, bufB, d8, tmp);
+        else ok = F.bit8 ? fast_decode_chunk<1, false, true>(bufA, size, n, bufB, d8, tmp)
+                         : fast_decode_chunk<1, false, false>(bufA, size, n, bufB, d8, tmp);
+      }
+      if (!ok) {
+        if (threadIdx.x == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CORRUPT);
+        __syncthreads();
+      }
+      continue;
+    }
     const bool ok = rze_decode(bufA, size, bufB, n, P.param[last], Bs, tmp);
     if (!ok) {
       if (threadIdx.x == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CORRUPT);
@@ -1129,7 +1280,9 @@ int launch_lossless_decode(const LosslessParams &p, int sm_count, void *stream) 
     per_sm = 1;
   uint64_t blocks = (uint64_t)sm_count * per_sm;
   if (blocks > p.n_chunks) blocks = p.n_chunks;
-  kvc_lossless_dec<<<(unsigned)blocks, LT, smem, (cudaStream_t)stream>>>(p);
+  FastSpec f;
+  if (!fast_spec(p, f)) f = FastSpec{0, 0, 0, 0};  // rze_w == 0: generic stages for every chunk
+  kvc_lossless_dec<<<(unsigned)blocks, LT, smem, (cudaStream_t)stream>>>(p, f);
   return (int)cudaGetLastError();
 }
 

@@ -192,8 +192,11 @@ def test_nonfinite_and_range_flags_match_oracle():
             assert np.array_equal(U.to_np(sg, nbytes), so)
 
 
-def test_corrupt_streams_are_rejected_and_outputs_untouched():
-    prof = dict(bits_k=4, bits_v=4, group_k=64, group_v=64, hadamard=True, stages=LC, chunk_bytes=1024)
+@pytest.mark.parametrize("chunk", [1024, 4096])
+def test_corrupt_streams_are_rejected_and_outputs_untouched(chunk):
+    """1 KiB chunks decode through the generic stage functions, 4 KiB chunks through
+    the fast chunk decoder; both must reject the same corruptions."""
+    prof = dict(bits_k=4, bits_v=4, group_k=64, group_v=64, hadamard=True, stages=LC, chunk_bytes=chunk)
     case = U.Case(L=1, T=300, H=2, dtype="bf16", dist="llama_sink", profile=prof, seed=4).materialize()
     codec, sg, nbytes, sg_np, so, _, _ = U.encode_both(case)
     lay = O.layout(U.oracle_profile(prof), case.oracle_shape())
