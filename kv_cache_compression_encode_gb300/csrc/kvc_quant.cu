@@ -81,6 +81,46 @@ __device__ __forceinline__ void put_code(uint32_t (&w)[NW], int idx, uint32_t c)
   if (sh + BITS > 32) w[wi + 1] |= (c & M) >> (32 - sh);
 }
 
+// 32 codes (BITS each, LSB first) -> 16 float pairs, exactly.
+template <int BITS>
+__device__ __forceinline__ void codes_to_f2(const uint32_t (&w)[BITS], float2 (&q)[16]) {
+  constexpr uint32_t kE = 0x4B000000u;  // the bits of 2^23
+  uint32_t b[32];
+  if constexpr (BITS == 4) {
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      const uint32_t lo = w[k] & 0x0F0F0F0Fu, hi = (w[k] >> 4) & 0x0F0F0F0Fu;  // byte j: codes 8k+2j, 8k+2j+1
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        b[8 * k + 2 * j] = __byte_perm(lo, kE, 0x7440u | j);
+        b[8 * k + 2 * j + 1] = __byte_perm(hi, kE, 0x7440u | j);
+      }
+    }
+  } else if constexpr (BITS == 8) {
+#pragma unroll
+    for (int k = 0; k < 8; k++)
+#pragma unroll
+      for (int j = 0; j < 4; j++) b[4 * k + j] = __byte_perm(w[k], kE, 0x7440u | j);
+  } else if constexpr (BITS == 2) {
+#pragma unroll
+    for (int k = 0; k < 2; k++)
+#pragma unroll
+      for (int f = 0; f < 4; f++) {
+        const uint32_t m = (w[k] >> (2 * f)) & 0x03030303u;  // byte j: code 16k + 4j + f
+#pragma unroll
+        for (int j = 0; j < 4; j++) b[16 * k + 4 * j + f] = __byte_perm(m, kE, 0x7440u | j);
+      }
+  } else {
+    uint32_t c[32];
+    unpack32<BITS>(w, c);
+#pragma unroll
+    for (int i = 0; i < 32; i++) b[i] = c[i] | kE;
+  }
+  const float2 e2 = bcast2(8388608.0f);
+#pragma unroll
+  for (int i = 0; i < 16; i++) q[i] = sub2(make_float2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1])), e2);
+}
+
 template <int BITS, bool HAD, bool BF16>
 __global__ void __launch_bounds__(kThreads, 2) kvc_enc_rows(const QuantParams P) {
   __shared__ uint32_t smask[2][32];
@@ -210,43 +250,88 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_rows(const QuantParams P)
 // ---------------------------------------------------------------------------
 // rows: decode
 // ---------------------------------------------------------------------------
-template <int BITS, bool HAD>
-__global__ void __launch_bounds__(kThreads) kvc_dec_rows(const QuantParams P) {
+template <int BITS, bool HAD, bool BF16>
+__global__ void __launch_bounds__(kThreads, 2) kvc_dec_rows(const QuantParams P) {
   if (P.check_corrupt && (*(volatile uint32_t *)P.status & KVC_FLAG_CORRUPT)) return;
+  __shared__ __align__(16) uint32_t fsign[2][64];  // bit 31 set where channel 64 half + c has Hadamard sign -1
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int part = lane & 3, rsub = lane >> 2;
-  const bool bf16 = P.g.bf16 != 0;
+  const int half = lane & 1, rsub = lane >> 1;
   const uint32_t H = P.g.H, T = P.g.T;
   const uint32_t NR = P.g.L * T * H;
-  const uint32_t n_it = (NR + 7) / 8;
-  const int gl = (int)(P.group >> 5);
-  const uint32_t row_code_bytes = kHeadDim * BITS / 8;
-  const uint32_t groups_per_row = kHeadDim / P.group;
-  const uint32_t sbits = P.sign[part];
+  const uint32_t n_it = (NR + 15) / 16;
+  const uint32_t G = P.group;
+  if (HAD && threadIdx.x < 128) {
+    const int c = threadIdx.x;
+    fsign[c >> 6][c & 63] = ((P.sign[c >> 5] >> (c & 31)) & 1u) << 31;
+  }
+  __syncthreads();
+  const float sg = half ? -1.0f : 1.0f;  // stride 64: lower lane a + b, upper lane a - b = -b + a
   uint32_t flags = 0;
 
   for (uint32_t it = blockIdx.x * (kThreads / 32) + warp; it < n_it; it += gridDim.x * (kThreads / 32)) {
-    const uint32_t R = it * 8 + rsub;
+    const uint32_t R = it * 16 + rsub;
     const bool valid = R < NR;
-    float v[32];
-    if (valid) {
-      uint32_t wds[BITS], q[32];
-      load_words<BITS>(P.codes + (size_t)R * row_code_bytes + 4 * BITS * part, wds);
-      const uint32_t meta =
-          *reinterpret_cast<const uint32_t *>(P.meta + ((size_t)R * groups_per_row + part / gl) * 4);
-      const float s = __half2float(__ushort_as_half((unsigned short)(meta & 0xffffu)));
-      const float z = __half2float(__ushort_as_half((unsigned short)(meta >> 16)));
-      unpack32<BITS>(wds, q);
+    float2 w[32];  // channels 64 half + 2i, +1
+    {
+      uint32_t cw[2 * BITS];
+      uint32_t m0 = 0, m1 = 0;  // group metadata of channels 64 half + 0..31 / 32..63
 #pragma unroll
-      for (int i = 0; i < 32; i++) v[i] = __fmaf_rn((float)q[i], s, z);
-    } else {
+      for (int k = 0; k < 2 * BITS; k++) cw[k] = 0u;
+      if (valid) {
+        const uint8_t *src = P.codes + (size_t)R * (kHeadDim * BITS / 8) + 8 * BITS * half;
+        if constexpr ((2 * BITS) % 4 == 0) {
 #pragma unroll
-      for (int i = 0; i < 32; i++) v[i] = 0.0f;
+          for (int k = 0; k < 2 * BITS; k += 4) {
+            const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src + 4 * k));
+            cw[k] = a.x; cw[k + 1] = a.y; cw[k + 2] = a.z; cw[k + 3] = a.w;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 2 * BITS; k += 2) {
+            const uint2 a = __ldg(reinterpret_cast<const uint2 *>(src + 4 * k));
+            cw[k] = a.x; cw[k + 1] = a.y;
+          }
+        }
+        const uint32_t *mp = reinterpret_cast<const uint32_t *>(P.meta);
+        if (G == 32) {
+          const uint2 mm = __ldg(reinterpret_cast<const uint2 *>(mp + (size_t)R * 4 + 2 * half));
+          m0 = mm.x;
+          m1 = mm.y;
+        } else {
+          m0 = m1 = __ldg(mp + (G == 64 ? (size_t)R * 2 + half : (size_t)R));
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {  // codes 32 hh .. 32 hh + 31
+        uint32_t wv[BITS];
+#pragma unroll
+        for (int k = 0; k < BITS; k++) wv[k] = cw[hh * BITS + k];
+        float2 qf[16];
+        codes_to_f2<BITS>(wv, qf);
+        const uint32_t m = hh ? m1 : m0;
+        const float2 s2 = bcast2(__half2float(__ushort_as_half((unsigned short)(m & 0xffffu))));
+        const float2 z2 = bcast2(__half2float(__ushort_as_half((unsigned short)(m >> 16))));
+#pragma unroll
+        for (int i = 0; i < 16; i++) w[16 * hh + i] = __ffma2_rn(qf[i], s2, z2);
+      }
     }
     if (HAD) {
-      fwht128(v, part);
-      scale_all(v, hadamard_scale());
-      apply_signs(v, sbits);
+      fwht64_pairs(w);
+      const float2 c2 = bcast2(hadamard_scale()), sg2 = bcast2(sg);
+#pragma unroll
+      for (int i = 0; i < 32; i++) {
+        const float2 o = make_float2(__shfl_xor_sync(kFull, w[i].x, 1), __shfl_xor_sync(kFull, w[i].y, 1));
+        w[i] = mul2(__ffma2_rn(w[i], sg2, o), c2);
+      }
+      const uint4 *fs = reinterpret_cast<const uint4 *>(fsign[half]);
+#pragma unroll
+      for (int k = 0; k < 16; k++) {  // signs of channels 4k .. 4k + 3 of this half
+        const uint4 m = fs[k];
+        w[2 * k].x = __uint_as_float(__float_as_uint(w[2 * k].x) ^ m.x);
+        w[2 * k].y = __uint_as_float(__float_as_uint(w[2 * k].y) ^ m.y);
+        w[2 * k + 1].x = __uint_as_float(__float_as_uint(w[2 * k + 1].x) ^ m.z);
+        w[2 * k + 1].y = __uint_as_float(__float_as_uint(w[2 * k + 1].y) ^ m.w);
+      }
     }
     if (valid) {
       const uint32_t h = R % H, lt = R / H, t = lt % T, l = lt / T;
@@ -255,9 +340,23 @@ __global__ void __launch_bounds__(kThreads) kvc_dec_rows(const QuantParams P) {
         flags |= KVC_FLAG_BAD_PAGE;
       } else {
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.layers[l]) + ro +
-                                               (size_t)(h * kHeadDim + 32 * part) * 2);
+                                               (size_t)(h * kHeadDim + 64 * half) * 2);
 #pragma unroll
-        for (int j = 0; j < 4; j++) dst[j] = pack8(v + 8 * j, bf16);
+        for (int k = 0; k < 8; k++) {
+          uint32_t u[4];
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            const float2 x = w[4 * k + e];
+            if (BF16) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(x.x, x.y);
+              u[e] = *reinterpret_cast<const uint32_t *>(&b2);
+            } else {
+              const __half2 h2 = __floats2half2_rn(x.x, x.y);
+              u[e] = *reinterpret_cast<const uint32_t *>(&h2);
+            }
+          }
+          dst[k] = make_uint4(u[0], u[1], u[2], u[3]);
+        }
       }
     }
   }
@@ -988,45 +1087,6 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P, con
 // ---------------------------------------------------------------------------
 constexpr int kKD = 128;
 
-// 32 codes (BITS each, LSB first) -> 16 float pairs, exactly.
-template <int BITS>
-__device__ __forceinline__ void codes_to_f2(const uint32_t (&w)[BITS], float2 (&q)[16]) {
-  constexpr uint32_t kE = 0x4B000000u;  // the bits of 2^23
-  uint32_t b[32];
-  if constexpr (BITS == 4) {
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-      const uint32_t lo = w[k] & 0x0F0F0F0Fu, hi = (w[k] >> 4) & 0x0F0F0F0Fu;  // byte j: codes 8k+2j, 8k+2j+1
-#pragma unroll
-      for (int j = 0; j < 4; j++) {
-        b[8 * k + 2 * j] = __byte_perm(lo, kE, 0x7440u | j);
-        b[8 * k + 2 * j + 1] = __byte_perm(hi, kE, 0x7440u | j);
-      }
-    }
-  } else if constexpr (BITS == 8) {
-#pragma unroll
-    for (int k = 0; k < 8; k++)
-#pragma unroll
-      for (int j = 0; j < 4; j++) b[4 * k + j] = __byte_perm(w[k], kE, 0x7440u | j);
-  } else if constexpr (BITS == 2) {
-#pragma unroll
-    for (int k = 0; k < 2; k++)
-#pragma unroll
-      for (int f = 0; f < 4; f++) {
-        const uint32_t m = (w[k] >> (2 * f)) & 0x03030303u;  // byte j: code 16k + 4j + f
-#pragma unroll
-        for (int j = 0; j < 4; j++) b[16 * k + 4 * j + f] = __byte_perm(m, kE, 0x7440u | j);
-      }
-  } else {
-    uint32_t c[32];
-    unpack32<BITS>(w, c);
-#pragma unroll
-    for (int i = 0; i < 32; i++) b[i] = c[i] | kE;
-  }
-  const float2 e2 = bcast2(8388608.0f);
-#pragma unroll
-  for (int i = 0; i < 16; i++) q[i] = sub2(make_float2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1])), e2);
-}
 
 // The D-phase inputs of a tile for channel c, copied by thread c into its own
 // slots of the shared buffers (so only thread c reads them, after its own
@@ -1410,7 +1470,7 @@ static int dispatch(const QuantParams &p, const TmaMaps *maps, bool had, bool en
                     const char **name) {
   const bool tile = use_tile(p);
   const uint64_t rows = (uint64_t)p.g.L * p.g.T * p.g.H;
-  const uint64_t units = tile ? (uint64_t)p.g.L * p.g.H * p.n_sb : (enc ? (rows + 127) / 128 : (rows + 63) / 64);
+  const uint64_t units = tile ? (uint64_t)p.g.L * p.g.H * p.n_sb : (rows + 127) / 128;
   if (enc) {
     if (p.axis == KVC_AXIS_OVER_TOKENS) {
       *name = "kvc_enc_ktile";
@@ -1446,8 +1506,11 @@ static int dispatch(const QuantParams &p, const TmaMaps *maps, bool had, bool en
                : run(kvc_dec_tile<BITS, false>, true, p, sm, st, units);
   }
   *name = "kvc_dec_rows";
-  return had ? run(kvc_dec_rows<BITS, true>, false, p, sm, st, units)
-             : run(kvc_dec_rows<BITS, false>, false, p, sm, st, units);
+  if (p.g.bf16)
+    return had ? run(kvc_dec_rows<BITS, true, true>, false, p, sm, st, units)
+               : run(kvc_dec_rows<BITS, false, true>, false, p, sm, st, units);
+  return had ? run(kvc_dec_rows<BITS, true, false>, false, p, sm, st, units)
+             : run(kvc_dec_rows<BITS, false, false>, false, p, sm, st, units);
 }
 
 static int dispatch_bits(const QuantParams &p, const TmaMaps *maps, bool enc, int sm, void *st, uint64_t *launches,
