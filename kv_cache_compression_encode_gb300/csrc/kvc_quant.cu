@@ -121,6 +121,34 @@ __device__ __forceinline__ void codes_to_f2(const uint32_t (&w)[BITS], float2 (&
   for (int i = 0; i < 16; i++) q[i] = sub2(make_float2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1])), e2);
 }
 
+// Codes of 32 qfast2 sums (bits 0x4B400000 + code, the code in the low byte) into
+// BITS words, LSB first.  2 and 4 bits: the codes of a byte are gathered with
+// integer multiply-adds (the magic's low byte is 0, so the low byte of
+// u1 * 2^BITS + u0 is code0 | code1 << BITS), bytes into words by byte_perm.
+template <int BITS>
+__device__ __forceinline__ void pack_sums32(const uint32_t (&u)[32], uint32_t (&cw)[BITS]) {
+  if constexpr (BITS == 4 || BITS == 2 || BITS == 8) {
+    constexpr int per_byte = 8 / BITS;
+    uint32_t b[4 * BITS];  // one byte (in the low 8 bits) per 8 / BITS codes
+#pragma unroll
+    for (int i = 0; i < 4 * BITS; i++) {
+      uint32_t x = u[per_byte * i + per_byte - 1];
+#pragma unroll
+      for (int j = per_byte - 2; j >= 0; j--) x = x * (1u << BITS) + u[per_byte * i + j];
+      b[i] = x;
+    }
+#pragma unroll
+    for (int w = 0; w < BITS; w++)
+      cw[w] = __byte_perm(__byte_perm(b[4 * w], b[4 * w + 1], 0x0040), __byte_perm(b[4 * w + 2], b[4 * w + 3], 0x0040),
+                          0x5410);
+  } else {
+#pragma unroll
+    for (int i = 0; i < BITS; i++) cw[i] = 0u;
+#pragma unroll
+    for (int i = 0; i < 32; i++) put_code<BITS>(cw, i, u[i]);
+  }
+}
+
 template <int BITS, bool HAD, bool BF16>
 __global__ void __launch_bounds__(kThreads, 2) kvc_enc_rows(const QuantParams P) {
   __shared__ uint32_t smask[2][32];
@@ -202,19 +230,26 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_rows(const QuantParams P)
     uint32_t f0 = 0, f1 = 0;
     const uint32_t meta0 = quant_params<BITS>(mn0, mx0, s0, z0, r0, f0);
     const uint32_t meta1 = quant_params<BITS>(mn1, mx1, s1, z1, r1, f1);
-    bool bad = f0 != 0 || f1 != 0;
     uint32_t wds[2 * BITS];
-#pragma unroll
-    for (int j = 0; j < 2 * BITS; j++) wds[j] = 0u;
+    float dm = 0.0f;
     {
       const float2 za = bcast2(z0), ra = bcast2(r0), zb = bcast2(z1), rb = bcast2(r1);
 #pragma unroll
-      for (int i = 0; i < 32; i++) {
-        const float2 u = qfast2<BITS>(w[i], i < 16 ? za : zb, i < 16 ? ra : rb, bad);
-        put_code<BITS>(wds, 2 * i, __float_as_uint(u.x));
-        put_code<BITS>(wds, 2 * i + 1, __float_as_uint(u.y));
+      for (int hh = 0; hh < 2; hh++) {  // codes 32 hh .. 32 hh + 31
+        uint32_t u[32];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+          const float2 s2 = qfast2m(w[16 * hh + i], hh ? zb : za, hh ? rb : ra, dm);
+          u[2 * i] = __float_as_uint(s2.x);
+          u[2 * i + 1] = __float_as_uint(s2.y);
+        }
+        uint32_t cw[BITS];
+        pack_sums32<BITS>(u, cw);
+#pragma unroll
+        for (int k = 0; k < BITS; k++) wds[hh * BITS + k] = cw[k];
       }
     }
+    bool bad = f0 != 0 || f1 != 0 || !(dm < tie_threshold<BITS>());
     if (__any_sync(kFull, bad)) {
       if (bad) {
 #pragma unroll
@@ -750,33 +785,6 @@ __device__ __forceinline__ void store_codes32(uint8_t *dst, const uint32_t (&cw)
   }
 }
 
-// Codes of 32 qfast2 sums (bits 0x4B400000 + code, the code in the low byte) into
-// BITS words, LSB first.  2 and 4 bits: the codes of a byte are gathered with
-// integer multiply-adds (the magic's low byte is 0, so the low byte of
-// u1 * 2^BITS + u0 is code0 | code1 << BITS), bytes into words by byte_perm.
-template <int BITS>
-__device__ __forceinline__ void pack_sums32(const uint32_t (&u)[32], uint32_t (&cw)[BITS]) {
-  if constexpr (BITS == 4 || BITS == 2 || BITS == 8) {
-    constexpr int per_byte = 8 / BITS;
-    uint32_t b[4 * BITS];  // one byte (in the low 8 bits) per 8 / BITS codes
-#pragma unroll
-    for (int i = 0; i < 4 * BITS; i++) {
-      uint32_t x = u[per_byte * i + per_byte - 1];
-#pragma unroll
-      for (int j = per_byte - 2; j >= 0; j--) x = x * (1u << BITS) + u[per_byte * i + j];
-      b[i] = x;
-    }
-#pragma unroll
-    for (int w = 0; w < BITS; w++)
-      cw[w] = __byte_perm(__byte_perm(b[4 * w], b[4 * w + 1], 0x0040), __byte_perm(b[4 * w + 2], b[4 * w + 3], 0x0040),
-                          0x5410);
-  } else {
-#pragma unroll
-    for (int i = 0; i < BITS; i++) cw[i] = 0u;
-#pragma unroll
-    for (int i = 0; i < 32; i++) put_code<BITS>(cw, i, u[i]);
-  }
-}
 
 // Tile coordinates, advanced by a fixed number of tiles without divisions.
 struct TilePos {
