@@ -227,9 +227,16 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_rows(const QuantParams P)
     if (valid && !finite2(mn0, mx0)) flags |= KVC_FLAG_NONFINITE;
     if (valid && !finite2(mn1, mx1)) flags |= KVC_FLAG_NONFINITE;
     float s0, z0, r0, s1, z1, r1;
-    uint32_t f0 = 0, f1 = 0;
+    uint32_t f0 = 0, f1 = 0, meta1;
     const uint32_t meta0 = quant_params<BITS>(mn0, mx0, s0, z0, r0, f0);
-    const uint32_t meta1 = quant_params<BITS>(mn1, mx1, s1, z1, r1, f1);
+    if (G == 32) {
+      meta1 = quant_params<BITS>(mn1, mx1, s1, z1, r1, f1);
+    } else {  // one group per lane: the second half shares the first half's parameters
+      meta1 = meta0;
+      s1 = s0;
+      z1 = z0;
+      r1 = r0;
+    }
     uint32_t wds[2 * BITS];
     float dm = 0.0f;
     {
