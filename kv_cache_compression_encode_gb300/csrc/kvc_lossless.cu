@@ -1096,19 +1096,28 @@ __global__ void __launch_bounds__(PT) kvc_decode_prepare(const LosslessParams P)
     } else if (stream_bytes < P.data_start) {
       if (tid == 0) s_bad = 1;
     } else {
+      // thread tid takes entries [S tid, S tid + S), S a multiple of 4: 16-byte
+      // loads of the table (the table is 16-byte aligned and padded to data_start)
       const uint32_t nc = P.n_chunks;
-      const uint32_t S = (nc + PT - 1) / PT;
+      const uint32_t S = ((nc + PT - 1) / PT + 3) & ~3u;
       const uint32_t i0 = min(nc, tid * S), i1 = min(nc, i0 + S);
       const uint32_t *table = reinterpret_cast<const uint32_t *>(P.stream + KVC_HEADER_BYTES);
       unsigned long long sum = 0;
       int bad = 0;
-      for (uint32_t i = i0; i < i1; i++) {
-        const uint32_t e = table[i], sz = e & 0x7fffffffu;
-        const uint64_t off = (uint64_t)i * P.chunk_bytes;
-        const uint32_t n = (uint32_t)min((uint64_t)P.chunk_bytes, P.payload_bytes - off);
-        if (e >> 31) bad |= sz != n;
-        else bad |= sz >= n;
-        sum += align16u(sz);
+      for (uint32_t i = i0; i < i1; i += 4) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(table + i);
+        const uint32_t e4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          if (i + k < i1) {
+            const uint32_t e = e4[k], sz = e & 0x7fffffffu;
+            const uint64_t off = (uint64_t)(i + k) * P.chunk_bytes;
+            const uint32_t n = (uint32_t)min((uint64_t)P.chunk_bytes, P.payload_bytes - off);
+            if (e >> 31) bad |= sz != n;
+            else bad |= sz >= n;
+            sum += align16u(sz);
+          }
+        }
       }
       if (bad) atomicOr(&s_bad, 1);
       // exclusive scan of the aligned sizes (64-bit)
@@ -1132,9 +1141,23 @@ __global__ void __launch_bounds__(PT) kvc_decode_prepare(const LosslessParams P)
       }
       __syncthreads();
       unsigned long long pos = P.data_start + x - sum + (warp ? tmp[warp - 1] : 0ull);
-      for (uint32_t i = i0; i < i1; i++) {
-        P.state[i] = pos;
-        pos += align16u(table[i] & 0x7fffffffu);
+      for (uint32_t i = i0; i < i1; i += 4) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(table + i);
+        const uint32_t e4[4] = {q.x, q.y, q.z, q.w};
+        unsigned long long o4[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          o4[k] = pos;
+          if (i + k < i1) pos += align16u(e4[k] & 0x7fffffffu);
+        }
+        if (i + 4 <= i1) {  // offsets of four chunks: two 16-byte stores
+          reinterpret_cast<ulonglong2 *>(P.state + i)[0] = make_ulonglong2(o4[0], o4[1]);
+          reinterpret_cast<ulonglong2 *>(P.state + i)[1] = make_ulonglong2(o4[2], o4[3]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; k++)
+            if (i + k < i1) P.state[i + k] = o4[k];
+        }
       }
       if (tid == 0 && P.data_start + tmp[PT / 32] > stream_bytes) s_bad = 1;
     }
