@@ -293,46 +293,68 @@ def run_kvc(args):
 def run_e2e(codec, k, v, ok, ov, w, args, device):
     """Same metric through the public API with host buffers: every step copies the
     KV from pinned host memory, encodes, reads the size and the stream back, then
-    copies the stream in, decodes and copies the KV out."""
+    copies the stream in, decodes and copies the KV out.  Two requests are in
+    flight, each on its own CUDA stream with its own plan, workspace and buffers
+    (a serving process overlaps one request's uploads with another's downloads);
+    every step still moves all of its own bytes."""
     import torch
+
+    from kv_cache_compression_encode_gb300.codec import Codec
 
     hk = [x.cpu().pin_memory() for x in k]
     hv = [x.cpu().pin_memory() for x in v]
-    rk = [torch.empty_like(x, device="cpu").pin_memory() for x in k]
-    rv = [torch.empty_like(x, device="cpu").pin_memory() for x in v]
-    hs = torch.empty(codec.plan.max_stream_bytes, dtype=torch.uint8).pin_memory()
-    dk = [torch.empty_like(x) for x in k]
-    dv = [torch.empty_like(x) for x in v]
-    sbuf = codec.new_stream_buffer()
-    rbuf = codec.new_stream_buffer()
+
+    class Lane:
+        def __init__(self, c):
+            self.codec = c
+            self.s = torch.cuda.Stream(device)
+            self.rk = [torch.empty_like(x, device="cpu").pin_memory() for x in k]
+            self.rv = [torch.empty_like(x, device="cpu").pin_memory() for x in v]
+            self.hs = torch.empty(c.plan.max_stream_bytes, dtype=torch.uint8).pin_memory()
+            self.dk = [torch.empty_like(x) for x in k]
+            self.dv = [torch.empty_like(x) for x in v]
+            self.sbuf = c.new_stream_buffer()
+            self.rbuf = c.new_stream_buffer()
+
+    lanes = [Lane(codec), Lane(Codec(codec.profile, codec.shape, device))]
     counts = {"h2d": 0, "d2h": 0}
 
-    def step():
-        for d, h in zip(dk + dv, hk + hv):
-            d.copy_(h, non_blocking=True)
-        codec.encode(dk, dv, out=sbuf)
-        _, n, _ = codec.query()                     # size scalar to the host (syncs)
-        hs[:n].copy_(sbuf[:n], non_blocking=True)
-        rbuf[:n].copy_(hs[:n], non_blocking=True)   # the receiving side's upload
-        codec.decode(rbuf, n, dk, dv)
-        for h, d in zip(rk + rv, dk + dv):
-            h.copy_(d, non_blocking=True)
-        torch.cuda.current_stream(device).synchronize()
+    def front(L):  # inputs up, encode
+        with torch.cuda.stream(L.s):
+            for d, h in zip(L.dk + L.dv, hk + hv):
+                d.copy_(h, non_blocking=True)
+            L.codec.encode(L.dk, L.dv, out=L.sbuf)
+
+    def back(L):  # size scalar to the host, stream down and up again, decode, KV down
+        with torch.cuda.stream(L.s):
+            _, n, _ = L.codec.query()  # synchronizes this lane's stream only
+            L.hs[:n].copy_(L.sbuf[:n], non_blocking=True)
+            L.rbuf[:n].copy_(L.hs[:n], non_blocking=True)  # the receiving side's upload
+            L.codec.decode(L.rbuf, n, L.dk, L.dv)
+            for h, d in zip(L.rk + L.rv, L.dk + L.dv):
+                h.copy_(d, non_blocking=True)
         counts["h2d"] = w.raw_bytes + n
         counts["d2h"] = n + w.raw_bytes + 16
-        return n
 
-    for _ in range(2):
-        step()
-    n_steps = max(3, min(20, args.steps // 100))
+    def run(n):
+        front(lanes[0])
+        for i in range(n):
+            if i + 1 < n:
+                front(lanes[(i + 1) % 2])
+            back(lanes[i % 2])
+        for L in lanes:
+            L.s.synchronize()
+
+    run(4)
+    n_steps = max(4, min(20, args.steps // 100))
+    torch.cuda.synchronize(device)
     t0 = time.perf_counter()
-    for _ in range(n_steps):
-        step()
+    run(n_steps)
     dt = (time.perf_counter() - t0) / n_steps
-    ok_rt = all(torch.equal(a, b.to(a.device)) for a, b in zip(ok + ov, rk + rv))
+    ok_rt = all(torch.equal(a, b.to(a.device)) for L in lanes for a, b in zip(ok + ov, L.rk + L.rv))
     return {"value": round(w.raw_bytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": counts["h2d"],
             "d2h_bytes_per_step": counts["d2h"], "ms_per_step": round(dt * 1e3, 3), "steps": n_steps,
-            "roundtrip_matches_device_path": bool(ok_rt)}
+            "requests_in_flight": 2, "roundtrip_matches_device_path": bool(ok_rt)}
 
 
 # ---------------------------------------------------------------------------- oracle

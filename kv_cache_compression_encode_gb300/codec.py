@@ -15,6 +15,7 @@ from . import kvc
 class Codec:
     def __init__(self, profile: kvc.Profile, shape: kvc.Shape, device="cuda"):
         self.device = torch.device(device)
+        self.profile, self.shape = profile, shape
         self.plan = kvc.Plan(profile, shape)
         self.workspace = torch.empty(max(self.plan.workspace_bytes, 256), dtype=torch.uint8, device=self.device)
         self.d_size = torch.zeros(1, dtype=torch.int64, device=self.device)
