@@ -503,33 +503,38 @@ __global__ void __launch_bounds__(LT) kvc_lossless_enc(const LosslessParams P) {
 // ===========================================================================
 // Fast encoder for the stage lists TUPL_8 [BIT_8] [DELTA_1] RZE_w (w = 1 or 2)
 // and chunk sizes that are multiples of 4 KiB up to 16 KiB.  A CTA holds eight
-// worker warps and one publisher warp.
-//  * Workers: each chunk arrives by cp.async in a slot of a ring.  TUPL_8 (and
-//    BIT_8) run as one register transform per 8-tuple block (a 4x4 byte
-//    transpose gathers byte j of the 8 tuples, an 8x8 bit transpose makes the 8
-//    bit-plane bytes) into a scratch buffer, stored swizzled so that the next
-//    pass reads it without bank conflicts; then the next chunk's load is
-//    issued into the next slot.  DELTA_1 and RZE run as one register pass: a
+// worker warps, two publisher warps and one loader warp, around a ring of
+// kRing chunk slots.
+//  * Loader: takes the CTA's next ticket (at most kAhead chunks ahead of the
+//    workers), announces it to the publishers and fetches the chunk into its
+//    slot with one bulk copy, completing on the slot's mbarrier.
+//  * Workers: with BIT_8 the chunk's encoded size is first computed from the
+//    chunk as loaded (fast_size_bit8) and published for the look-back at once;
+//    an incompressible chunk is then done.  Otherwise TUPL_8 (and BIT_8) run
+//    as one register transform per 8-tuple block (a 4x4 byte transpose gathers
+//    byte j of the 8 tuples, an 8x8 bit transpose makes the 8 bit-plane bytes)
+//    into a scratch buffer, stored swizzled so that the next pass reads it
+//    without bank conflicts.  DELTA_1 and RZE run as one register pass: a
 //    thread owns 64 contiguous bytes, takes the word bitmaps of the byte
-//    differences, and one block scan of its counts gives its output offsets.  The encoded size is known before anything is written, so the
-//    chunk's aligned size is published for the look-back right then, and an
-//    incompressible chunk costs no compaction: its slot still holds it as
-//    loaded.  Otherwise the encoded chunk is written over it.  The slot is then
-//    handed to the publisher.
-//  * Publisher: the workers announce each ticket the moment they take it, so
-//    the publisher walks back over the chunk's predecessors (32 at a time)
+//    differences, and one block scan of its counts gives its output offsets;
+//    the encoded chunk is written over its slot.  The slot is then handed to a
+//    publisher.
+//  * Publishers (chunks k = p, p + 2, ... for warp p): each walks back over the
+//    chunk's predecessors (32 at a time) as soon as its ticket is announced,
 //    while the chunk is still being encoded.  When the slot is full it
 //    publishes the inclusive prefix, writes the chunk-table entry, copies the
 //    chunk to the stream with one bulk copy and hands the slot back once the
-//    copy has read it.  Workers never wait on other CTAs, only on a slot of
+//    copy has read it.  Workers never wait on other CTAs, only on slots of
 //    their own ring.
-// Tickets, full slots and free slots pass between the two sides through
+// Tickets, loaded, started, full and free slots pass between the warps through
 // mbarriers; every wait is bounded and sets KVC_FLAG_TIMEOUT when it runs out.  A
 // chunk whose length is not a multiple of 4 KiB (only the last one can be) runs
 // the generic stage functions on the worker threads.
 // ===========================================================================
 constexpr int FT = 256;        // worker threads
-constexpr int FW = FT + 32;    // workers + the publisher warp
+constexpr int kPubWarps = 2;  // publisher warps, taking the CTA's chunks in turn
+constexpr int FW = FT + 32 * kPubWarps + 32;  // workers + publishers + the loader warp
+constexpr uint32_t kAhead = 2;  // the loader takes a ticket at most this many chunks ahead
 constexpr int kRing = 5;       // slots per CTA (16 KiB chunks: 2 CTAs per SM)
 constexpr int kFastCtasPerSm = 2;
 constexpr uint32_t kFastMaxChunk = 16384;
@@ -550,6 +555,11 @@ __device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(b)) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t *b, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_addr(b)),
+               "r"(bytes)
+               : "memory");
+}
 // Waits until the phase of parity `par` has completed; false after kMbarTries tries.
 __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t par) {
   for (uint32_t i = 0; i < kMbarTries; i++) {
@@ -569,13 +579,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t par) {
 // 8 distinct bank groups.  swzb is that map on a byte offset.
 __device__ __forceinline__ uint32_t swzb(uint32_t x) { return (x & ~0x30u) | ((((x >> 4) + (x >> 7)) & 3u) << 4); }
 __device__ __forceinline__ bool fast_len(uint32_t n) { return (n & 4095u) == 0 && n <= kFastMaxChunk; }
-
-__device__ void issue_chunk_load(const LosslessParams &P, uint32_t t, uint8_t *dst) {
-  const uint64_t off = (uint64_t)t * P.chunk_bytes;
-  const uint32_t n = (uint32_t)min((uint64_t)P.chunk_bytes, P.payload_bytes - off);
-  const uint8_t *src = P.payload + off;
-  for (uint32_t u = threadIdx.x; u < n / 16; u += FT) cp_async16(dst + 16 * u, src + 16 * u);
-}
 
 // 4x4 byte transpose: o[j] = byte j of a, b, c, d.
 __device__ __forceinline__ void byte_t4x4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t (&o)[4]) {
@@ -639,6 +642,125 @@ __device__ void fast_transform(const uint8_t *in, uint8_t *out, uint32_t n) {
   bsync<FT>();
 }
 
+// The encoded size of a fast chunk under TUPL_8, BIT_8, [DELTA_1], RZE_w computed
+// from the chunk as loaded (plain, in shared memory), without the transform.
+// Bit-plane byte (p, j) of block beta holds bit p of byte j of the block's 8
+// tuples, so it is nonzero iff bit p of OR_i tuple_i[j] is set; with DELTA_1 the
+// stream byte is nonzero iff the plane byte differs from the one before it, which
+// for beta > 0 is the same plane's byte in block beta - 1: bit p of
+// OR_i (tuple_i[j] ^ prev_tuple_i[j]).  So 64 nonzero flags per block come from an
+// OR-fold of the block (XOR'd with the previous one); block 0, whose predecessors
+// are the last bytes of the previous planes, takes the real transform of blocks 0
+// and n/64 - 1.  Elements (W = 2: the plane bytes of blocks 2u, 2u + 1) and
+// level-1 bitmap bytes (8 elements: 8 W consecutive blocks of one plane) are ORs
+// of these flags across neighbouring threads.  Returns nb2 + totB + W totW, the
+// size the full pass computes (uniform across the CTA).
+__device__ __forceinline__ uint64_t plane_bytes(const uint32_t (&w)[16], uint32_t j) {  // byte p = plane (p, j)
+  const bool h = j >= 4;
+  uint32_t L[4], M[4];
+  byte_t4x4(h ? w[1] : w[0], h ? w[3] : w[2], h ? w[5] : w[4], h ? w[7] : w[6], L);
+  byte_t4x4(h ? w[9] : w[8], h ? w[11] : w[10], h ? w[13] : w[12], h ? w[15] : w[14], M);
+  const uint32_t q = j & 3u;
+  uint32_t lo = q == 0 ? L[0] : q == 1 ? L[1] : q == 2 ? L[2] : L[3];
+  uint32_t hi = q == 0 ? M[0] : q == 1 ? M[1] : q == 2 ? M[2] : M[3];
+  bits8x8(lo, hi);
+  return ((uint64_t)hi << 32) | lo;
+}
+
+template <int W, bool DELTA>
+__device__ uint32_t fast_size_bit8(const uint8_t *S, uint32_t n, uint32_t *wsum) {
+  const uint32_t nthr = n / 64, nb = n / (8 * W), nb2 = nb / 8;
+  const uint32_t t = threadIdx.x;
+  const int lane = t & 31, warp = t >> 5;
+  const bool active = t < nthr;
+  uint32_t olo = 0, ohi = 0;  // flag of plane (p, j): bit 8j + p of (ohi:olo)
+  if (active && !(DELTA && t == 0)) {
+    // the fold does not depend on the order of the four units: reading them
+    // rotated by (t >> 1) & 3 keeps 8 lanes on 8 distinct bank groups
+    const uint4 *blk = reinterpret_cast<const uint4 *>(S) + 4 * t;
+    const uint32_t rot = (t >> 1) & 3u;
+    uint32_t x[16];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      const uint4 v = blk[(k + rot) & 3u];
+      x[4 * k] = v.x; x[4 * k + 1] = v.y; x[4 * k + 2] = v.z; x[4 * k + 3] = v.w;
+    }
+    if (DELTA) {
+      const uint4 *pb = blk - 4;
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const uint4 v = pb[(k + rot) & 3u];
+        x[4 * k] ^= v.x; x[4 * k + 1] ^= v.y; x[4 * k + 2] ^= v.z; x[4 * k + 3] ^= v.w;
+      }
+    }
+    olo = x[0] | x[2] | x[4] | x[6] | x[8] | x[10] | x[12] | x[14];
+    ohi = x[1] | x[3] | x[5] | x[7] | x[9] | x[11] | x[13] | x[15];
+  }
+  if (DELTA && warp == 0) {  // block 0: lane j < 8 compares plane (p, j) with its predecessor in the last block
+    uint64_t pb0 = 0, pbl = 0;
+    if (lane < 8) {
+      uint32_t x[16], y[16];
+      const uint4 *b0 = reinterpret_cast<const uint4 *>(S), *bl = b0 + 4 * (nthr - 1);
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const uint4 v = b0[k], u = bl[k];
+        x[4 * k] = v.x; x[4 * k + 1] = v.y; x[4 * k + 2] = v.z; x[4 * k + 3] = v.w;
+        y[4 * k] = u.x; y[4 * k + 1] = u.y; y[4 * k + 2] = u.z; y[4 * k + 3] = u.w;
+      }
+      pb0 = plane_bytes(x, lane);
+      pbl = plane_bytes(y, lane);
+    }
+    // (p, j) follows (p, j - 1) of the last block; (p, 0) follows (p - 1, 7)
+    const uint64_t up = __shfl_up_sync(0xffffffffu, pbl, 1), l7 = __shfl_sync(0xffffffffu, pbl, 7);
+    const uint64_t pred = lane == 0 ? (l7 << 8) : up;
+    const uint64_t d = pb0 ^ pred;
+    const uint64_t f = (((d & 0x7f7f7f7f7f7f7f7full) + 0x7f7f7f7f7f7f7f7full) | d) & 0x8080808080808080ull;
+    const uint32_t fb = lane < 8 ? (uint32_t)(((f >> 7) * 0x0102040810204080ull) >> 56) : 0u;  // bit p
+    uint32_t lo0 = 0, hi0 = 0;
+#pragma unroll
+    for (int jj = 0; jj < 8; jj++) {
+      const uint32_t b = __shfl_sync(0xffffffffu, fb, jj);
+      if (jj < 4) lo0 |= b << (8 * jj);
+      else hi0 |= b << (8 * (jj - 4));
+    }
+    if (t == 0) {
+      olo = lo0;
+      ohi = hi0;
+    }
+  }
+  uint32_t cw = 0, cb = 0;
+  if (W == 2) {  // elements: the flags of blocks 2u and 2u + 1; bitmap bytes: 16 blocks
+    const uint32_t elo = olo | __shfl_xor_sync(0xffffffffu, olo, 1), ehi = ohi | __shfl_xor_sync(0xffffffffu, ohi, 1);
+    uint32_t glo = elo, ghi = ehi;
+#pragma unroll
+    for (int o = 2; o < 16; o <<= 1) {
+      glo |= __shfl_xor_sync(0xffffffffu, glo, o);
+      ghi |= __shfl_xor_sync(0xffffffffu, ghi, o);
+    }
+    if (active && (t & 1) == 0) cw = __popc(elo) + __popc(ehi);
+    if (active && (t & 15) == 0) cb = __popc(glo) + __popc(ghi);
+  } else {  // elements: the plane bytes; bitmap bytes: 8 blocks
+    uint32_t glo = olo, ghi = ohi;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      glo |= __shfl_xor_sync(0xffffffffu, glo, o);
+      ghi |= __shfl_xor_sync(0xffffffffu, ghi, o);
+    }
+    if (active) cw = __popc(olo) + __popc(ohi);
+    if (active && (t & 7) == 0) cb = __popc(glo) + __popc(ghi);
+  }
+  uint32_t c = (cb << 16) | cw;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  if (lane == 0) wsum[warp] = c;
+  bsync<FT>();
+  uint32_t tot = 0;
+#pragma unroll
+  for (int i = 0; i < FT / 32; i++) tot += wsum[i];
+  bsync<FT>();  // wsum is reused right after
+  return nb2 + (tot >> 16) + W * (tot & 0xffffu);
+}
+
 // DELTA_1 (optional) and RZE_w of a transformed fast chunk held swizzled in `in`;
 // the encoded chunk goes to `out` (which may be `in` itself: every read happens
 // before the first barrier).  Returns the encoded size; nothing is written when it
@@ -651,7 +773,7 @@ __device__ __forceinline__ void publish_size(const LosslessParams &P, uint32_t t
 
 template <int W, bool DELTA>
 __device__ uint32_t fast_delta_rze(const uint8_t *in, uint8_t *out, uint32_t n, uint32_t *wsum, const LosslessParams &P,
-                                   uint32_t ticket) {
+                                   uint32_t ticket, bool publish = true) {
   const uint32_t nthr = n / 64, nb = n / (8 * W), nb2 = nb / 8;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t t = threadIdx.x;
@@ -717,7 +839,7 @@ __device__ uint32_t fast_delta_rze(const uint8_t *in, uint8_t *out, uint32_t n, 
   }
   const uint32_t totB = tot >> 16, totW = tot & 0xffffu;
   const uint32_t size = nb2 + totB + W * totW;
-  if (t == 0) publish_size(P, ticket, align16u(size < n ? size : n));  // before the compaction
+  if (t == 0 && publish) publish_size(P, ticket, align16u(size < n ? size : n));  // before the compaction
   if (size >= n) return size;  // uniform: the chunk is stored raw
   const uint32_t ex = wb + sc - c;
   uint32_t rB = ex >> 16, rW = ex & 0xffffu;
@@ -783,27 +905,71 @@ __global__ void __launch_bounds__(FW, kFastCtasPerSm) kvc_lossless_enc_fast(cons
   uint32_t *wsum = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(Bs) + cb / 8 + 64);  // scan words
   // Chunk k of this CTA lives in slot k % kRing: loaded there, encoded over itself
   // when it compresses, copied out from there either way.  tick[j]: the ticket of
-  // chunk k (k % 2kRing == j) is announced, a value >= n_chunks meaning "no more
-  // chunks"; full[s]: the slot holds the chunk's stored bytes; empty[s]: the
-  // publisher is done with the slot.
-  __shared__ __align__(8) uint64_t s_tick[2 * kRing], s_full[kRing], s_empty[kRing];
+  // chunk k (k % 2kRing == j) is known, a value >= n_chunks meaning "no more
+  // chunks"; loaded[s]: the chunk has arrived (or the stop is known);
+  // started[s]: the workers have begun it; full[s]: the slot holds the chunk's
+  // stored bytes; empty[s]: the publisher is done with the slot.
+  __shared__ __align__(8) uint64_t s_tick[2 * kRing], s_loaded[kRing], s_started[kRing], s_full[kRing], s_empty[kRing];
   __shared__ uint32_t s_ticket[2 * kRing], s_word[kRing], s_from_payload[kRing];
-  __shared__ uint32_t s_t;
   const uint32_t nc = P.n_chunks;
-  uint32_t *ticket_ctr = P.ctrl + kCtrlTicket;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRing; s++) {
+      mbar_init(&s_loaded[s], 1);
+      mbar_init(&s_started[s], 1);
       mbar_init(&s_full[s], 1);
       mbar_init(&s_empty[s], 1);
     }
     for (int j = 0; j < 2 * kRing; j++) mbar_init(&s_tick[j], 1);
-    s_t = atomicAdd(ticket_ctr, 1u);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  if (threadIdx.x >= FT) {  // ---- publisher warp
+  if (threadIdx.x >= FT + 32 * kPubWarps) {  // ---- loader warp
+    if ((threadIdx.x & 31) != 0) return;
+    uint32_t *ticket_ctr = P.ctrl + kCtrlTicket;
+    uint32_t k = 0, first = 0;  // loads [first, k) may still be pending at the end
+    for (;; k++) {
+      const uint32_t s = k % kRing, j = k % (2 * kRing);
+      // a ticket is taken only kAhead chunks ahead of the workers (a ticket held
+      // while idle would hold up every later chunk's look-back), and the slot's
+      // previous chunk must have been copied out
+      if ((k >= kAhead && !mbar_wait(&s_started[(k - kAhead) % kRing], ((k - kAhead) / kRing) & 1u)) ||
+          (k >= kRing && !mbar_wait(&s_empty[s], (k / kRing - 1) & 1u))) {
+        atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
+        break;
+      }
+      const uint32_t t = atomicAdd(ticket_ctr, 1u);
+      if (t >= nc) {  // every publisher warp and the workers learn of the stop
+        for (uint32_t q = 0; q < (uint32_t)kPubWarps; q++) {
+          const uint32_t jq = (k + q) % (2 * kRing);
+          s_ticket[jq] = nc;
+          mbar_arrive(&s_tick[jq]);
+        }
+        mbar_arrive(&s_loaded[s]);
+        first = 1;  // chunk k - kRing's slot has been reused by the stop
+        break;
+      }
+      s_ticket[j] = t;
+      mbar_arrive(&s_tick[j]);
+      const uint64_t off = (uint64_t)t * cb;
+      const uint32_t n = (uint32_t)min((uint64_t)cb, P.payload_bytes - off);
+      mbar_arrive_tx(&s_loaded[s], n);
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+              smem_addr(ring + s * slot_bytes)),
+          "l"(P.payload + off), "r"(n), "r"(smem_addr(&s_loaded[s]))
+          : "memory");
+    }
+    // no load may still be landing when the CTA ends (only reachable with every
+    // load consumed, or after a timeout)
+    for (uint32_t q = k + first > kRing ? k + first - kRing : 0; q < k; q++)
+      mbar_wait(&s_loaded[q % kRing], (q / kRing) & 1u);
+    return;
+  }
+
+  if (threadIdx.x >= FT && threadIdx.x < FT + 32 * kPubWarps) {  // ---- publisher warps: chunks k = p, p + kPubWarps, ...
     const int lane = threadIdx.x & 31;
-    for (uint32_t k = 0;; k++) {
+    for (uint32_t k = (threadIdx.x - FT) >> 5;; k += kPubWarps) {
       const uint32_t j = k % (2 * kRing), s = k % kRing;
       if (!mbar_wait(&s_tick[j], (k / (2 * kRing)) & 1u)) {
         if (lane == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
@@ -853,42 +1019,46 @@ __global__ void __launch_bounds__(FW, kFastCtasPerSm) kvc_lossless_enc_fast(cons
   }
 
   // ---- workers
-  uint32_t t = s_t;
-  if (threadIdx.x == 0) {
-    s_ticket[0] = t;
-    mbar_arrive(&s_tick[0]);
-  }
-  if (t < nc) issue_chunk_load(P, t, ring);
-  cp_async_commit();
-  for (uint32_t k = 0; t < nc; k++) {
-    const uint32_t s = k % kRing, s1 = (k + 1) % kRing, jn = (k + 1) % (2 * kRing);
+  for (uint32_t k = 0;; k++) {
+    const uint32_t s = k % kRing;
     uint8_t *const S = ring + s * slot_bytes;
-    cp_async_wait<0>();
-    bsync<FT>();
+    if (!mbar_wait(&s_loaded[s], (k / kRing) & 1u)) {
+      if (threadIdx.x == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
+      break;
+    }
+    const uint32_t t = s_ticket[k % (2 * kRing)];
+    if (t >= nc) break;
+    if (threadIdx.x == 0) mbar_arrive(&s_started[s]);
 
     const uint64_t off = (uint64_t)t * cb;
     const uint32_t n = (uint32_t)min((uint64_t)cb, P.payload_bytes - off);
-    uint32_t size = n, tn;
+    uint32_t size = n;
     bool raw, from_payload = false;
     if (fast_len(n)) {
-      if (threadIdx.x == 0) {  // the next chunk: announced to the publisher at once, loaded after the transform
-        s_t = s_ticket[jn] = atomicAdd(ticket_ctr, 1u);
-        mbar_arrive(&s_tick[jn]);
-        if (k + 1 >= kRing && !mbar_wait(&s_empty[s1], ((k + 1) / kRing - 1) & 1u))
-          atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
+      // with BIT_8 the size is known from the chunk as loaded; an incompressible
+      // chunk then skips the transform altogether
+      uint32_t es = 0;
+      if (F.bit8) {
+        if (F.rze_w == 2) es = F.delta1 ? fast_size_bit8<2, true>(S, n, wsum) : fast_size_bit8<2, false>(S, n, wsum);
+        else es = F.delta1 ? fast_size_bit8<1, true>(S, n, wsum) : fast_size_bit8<1, false>(S, n, wsum);
+        if (threadIdx.x == 0) publish_size(P, t, align16u(es < n ? es : n));
       }
-      if (F.bit8) fast_transform<true>(S, A, n);
-      else fast_transform<false>(S, A, n);
-      tn = s_t;
-      if (tn < nc) issue_chunk_load(P, tn, ring + s1 * slot_bytes);
-      cp_async_commit();
-      uint32_t rs;
-      if (F.rze_w == 2)
-        rs = F.delta1 ? fast_delta_rze<2, true>(A, S, n, wsum, P, t) : fast_delta_rze<2, false>(A, S, n, wsum, P, t);
-      else
-        rs = F.delta1 ? fast_delta_rze<1, true>(A, S, n, wsum, P, t) : fast_delta_rze<1, false>(A, S, n, wsum, P, t);
-      raw = rs >= n;  // stored raw: the slot still holds the chunk as loaded
-      if (!raw) size = rs;
+      if (F.bit8 && es >= n) {
+        raw = true;  // the slot holds the chunk as loaded
+      } else {
+        if (F.bit8) fast_transform<true>(S, A, n);
+        else fast_transform<false>(S, A, n);
+        const bool pub = !F.bit8;  // with BIT_8 the size is already out
+        uint32_t rs;
+        if (F.rze_w == 2)
+          rs = F.delta1 ? fast_delta_rze<2, true>(A, S, n, wsum, P, t, pub) : fast_delta_rze<2, false>(A, S, n, wsum, P, t, pub);
+        else
+          rs = F.delta1 ? fast_delta_rze<1, true>(A, S, n, wsum, P, t, pub) : fast_delta_rze<1, false>(A, S, n, wsum, P, t, pub);
+        raw = rs >= n;  // stored raw: the slot still holds the chunk as loaded
+        if (!raw) size = rs;
+        if (F.bit8 && rs != es && threadIdx.x == 0)  // the two size computations must agree
+          atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CORRUPT);
+      }
     } else {
       uint8_t *cur_b = S, *nxt_b = A;
       for (uint32_t st = 0; st + 1 < P.n_stages; st++) {
@@ -909,17 +1079,7 @@ __global__ void __launch_bounds__(FW, kFastCtasPerSm) kvc_lossless_enc_fast(cons
       } else {
         from_payload = P.n_stages > 1;  // the stages wrote over the slot
       }
-      if (threadIdx.x == 0) {
-        publish_size(P, t, align16u(size));
-        s_t = s_ticket[jn] = atomicAdd(ticket_ctr, 1u);
-        mbar_arrive(&s_tick[jn]);
-        if (k + 1 >= kRing && !mbar_wait(&s_empty[s1], ((k + 1) / kRing - 1) & 1u))
-          atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_TIMEOUT);
-      }
-      bsync<FT>();
-      tn = s_t;
-      if (tn < nc) issue_chunk_load(P, tn, ring + s1 * slot_bytes);
-      cp_async_commit();
+      if (threadIdx.x == 0) publish_size(P, t, align16u(size));
     }
     const uint32_t asz = align16u(size);
     if (!raw && threadIdx.x < asz - size) S[size + threadIdx.x] = 0;
@@ -931,9 +1091,7 @@ __global__ void __launch_bounds__(FW, kFastCtasPerSm) kvc_lossless_enc_fast(cons
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     bsync<FT>();
     if (threadIdx.x == 0) mbar_arrive(&s_full[s]);
-    t = tn;
   }
-  cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------------------
