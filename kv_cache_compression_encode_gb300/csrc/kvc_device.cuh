@@ -47,6 +47,33 @@ __device__ __forceinline__ uint4 pack8(const float *x, bool bf16) {
 
 // Byte offset of token t's row inside one layer's buffer, or ~0 for a block-table
 // entry outside [0, num_pages) (the caller treats the row as absent and flags it).
+// 32 bytes to global memory in one access when `p` is 32-byte aligned (the
+// 256-bit vector store of sm_100 and later), else as two 16-byte stores.
+__device__ __forceinline__ void st_global32(void *p, const uint32_t (&u)[8]) {
+  if ((reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(u[0]), "r"(u[1]), "r"(u[2]),
+                 "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7])
+                 : "memory");
+  } else {
+    uint4 *q = reinterpret_cast<uint4 *>(p);
+    q[0] = make_uint4(u[0], u[1], u[2], u[3]);
+    q[1] = make_uint4(u[4], u[5], u[6], u[7]);
+  }
+}
+
+// 32 read-only bytes from global memory, one 256-bit access when `p` is 32-byte
+// aligned, else two 16-byte loads.
+__device__ __forceinline__ void ld_global32_nc(const void *p, uint4 &a, uint4 &b) {
+  if ((reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
+    asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(p));
+  } else {
+    a = __ldg(reinterpret_cast<const uint4 *>(p));
+    b = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
+  }
+}
+
 __device__ __forceinline__ uint64_t row_offset(const KvGeom &g, uint32_t t) {
   if (g.block_table) {
     uint32_t page = (uint32_t)__ldg(g.block_table + (t >> g.page_shift));

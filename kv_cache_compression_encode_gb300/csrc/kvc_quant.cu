@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_rows(const QuantParams P)
           const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(P.layers[l]) + ro +
                                                              (size_t)(h * kHeadDim + 64 * half) * 2);
 #pragma unroll
-          for (int j = 0; j < 8; j++) q[j] = __ldg(src + j);
+          for (int j = 0; j < 4; j++) ld_global32_nc(src + 2 * j, q[2 * j], q[2 * j + 1]);
         }
       }
 #pragma unroll
@@ -381,14 +381,13 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_dec_rows(const QuantParams P)
       if (ro == ~0ull) {
         flags |= KVC_FLAG_BAD_PAGE;
       } else {
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.layers[l]) + ro +
-                                               (size_t)(h * kHeadDim + 64 * half) * 2);
+        uint8_t *dst = static_cast<uint8_t *>(P.layers[l]) + ro + (size_t)(h * kHeadDim + 64 * half) * 2;
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-          uint32_t u[4];
+        for (int k = 0; k < 4; k++) {
+          uint32_t u[8];
 #pragma unroll
-          for (int e = 0; e < 4; e++) {
-            const float2 x = w[4 * k + e];
+          for (int e = 0; e < 8; e++) {
+            const float2 x = w[8 * k + e];
             if (BF16) {
               const __nv_bfloat162 b2 = __floats2bfloat162_rn(x.x, x.y);
               u[e] = *reinterpret_cast<const uint32_t *>(&b2);
@@ -397,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_dec_rows(const QuantParams P)
               u[e] = *reinterpret_cast<const uint32_t *>(&h2);
             }
           }
-          dst[k] = make_uint4(u[0], u[1], u[2], u[3]);
+          st_global32(dst + 32 * k, u);
         }
       }
     }
@@ -1292,13 +1291,13 @@ __global__ void __launch_bounds__(kKD, 3) kvc_dec_ktile(const QuantParams P) {
       if (ro == ~0ull) {
         flags |= KVC_FLAG_BAD_PAGE;
       } else {
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.layers[l]) + ro + (size_t)h * kHeadDim * 2);
+        uint8_t *dst = static_cast<uint8_t *>(P.layers[l]) + ro + (size_t)h * kHeadDim * 2;
 #pragma unroll
-        for (int k = 0; k < 16; k++) {
-          uint32_t u[4];
+        for (int k = 0; k < 8; k++) {
+          uint32_t u[8];
 #pragma unroll
-          for (int i = 0; i < 4; i++) {
-            const float2 x = v[4 * k + i];
+          for (int i = 0; i < 8; i++) {
+            const float2 x = v[8 * k + i];
             if (BF16) {
               const __nv_bfloat162 b2 = __floats2bfloat162_rn(x.x, x.y);
               u[i] = *reinterpret_cast<const uint32_t *>(&b2);
@@ -1307,7 +1306,7 @@ __global__ void __launch_bounds__(kKD, 3) kvc_dec_ktile(const QuantParams P) {
               u[i] = *reinterpret_cast<const uint32_t *>(&h2);
             }
           }
-          dst[k] = make_uint4(u[0], u[1], u[2], u[3]);
+          st_global32(dst + 32 * k, u);
         }
       }
     }
