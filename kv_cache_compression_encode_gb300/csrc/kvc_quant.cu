@@ -1102,17 +1102,31 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P, con
 constexpr int kKD = 128;
 
 
+// Byte offset `o` of channel c's code slot, rotated so that the 8 lanes of a
+// 16-byte shared access phase hit 8 distinct bank groups: 16-byte unit u of the
+// slot is stored at unit u ^ kdec_rot<BITS>(c) (BITS = 3: slots of 3 units, not
+// rotated).
+template <int BITS>
+__device__ __forceinline__ uint32_t kdec_rot(int c) {
+  if constexpr (BITS == 2) return ((uint32_t)c >> 2) & 1u;
+  else if constexpr (BITS == 4) return ((uint32_t)c >> 1) & 3u;
+  else if constexpr (BITS == 8) return (uint32_t)c & 7u;
+  else return 0u;
+}
+
 // The D-phase inputs of a tile for channel c, copied by thread c into its own
 // slots of the shared buffers (so only thread c reads them, after its own
 // cp.async wait): its codes over the tile's 128 rows (16*BITS bytes: a segment of
-// each of the tile's 128 / G token-group records) at cbuf + 16*BITS*c, and the
-// group metadata words at mbuf[128 gi + c].  Groups past the end are zero.
+// each of the tile's 128 / G token-group records) at cbuf + 16*BITS*c, 16-byte
+// units rotated by kdec_rot, and the group metadata words at mbuf[128 gi + c].
+// Groups past the end are zero.
 template <int BITS>
 __device__ __forceinline__ void kdec_issue(const QuantParams &P, uint32_t sb, uint32_t lh, int c, uint8_t *cbuf,
                                            uint32_t *mbuf) {
   const uint32_t G = P.group, ng = 128 / G, rec = G * BITS / 8;
   const size_t g0 = ((size_t)lh * P.n_tg + sb * ng) * kHeadDim + c;  // record of the tile's first group
   uint8_t *dst = cbuf + 16 * BITS * c;
+  const uint32_t rot = kdec_rot<BITS>(c) << 4;
   for (uint32_t gi = 0; gi < ng; gi++) {
     const size_t g = g0 + (size_t)gi * kHeadDim;
     if (sb * ng + gi < P.n_tg) {
@@ -1120,16 +1134,16 @@ __device__ __forceinline__ void kdec_issue(const QuantParams &P, uint32_t sb, ui
       asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(m), "l"(P.meta + g * 4) : "memory");
       const uint8_t *src = P.codes + g * rec;
       if ((rec & 15) == 0) {
-        for (uint32_t o = 0; o < rec; o += 16) cp_async16_q(dst + gi * rec + o, src + o);
+        for (uint32_t o = 0; o < rec; o += 16) cp_async16_q(dst + ((gi * rec + o) ^ rot), src + o);
       } else {
         for (uint32_t o = 0; o < rec; o += 4) {
-          const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst + gi * rec + o);
+          const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst + ((gi * rec + o) ^ rot));
           asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src + o) : "memory");
         }
       }
     } else {
       mbuf[128 * gi + c] = 0u;
-      for (uint32_t o = 0; o < rec; o += 4) *reinterpret_cast<uint32_t *>(dst + gi * rec + o) = 0u;
+      for (uint32_t o = 0; o < rec; o += 4) *reinterpret_cast<uint32_t *>(dst + ((gi * rec + o) ^ rot)) = 0u;
     }
   }
   cp_async_commit_q();
@@ -1154,9 +1168,10 @@ __device__ __forceinline__ void kdec_columns(const QuantParams &P, float *Y, flo
 #pragma unroll
     for (int k = 0; k < 12; k++) cw[k] = cs[k];
   } else {
+    const uint32_t rot = kdec_rot<BITS>(tid);
 #pragma unroll
     for (int k = 0; k < BITS; k++) {
-      const uint4 a = reinterpret_cast<const uint4 *>(cs)[k];
+      const uint4 a = reinterpret_cast<const uint4 *>(cs)[k ^ rot];
       cw[4 * k] = a.x; cw[4 * k + 1] = a.y; cw[4 * k + 2] = a.z; cw[4 * k + 3] = a.w;
     }
   }
