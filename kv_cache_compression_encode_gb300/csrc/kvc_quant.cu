@@ -167,16 +167,30 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_rows(const QuantParams P)
   const float sg = half ? -1.0f : 1.0f;  // stride 64: lower lane a + b, upper lane a - b = -b + a
   uint32_t flags = 0;
 
-  for (uint32_t it = blockIdx.x * (kThreads / 32) + warp; it < n_it; it += gridDim.x * (kThreads / 32)) {
+  // row R = (l * T + t) * H + h, advanced by a fixed number of rows without divisions
+  const uint32_t it0 = blockIdx.x * (kThreads / 32) + warp, it_step = gridDim.x * (kThreads / 32);
+  const uint32_t R0 = it0 * 16 + rsub, dR = it_step * 16;
+  uint32_t rh = R0 % H, rt = (R0 / H) % T, rl = R0 / H / T;
+  const uint32_t dh = dR % H, dt = (dR / H) % T, dl = dR / H / T;
+  for (uint32_t it = it0; it < n_it; it += it_step) {
     const uint32_t R = it * 16 + rsub;
     const bool valid = R < NR;
+    const uint32_t h = rh, t = rt, l = rl;
+    {  // the next row of this lane
+      rh += dh;
+      uint32_t c = rh >= H;
+      rh -= c ? H : 0u;
+      rt += dt + c;
+      c = rt >= T;
+      rt -= c ? T : 0u;
+      rl += dl + c;
+    }
     float2 w[32];
     {
       uint4 q[8];
 #pragma unroll
       for (int j = 0; j < 8; j++) q[j] = make_uint4(0u, 0u, 0u, 0u);
       if (valid) {
-        const uint32_t h = R % H, lt = R / H, t = lt % T, l = lt / T;
         const uint64_t ro = row_offset(P.g, t);
         if (ro == ~0ull) {
           flags |= KVC_FLAG_BAD_PAGE;
@@ -310,9 +324,24 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_dec_rows(const QuantParams P)
   const float sg = half ? -1.0f : 1.0f;  // stride 64: lower lane a + b, upper lane a - b = -b + a
   uint32_t flags = 0;
 
-  for (uint32_t it = blockIdx.x * (kThreads / 32) + warp; it < n_it; it += gridDim.x * (kThreads / 32)) {
+  // row R = (l * T + t) * H + h, advanced by a fixed number of rows without divisions
+  const uint32_t it0 = blockIdx.x * (kThreads / 32) + warp, it_step = gridDim.x * (kThreads / 32);
+  const uint32_t R0 = it0 * 16 + rsub, dR = it_step * 16;
+  uint32_t rh = R0 % H, rt = (R0 / H) % T, rl = R0 / H / T;
+  const uint32_t dh = dR % H, dt = (dR / H) % T, dl = dR / H / T;
+  for (uint32_t it = it0; it < n_it; it += it_step) {
     const uint32_t R = it * 16 + rsub;
     const bool valid = R < NR;
+    const uint32_t h = rh, t = rt, l = rl;
+    {  // the next row of this lane
+      rh += dh;
+      uint32_t c = rh >= H;
+      rh -= c ? H : 0u;
+      rt += dt + c;
+      c = rt >= T;
+      rt -= c ? T : 0u;
+      rl += dl + c;
+    }
     float2 w[32];  // channels 64 half + 2i, +1
     {
       uint32_t cw[2 * BITS];
@@ -376,7 +405,6 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_dec_rows(const QuantParams P)
       }
     }
     if (valid) {
-      const uint32_t h = R % H, lt = R / H, t = lt % T, l = lt / T;
       const uint64_t ro = row_offset(P.g, t);
       if (ro == ~0ull) {
         flags |= KVC_FLAG_BAD_PAGE;
