@@ -676,7 +676,7 @@ __global__ void __launch_bounds__(kThreads) kvc_enc_tile(const QuantParams P) {
 // ---------------------------------------------------------------------------
 // key tile, groups over tokens (the key default): kvc_enc_ktile
 //
-// Per (layer, head, 128-token) tile, 512 threads, five barriers (three without smoothing):
+// Per (layer, head, 128-token) tile, 512 threads, four barriers (three without smoothing):
 //  A  (smoothing only) warp w takes channel octet w over all 128 rows of the
 //     stage (lane l: rows l + 32i).  The per-channel minima and maxima run on
 //     the packed 16-bit pairs and are reduced across the warp by a halving
@@ -703,7 +703,7 @@ __global__ void __launch_bounds__(kThreads) kvc_enc_tile(const QuantParams P) {
 constexpr int kKT = 512;
 constexpr int kTabStride = 36;  // floats per 32-channel part in the parameter tables (spreads the parts over banks)
 // 1 KiB slack for aligning the stage to the swizzle's 1 KiB period
-constexpr size_t kKtileSmem = 1024 + 128 * 256 + (size_t)128 * 128 * 4 + 2 * 4 * kTabStride * 4;
+constexpr size_t kKtileSmem = 1024 + 128 * 256 + (size_t)128 * 128 * 4 + 2 * 4 * kTabStride * 4 + 256 * 4;
 
 __device__ __forceinline__ uint32_t stage_off(uint32_t k, uint32_t r) {
   return (k >> 3) * 16384u + 128u * r + 16u * ((k & 7u) ^ (r & 7u));
@@ -850,6 +850,7 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P, con
   float *Y = reinterpret_cast<float *>(stage + 128 * 256);             // [128][128] fp32, swizzled
   float *tab_mu = Y + 128 * 128;                                       // [4 parts][kTabStride]
   float *tab_inv = tab_mu + 4 * kTabStride;
+  float *st = tab_inv + 4 * kTabStride;  // A: channel c minimum at st[c], maximum at st[128 + c]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t H = P.g.H, T = P.g.T, n_sb = P.n_sb, G = P.group;
   const uint32_t n_tiles = P.g.L * H * n_sb;
@@ -893,7 +894,12 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P, con
     nxt.advance(step_sb, step_h, step_l, n_sb, H);
     if (!tma) cp_async_wait_all_q();
     else if (!ktile_wait(&stage_bar, it & 1u)) flags |= KVC_FLAG_TIMEOUT;
-    __syncthreads();  // the stage holds this tile; every thread is done with the previous Y
+    // the stage holds this tile.  With smoothing and TMA a warp that is done with
+    // the previous tile's D goes straight on to A (which reads only the stage and
+    // writes only st); the barrier after A then also ends every read of the
+    // previous Y.  Otherwise a barrier here (cp.async data is visible to the
+    // other threads only after it, and C writes Y).
+    if (!tma || !smooth) __syncthreads();
 
     // ---- A: smoothing parameters.  Minima and maxima run on the packed 16-bit
     // pairs (exact); lanes 8j..8j+7 end with pair j (channels 2j, 2j+1 of the octet).
@@ -929,7 +935,6 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P, con
         mn[0] = pmin2_n<BF16>(mn[0], __shfl_xor_sync(kFull, mn[0], o));
         mx[0] = pmax2_n<BF16>(mx[0], __shfl_xor_sync(kFull, mx[0], o));
       }
-      float *st = Y;  // the statistics of channel c at st[c] (minimum) and st[128 + c] (maximum)
       if ((lane & 3) == 0) {
         const int hi = (lane >> 2) & 1;  // lane 8j: channel 2j, lane 8j + 4: channel 2j + 1
         const int ch = 8 * warp + 2 * (lane >> 3) + hi;
