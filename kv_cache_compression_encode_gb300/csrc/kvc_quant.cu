@@ -676,7 +676,7 @@ __global__ void __launch_bounds__(kThreads) kvc_enc_tile(const QuantParams P) {
 // ---------------------------------------------------------------------------
 // key tile, groups over tokens (the key default): kvc_enc_ktile
 //
-// Per (layer, head, 128-token) tile, 512 threads, four barriers (three without smoothing):
+// Per (layer, head, 128-token) tile, 512 threads, three barriers (four with smoothing and cp.async loads):
 //  A  (smoothing only) warp w takes channel octet w over all 128 rows of the
 //     stage (lane l: rows l + 32i).  The per-channel minima and maxima run on
 //     the packed 16-bit pairs and are reduced across the warp by a halving
@@ -960,7 +960,8 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P, con
         reinterpret_cast<uint16_t *>(P.mu)[cell] = (uint16_t)mub;
         P.ex[cell] = (int8_t)e;
       }
-      __syncthreads();
+      // no barrier here: C reads only the stage until its own barrier, which also
+      // publishes the parameter table before the smoothing uses it
     }
 
     // ---- C: row pass
