@@ -1341,12 +1341,16 @@ __global__ void __launch_bounds__(kKD, 3) kvc_dec_ktile(const QuantParams P) {
         flags |= KVC_FLAG_BAD_PAGE;
       } else {
         uint8_t *dst = static_cast<uint8_t *>(P.layers[l]) + ro + (size_t)h * kHeadDim * 2;
+        // the 256-byte row goes out by one bulk copy from this thread's own Y row,
+        // which it has read already; starting it 16 (r % 16) bytes into that row
+        // spreads the 8 rows of a 16-byte store phase over 8 bank groups
+        uint4 *srow = reinterpret_cast<uint4 *>(Y + r * 128) + (r & 15);
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-          uint32_t u[8];
+        for (int k = 0; k < 16; k++) {
+          uint32_t u[4];
 #pragma unroll
-          for (int i = 0; i < 8; i++) {
-            const float2 x = v[8 * k + i];
+          for (int i = 0; i < 4; i++) {
+            const float2 x = v[4 * k + i];
             if (BF16) {
               const __nv_bfloat162 b2 = __floats2bfloat162_rn(x.x, x.y);
               u[i] = *reinterpret_cast<const uint32_t *>(&b2);
@@ -1355,15 +1359,22 @@ __global__ void __launch_bounds__(kKD, 3) kvc_dec_ktile(const QuantParams P) {
               u[i] = *reinterpret_cast<const uint32_t *>(&h2);
             }
           }
-          st_global32(dst + 32 * k, u);
+          srow[k] = make_uint4(u[0], u[1], u[2], u[3]);
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the stores above before the async read
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], 256;" ::"l"(dst),
+                     "r"(smem_u32(srow))
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
     }
-
+    // the next tile's D writes Y: every row copy must have read its bytes
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     __syncthreads();
     cur = nxt;
   }
   cp_async_wait_all_q();
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   if (flags) atomicOr(P.status, flags);
 }
 
