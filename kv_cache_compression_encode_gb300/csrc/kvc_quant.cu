@@ -41,6 +41,8 @@ __device__ __forceinline__ uint32_t pair_sign_mask(uint32_t sbits, int j) {
   return (((sbits >> j) & 1u) << 15) | (((sbits >> (j + 1)) & 1u) << 31);
 }
 
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
 __device__ __forceinline__ float2 unpack_pair(uint32_t u, bool bf16) {
   if (bf16) return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
   return __half22float2(*reinterpret_cast<const __half2 *>(&u));
@@ -306,12 +308,19 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_rows(const QuantParams P)
 // ---------------------------------------------------------------------------
 // rows: decode
 // ---------------------------------------------------------------------------
+constexpr size_t kDecRowsSmem = (size_t)(kThreads / 32) * 16 * 512;  // the row slots of kvc_dec_rows
+
 template <int BITS, bool HAD, bool BF16>
 __global__ void __launch_bounds__(kThreads, 2) kvc_dec_rows(const QuantParams P) {
   if (P.check_corrupt && (*(volatile uint32_t *)P.status & KVC_FLAG_CORRUPT)) return;
   __shared__ __align__(16) uint32_t fsign[2][64];  // bit 31 set where channel 64 half + c has Hadamard sign -1
+  extern __shared__ uint4 rows_out[];  // per warp 16 row slots of 512 B
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int half = lane & 1, rsub = lane >> 1;
+  const int half = lane >> 4, rsub = lane & 15;  // lane: channels 64 half .. 64 half + 63 of row rsub
+  // row rsub is assembled 16 (rsub % 8) bytes into its slot (the 8 rows of a
+  // 16-byte store phase then sit in 8 distinct bank groups) and leaves by one
+  // 256-byte bulk copy
+  uint4 *const oslot = rows_out + (warp * 16 + rsub) * 32 + (rsub & 7) + 8 * half;
   const uint32_t H = P.g.H, T = P.g.T;
   const uint32_t NR = P.g.L * T * H;
   const uint32_t n_it = (NR + 15) / 16;
@@ -391,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_dec_rows(const QuantParams P)
       const float2 c2 = bcast2(hadamard_scale()), sg2 = bcast2(sg);
 #pragma unroll
       for (int i = 0; i < 32; i++) {
-        const float2 o = make_float2(__shfl_xor_sync(kFull, w[i].x, 1), __shfl_xor_sync(kFull, w[i].y, 1));
+        const float2 o = make_float2(__shfl_xor_sync(kFull, w[i].x, 16), __shfl_xor_sync(kFull, w[i].y, 16));
         w[i] = mul2(__ffma2_rn(w[i], sg2, o), c2);
       }
       const uint4 *fs = reinterpret_cast<const uint4 *>(fsign[half]);
@@ -404,31 +413,47 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_dec_rows(const QuantParams P)
         w[2 * k + 1].y = __uint_as_float(__float_as_uint(w[2 * k + 1].y) ^ m.w);
       }
     }
+    bool put = false;
+    uint8_t *dst = nullptr;
     if (valid) {
       const uint64_t ro = row_offset(P.g, t);
       if (ro == ~0ull) {
         flags |= KVC_FLAG_BAD_PAGE;
       } else {
-        uint8_t *dst = static_cast<uint8_t *>(P.layers[l]) + ro + (size_t)(h * kHeadDim + 64 * half) * 2;
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          uint32_t u[8];
-#pragma unroll
-          for (int e = 0; e < 8; e++) {
-            const float2 x = w[8 * k + e];
-            if (BF16) {
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(x.x, x.y);
-              u[e] = *reinterpret_cast<const uint32_t *>(&b2);
-            } else {
-              const __half2 h2 = __floats2half2_rn(x.x, x.y);
-              u[e] = *reinterpret_cast<const uint32_t *>(&h2);
-            }
-          }
-          st_global32(dst + 32 * k, u);
-        }
+        put = true;
+        dst = static_cast<uint8_t *>(P.layers[l]) + ro + (size_t)h * kHeadDim * 2;
       }
     }
+    // the previous row copy from this slot has read it
+    if (half == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncwarp();
+    if (put) {
+#pragma unroll
+      for (int k = 0; k < 8; k++) {
+        uint32_t u[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const float2 x = w[4 * k + e];
+          if (BF16) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(x.x, x.y);
+            u[e] = *reinterpret_cast<const uint32_t *>(&b2);
+          } else {
+            const __half2 h2 = __floats2half2_rn(x.x, x.y);
+            u[e] = *reinterpret_cast<const uint32_t *>(&h2);
+          }
+        }
+        oslot[k] = make_uint4(u[0], u[1], u[2], u[3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the stores above before the async read
+    }
+    __syncwarp();
+    if (put && half == 0) {
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], 256;" ::"l"(dst), "r"(smem_u32(oslot))
+                   : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
   }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   if (flags) atomicOr(P.status, flags);
 }
 
@@ -719,7 +744,6 @@ __device__ __forceinline__ void cp_async16_q(void *smem, const void *gmem) {
 __device__ __forceinline__ void cp_async_commit_q() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all_q() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 // The tile's two boxes by TMA (one thread): the mbarrier expects their 32 KiB.
 __device__ __forceinline__ void ktile_tma(const CUtensorMap *map, uint32_t h, uint32_t t0, uint8_t *stage,
                                           uint64_t *bar) {
@@ -1511,7 +1535,7 @@ template <typename K>
 static int run(K kernel, bool tile, const QuantParams &p, int sm_count, void *stream, uint64_t work_units,
                size_t smem_override = 0, int threads = kThreads) {
   const size_t smem = smem_override ? smem_override : (tile ? kTileSmem : 0);
-  if (tile) {
+  if (smem > 0) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
   }
@@ -1581,10 +1605,10 @@ static int dispatch(const QuantParams &p, const TmaMaps *maps, bool had, bool en
   }
   *name = "kvc_dec_rows";
   if (p.g.bf16)
-    return had ? run(kvc_dec_rows<BITS, true, true>, false, p, sm, st, units)
-               : run(kvc_dec_rows<BITS, false, true>, false, p, sm, st, units);
-  return had ? run(kvc_dec_rows<BITS, true, false>, false, p, sm, st, units)
-             : run(kvc_dec_rows<BITS, false, false>, false, p, sm, st, units);
+    return had ? run(kvc_dec_rows<BITS, true, true>, false, p, sm, st, units, kDecRowsSmem)
+               : run(kvc_dec_rows<BITS, false, true>, false, p, sm, st, units, kDecRowsSmem);
+  return had ? run(kvc_dec_rows<BITS, true, false>, false, p, sm, st, units, kDecRowsSmem)
+             : run(kvc_dec_rows<BITS, false, false>, false, p, sm, st, units, kDecRowsSmem);
 }
 
 static int dispatch_bits(const QuantParams &p, const TmaMaps *maps, bool enc, int sm, void *st, uint64_t *launches,
