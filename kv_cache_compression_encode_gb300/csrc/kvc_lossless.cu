@@ -1144,22 +1144,42 @@ __device__ bool fast_decode_chunk(const uint8_t *in, uint32_t size, uint32_t n, 
   uint32_t x[16];
 #pragma unroll
   for (int i = 0; i < 16; i++) x[i] = 0u;
-  if (active) {
-    const uint8_t *E = in + nb2 + totB;
+  if (active && (blo | bhi)) {
+    // this thread's nonzero elements are contiguous from byte nb2 + totB + W e of
+    // the chunk: they are taken from a bit window refilled with aligned 32-bit
+    // words (the reads stay inside the chunk buffer, which has 64 spare bytes)
+    const uint32_t *Wd = reinterpret_cast<const uint32_t *>(in);
+    const uint32_t a0 = nb2 + totB + W * e;
+    uint32_t wi = a0 >> 2;
+    uint64_t win = Wd[wi++] >> (8 * (a0 & 3u));
+    uint32_t have = 32 - 8 * (a0 & 3u);
 #pragma unroll
     for (int i = 0; i < 16; i++) {
       if (W == 2) {
 #pragma unroll
         for (int hh = 0; hh < 2; hh++)
           if ((blo >> (2 * i + hh)) & 1u) {
-            x[i] |= ((uint32_t)E[2 * e] | ((uint32_t)E[2 * e + 1] << 8)) << (16 * hh);
-            e++;
+            if (have < 16) {
+              win |= (uint64_t)Wd[wi++] << have;
+              have += 32;
+            }
+            x[i] |= ((uint32_t)win & 0xffffu) << (16 * hh);
+            win >>= 16;
+            have -= 16;
           }
       } else {
         const uint32_t bits = i < 8 ? (blo >> (4 * i)) : (bhi >> (4 * (i - 8)));
 #pragma unroll
         for (int b = 0; b < 4; b++)
-          if ((bits >> b) & 1u) x[i] |= (uint32_t)E[e++] << (8 * b);
+          if ((bits >> b) & 1u) {
+            if (have < 8) {
+              win |= (uint64_t)Wd[wi++] << have;
+              have += 32;
+            }
+            x[i] |= ((uint32_t)win & 0xffu) << (8 * b);
+            win >>= 8;
+            have -= 8;
+          }
       }
     }
   }
