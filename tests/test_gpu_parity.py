@@ -260,6 +260,39 @@ def test_bad_block_table_entry_is_flagged():
     assert st == kvc.KVC_ERR_INVALID_ARG and flags & kvc.FLAG_BAD_PAGE
 
 
+@pytest.mark.parametrize("had", [False, True])
+def test_bad_block_table_entry_on_decode(had):
+    """Decoding through a block table with one out-of-range entry flags BAD_PAGE,
+    writes every row of the valid pages exactly as a clean decode does, and
+    leaves the page the bad entry replaced untouched (both decoders: keys in
+    128-token tiles, values row by row)."""
+    prof = dict(hadamard=had, bits_k=4, bits_v=4, group_k=128, group_v=128, stages=LC, chunk_bytes=4096)
+    case = U.Case(L=2, T=256, H=2, profile=prof, page_size=16, seed=11).materialize()
+    codec = Codec(kvc.make_profile(**prof), case.kvc_shape())
+    sg = codec.encode(case.k, case.v, case.block_table)
+    st, nbytes, flags = codec.query()
+    assert st == kvc.KVC_OK and flags == 0
+    rk, rv = case.empty_like_kv()
+    codec.decode(sg, nbytes, rk, rv, case.block_table)
+    st, _, flags = codec.query()
+    assert st == kvc.KVC_OK and flags == 0
+    bad_entry = 3
+    bt = case.block_table.clone()
+    lost = int(bt[bad_entry])
+    bt[bad_entry] = 1 << 20
+    ok, ov = case.empty_like_kv()
+    codec.decode(sg, nbytes, ok, ov, bt)
+    st, _, flags = codec.query()
+    assert st == kvc.KVC_ERR_INVALID_ARG and flags & kvc.FLAG_BAD_PAGE
+    canary = case.empty_like_kv()[0][0][lost]
+    for got, ref in zip(ok + ov, rk + rv):
+        for pg in range(case.n_pages):
+            if pg == lost:
+                assert torch.equal(got[pg], canary), "a row landed in the page of the bad entry"
+            else:
+                assert torch.equal(got[pg], ref[pg]), f"page {pg} differs from the clean decode"
+
+
 def test_repeatable_and_independent_streams():
     prof = dict(bits_k=4, bits_v=4, group_k=128, group_v=128, hadamard=True, stages=FULL, chunk_bytes=2048)
     case = U.Case(L=2, T=512, H=4, profile=prof, seed=9).materialize()
