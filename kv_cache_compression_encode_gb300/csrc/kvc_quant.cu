@@ -11,13 +11,17 @@
 //
 // Two kernel shapes:
 //  * rows  -- groups over channels, no smoothing (the value default).  A warp owns
-//    8 rows (token, head) at a time, 4 lanes per row, 32 channels per lane; the
-//    Hadamard butterflies run in registers (strides 1..16) and across the 4 lanes
-//    (strides 32, 64).  No shared memory.
-//  * tile  -- groups over tokens and/or smoothing (the key default).  A CTA owns a
-//    (layer, head, 128-token) tile in shared memory: per-channel statistics over
-//    tokens, the row-wise Hadamard pass, then a column pass that quantizes and
-//    packs each channel's token group.
+//    16 rows (token, head) at a time, 2 lanes per row, 64 channels per lane; the
+//    Hadamard butterflies run in registers (strides 1..32) and across the lane
+//    pair (stride 64).  The decoder assembles its output rows in shared memory
+//    and writes each with one bulk copy.
+//  * key tile -- groups over tokens (the key default, kvc_enc_ktile /
+//    kvc_dec_ktile).  A CTA owns a (layer, head, 128-token) tile in shared memory:
+//    per-channel smoothing statistics over tokens, the row-wise Hadamard pass,
+//    then a column pass that quantizes and packs each channel's token group (and
+//    the reverse for decoding).
+//  * tile  -- smoothing with groups over channels (kvc_enc_tile / kvc_dec_tile),
+//    the general layout for the less common profiles.
 #include <cuda_runtime.h>
 
 #include "kvc_device.cuh"
