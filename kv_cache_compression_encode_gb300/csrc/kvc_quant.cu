@@ -895,6 +895,7 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P, con
   const float *Yd0 = Y + 32 * dq * 128 + 4 * (int)ycol4(dc >> 2, 32 * dq) + (dc & 3);      // even rows
   const float *Yd1 = Y + 32 * dq * 128 + 4 * (int)ycol4(dc >> 2, 32 * dq + 1) + (dc & 3);  // odd rows
   const int tiles_groups = 128 / (int)G;
+  const uint32_t dq_group = (uint32_t)((32 * dq) / (int)G);  // D: this quarter's group within the tile
   const uint32_t rec_bytes = G * BITS / 8, seg_off = (uint32_t)((32 * dq) % (int)G) * BITS / 8;
   const bool d_first = ((32 * dq) % (int)G) == 0;          // D: the quarter that starts its group writes the metadata
   // the persistent grid advances by gridDim.x tiles
@@ -1089,7 +1090,7 @@ __global__ void __launch_bounds__(kKT, 2) kvc_enc_ktile(const QuantParams P, con
         mn = fmin_n(mn, __shfl_xor_sync(kFull, mn, o));
         mx = fmax_n(mx, __shfl_xor_sync(kFull, mx, o));
       }
-      const uint32_t tg = sb * tiles_groups + (32 * dq) / (int)G;
+      const uint32_t tg = sb * tiles_groups + dq_group;
       const bool active = tg < P.n_tg;  // a quarter past the end of an existing group still writes its (zero) codes
       float sc = 0.0f, z = 0.0f, rr = 0.0f;
       uint32_t meta = 0, fl = 0;
@@ -1185,7 +1186,7 @@ __device__ __forceinline__ uint32_t kdec_rot(int c) {
 template <int BITS>
 __device__ __forceinline__ void kdec_issue(const QuantParams &P, uint32_t sb, uint32_t lh, int c, uint8_t *cbuf,
                                            uint32_t *mbuf) {
-  const uint32_t G = P.group, ng = 128 / G, rec = G * BITS / 8;
+  const uint32_t G = P.group, ng = 128u >> (31 - __clz(G)), rec = G * BITS / 8;  // G is 32, 64 or 128
   const size_t g0 = ((size_t)lh * P.n_tg + sb * ng) * kHeadDim + c;  // record of the tile's first group
   uint8_t *dst = cbuf + 16 * BITS * c;
   const uint32_t rot = kdec_rot<BITS>(c) << 4;
@@ -1237,7 +1238,7 @@ __device__ __forceinline__ void kdec_columns(const QuantParams &P, float *Y, flo
       cw[4 * k] = a.x; cw[4 * k + 1] = a.y; cw[4 * k + 2] = a.z; cw[4 * k + 3] = a.w;
     }
   }
-  const uint32_t ng = 128 / G;
+  const uint32_t gsh = 31 - __clz(G), ng = 128u >> gsh;  // G is 32, 64 or 128
   uint32_t meta[4];
 #pragma unroll
   for (uint32_t gi = 0; gi < 4; gi++) meta[gi] = gi < ng ? mbuf[128 * gi + tid] : 0u;
@@ -1248,7 +1249,7 @@ __device__ __forceinline__ void kdec_columns(const QuantParams &P, float *Y, flo
 #pragma unroll
     for (int k = 0; k < BITS; k++) w[k] = cw[seg * BITS + k];
     codes_to_f2<BITS>(w, qf);
-    const uint32_t gi = (uint32_t)(32 * seg) / G;
+    const uint32_t gi = (uint32_t)(32 * seg) >> gsh;
     const uint32_t m = gi == 0 ? meta[0] : gi == 1 ? meta[1] : gi == 2 ? meta[2] : meta[3];
     const float2 s2 = bcast2(__half2float(__ushort_as_half((unsigned short)(m & 0xffffu))));
     const float2 z2 = bcast2(__half2float(__ushort_as_half((unsigned short)(m >> 16))));
