@@ -159,6 +159,22 @@ def kernel_bytes(plan, w, name: str, stream_bytes: int) -> int:
     }.get(name, 0)
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """Longest timed region over the ranks: the job is done when its slowest rank is."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(raw_bytes: int, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job GB/s: the input bytes of every rank's steps over the slowest rank's time."""
+    return raw_bytes * world * steps / (max_ms * 1e-3) / 1e9
+
+
 def run_kvc(args):
     import torch
     import torch.distributed as dist
@@ -236,17 +252,14 @@ def run_kvc(args):
     launches = codec.plan.launches - launches0
     recs = kvc.kvc_timing_read(codec.plan, args.steps * 8 + 64)
     kvc.kvc_timing_enable(codec.plan, False)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, device)
     st, _, flags = codec.query()
     if st != kvc.KVC_OK:
         raise RuntimeError(f"timed steps reported {kvc.status_str(st)} flags={flags}")
 
     if rank == 0:
         ms_step = total_ms / args.steps
-        value = raw * world * args.steps / (total_ms * 1e-3) / 1e9
+        value = job_throughput(raw, world, args.steps, total_ms)
         # per-kernel live timings
         per = {}
         for name, ms in recs:
