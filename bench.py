@@ -175,6 +175,16 @@ def job_throughput(raw_bytes: int, world: int, steps: int, max_ms: float) -> flo
     return raw_bytes * world * steps / (max_ms * 1e-3) / 1e9
 
 
+def benefit_report(enc_gbs: float, dec_gbs: float, cr: float) -> dict:
+    """s_p and the break-even link bandwidth B*_p of the measured profile (KVServe
+    §3.1 and §6.1 Eq. (5)): compressing pays off on links slower than B*_p."""
+    from kv_cache_compression_encode_gb300.benefit import break_even_bandwidth, effective_throughput
+
+    s_p = effective_throughput(enc_gbs, dec_gbs)
+    return {"s_p_gbs": round(s_p, 2), "break_even_gbs": round(break_even_bandwidth(cr, s_p), 2),
+            "compression_ratio": round(cr, 4)}
+
+
 def run_kvc(args):
     import torch
     import torch.distributed as dist
@@ -291,6 +301,7 @@ def run_kvc(args):
                        "step": "kvc_encode + kvc_decode", "l2": "inputs larger than L2 (no flush needed)",
                        "parallelism": f"replicas x{world}"},
             "encode_gbs": round(raw / (enc_ms * 1e-3) / 1e9, 2), "decode_gbs": round(raw / (dec_ms * 1e-3) / 1e9, 2),
+            "benefit": benefit_report(raw / (enc_ms * 1e-3) / 1e9, raw / (dec_ms * 1e-3) / 1e9, raw / nbytes),
             "roofline": {"bound": "hbm", "kernel": top, "achieved": round(achieved, 1), "peak": peak,
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                          else "fallback", "unit": "GB/s", "frac": round(achieved / peak, 4),
