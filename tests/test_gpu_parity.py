@@ -293,6 +293,59 @@ def test_bad_block_table_entry_on_decode(had):
                 assert torch.equal(got[pg], ref[pg]), f"page {pg} differs from the clean decode"
 
 
+def test_strided_layers_writes_stay_in_their_rows():
+    """Strided token rows (256 padding bytes after each token) inside one buffer
+    with guard bytes between the layers: encode reads only the rows, decode writes
+    only the rows (both decoders' row copies), and the rows match a decode into a
+    dense layout."""
+    prof = dict(hadamard=True, bits_k=4, bits_v=4, group_k=64, group_v=128, stages=FULL, chunk_bytes=4096)
+    from kv_cache_compression_encode_gb300 import synth
+    L, T, H, D = 2, 300, 3, 128
+    row, ts, guard = H * D * 2, H * D * 2 + 256, 4096
+    span = T * ts
+
+    def carve(fill):
+        buf = torch.full((guard + L * (span + guard),), fill, dtype=torch.uint8, device="cuda")
+        views = [buf[guard + l * (span + guard): guard + l * (span + guard) + span] for l in range(L)]
+        return buf, views
+
+    kbuf, kin = carve(0x7E)
+    vbuf, vin = carve(0x7E)
+    dense_k, dense_v = [], []
+    for l in range(L):
+        k, v = synth.layer_kv("llama", l, T, H, D, "bf16", 31, "cuda")
+        dense_k.append(k.contiguous()); dense_v.append(v.contiguous())
+        for dst, src in ((kin[l], k), (vin[l], v)):
+            dst.view(T, ts)[:, :row].copy_(src.contiguous().view(torch.uint8).view(T, row))
+    strided = kvc.make_shape(L, T, H, D, kvc.BF16, token_stride=ts)
+    codec = Codec(kvc.make_profile(**prof), strided)
+    sg = codec.encode(kin, vin)
+    st, nbytes, flags = codec.query()
+    assert st == kvc.KVC_OK and flags == 0
+    # the same stream from the dense layout
+    dcodec = Codec(kvc.make_profile(**prof), kvc.make_shape(L, T, H, D, kvc.BF16))
+    sd = dcodec.encode(dense_k, dense_v)
+    _, nd, _ = dcodec.query()
+    assert nd == nbytes and torch.equal(sg[:nbytes], sd[:nd])
+    # decode into strided rows surrounded by canary bytes
+    okbuf, kout = carve(0x5A)
+    ovbuf, vout = carve(0x5A)
+    codec.decode(sg, nbytes, kout, vout)
+    st, _, flags = codec.query()
+    assert st == kvc.KVC_OK and flags == 0
+    rk = [torch.empty_like(x) for x in dense_k]
+    rv = [torch.empty_like(x) for x in dense_v]
+    dcodec.decode(sd, nd, rk, rv)
+    assert dcodec.query()[0] == kvc.KVC_OK
+    for buf, outs, refs in ((okbuf, kout, rk), (ovbuf, vout, rv)):
+        mask = torch.ones_like(buf, dtype=torch.bool)  # True: bytes nothing may write
+        for l in range(L):
+            base = guard + l * (span + guard)
+            mask[base: base + span].view(T, ts)[:, :row] = False
+            assert torch.equal(outs[l].view(T, ts)[:, :row], refs[l].view(torch.uint8).view(T, row)), f"layer {l}"
+        assert bool((buf[mask] == 0x5A).all()), "a decoder wrote outside the token rows"
+
+
 def test_repeatable_and_independent_streams():
     prof = dict(bits_k=4, bits_v=4, group_k=128, group_v=128, hadamard=True, stages=FULL, chunk_bytes=2048)
     case = U.Case(L=2, T=512, H=4, profile=prof, seed=9).materialize()
