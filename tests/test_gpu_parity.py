@@ -346,6 +346,31 @@ def test_strided_layers_writes_stay_in_their_rows():
         assert bool((buf[mask] == 0x5A).all()), "a decoder wrote outside the token rows"
 
 
+@pytest.mark.parametrize("stages", [FULL, LC, ((1, 2), (3, 4), (4, 1))])
+def test_step_outputs_stay_inside_their_sizes(stages):
+    """Each step writes exactly its output's bytes: the payload's payload_bytes
+    (quantize, lossless decode) and the stream's reported size (lossless encode);
+    the bytes after them (canary) are untouched."""
+    prof = dict(hadamard=True, bits_k=4, bits_v=4, group_k=128, group_v=128, stages=stages, chunk_bytes=4096)
+    case = U.Case(L=2, T=300, H=3, profile=prof, seed=41).materialize()
+    codec = Codec(kvc.make_profile(**prof), case.kvc_shape())
+    n, cap, guard = codec.plan.payload_bytes, codec.plan.max_stream_bytes, 4096
+    payload = torch.full((n + guard,), 0xA5, dtype=torch.uint8, device="cuda")
+    codec.quantize(case.k, case.v, out=payload)
+    assert codec.query()[0] == kvc.KVC_OK
+    assert bool((payload[n:] == 0xA5).all()), "quantize wrote past the payload"
+    stream = torch.full((cap + guard,), 0xA5, dtype=torch.uint8, device="cuda")
+    codec.lossless_encode(payload, out=stream)
+    st, nbytes, _ = codec.query()
+    assert st == kvc.KVC_OK and nbytes <= cap
+    assert bool((stream[nbytes:] == 0xA5).all()), "the encoder wrote past the stream's size"
+    back = torch.full((n + guard,), 0xA5, dtype=torch.uint8, device="cuda")
+    codec.lossless_decode(stream, nbytes, out=back)
+    assert codec.query()[0] == kvc.KVC_OK
+    assert torch.equal(back[:n], payload[:n])
+    assert bool((back[n:] == 0xA5).all()), "the decoder wrote past the payload"
+
+
 def test_repeatable_and_independent_streams():
     prof = dict(bits_k=4, bits_v=4, group_k=128, group_v=128, hadamard=True, stages=FULL, chunk_bytes=2048)
     case = U.Case(L=2, T=512, H=4, profile=prof, seed=9).materialize()
