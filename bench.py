@@ -317,9 +317,9 @@ def run_kvc(args):
 def run_e2e(codec, k, v, ok, ov, w, args, device):
     """Same metric through the public API with host buffers: every step copies the
     KV from pinned host memory, encodes, reads the size and the stream back, then
-    copies the stream in, decodes and copies the KV out.  Two requests are in
+    copies the stream in, decodes and copies the KV out.  Three requests are in
     flight, each on its own CUDA stream with its own plan, workspace and buffers
-    (a serving process overlaps one request's uploads with another's downloads);
+    (a serving process overlaps one request's uploads with others' downloads);
     every step still moves all of its own bytes."""
     import torch
 
@@ -340,7 +340,8 @@ def run_e2e(codec, k, v, ok, ov, w, args, device):
             self.sbuf = c.new_stream_buffer()
             self.rbuf = c.new_stream_buffer()
 
-    lanes = [Lane(codec), Lane(Codec(codec.profile, codec.shape, device))]
+    n_lanes = 3
+    lanes = [Lane(codec)] + [Lane(Codec(codec.profile, codec.shape, device)) for _ in range(n_lanes - 1)]
     counts = {"h2d": 0, "d2h": 0}
 
     def front(L):  # inputs up, encode
@@ -360,12 +361,13 @@ def run_e2e(codec, k, v, ok, ov, w, args, device):
         counts["h2d"] = w.raw_bytes + n
         counts["d2h"] = n + w.raw_bytes + 16
 
-    def run(n):
-        front(lanes[0])
+    def run(n):  # request i: front when i - (n_lanes - 1) has been taken back, then back in order
+        for j in range(min(n_lanes - 1, n)):
+            front(lanes[j])
         for i in range(n):
-            if i + 1 < n:
-                front(lanes[(i + 1) % 2])
-            back(lanes[i % 2])
+            if i + n_lanes - 1 < n:
+                front(lanes[(i + n_lanes - 1) % n_lanes])
+            back(lanes[i % n_lanes])
         for L in lanes:
             L.s.synchronize()
 
@@ -378,7 +380,7 @@ def run_e2e(codec, k, v, ok, ov, w, args, device):
     ok_rt = all(torch.equal(a, b.to(a.device)) for L in lanes for a, b in zip(ok + ov, L.rk + L.rv))
     return {"value": round(w.raw_bytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": counts["h2d"],
             "d2h_bytes_per_step": counts["d2h"], "ms_per_step": round(dt * 1e3, 3), "steps": n_steps,
-            "requests_in_flight": 2, "roundtrip_matches_device_path": bool(ok_rt)}
+            "requests_in_flight": n_lanes, "roundtrip_matches_device_path": bool(ok_rt)}
 
 
 # ---------------------------------------------------------------------------- oracle
