@@ -550,7 +550,10 @@ static kvc_status lossless_decode_impl(kvc_plan_s *P, const void *d_stream, size
   lp.stream = static_cast<uint8_t *>(const_cast<void *>(d_stream));
   lp.stream_cap = stream_bytes;
   lp.out_payload = Q;
-  {
+  lp.fused_offsets = lossless_decode_fusable(lp, P->sm_count) ? 1u : 0u;
+  if (lp.fused_offsets) {  // the decoder checks the stream itself: only the status word is reset first
+    if (cudaMemsetAsync(lp.ctrl + kCtrlFlags, 0, sizeof(uint32_t), st) != cudaSuccess) return KVC_ERR_CUDA;
+  } else {
     Bracket br(P, st);
     const int rc = launch_decode_prepare(lp, st);
     br.done("kvc_decode_prepare");

@@ -96,7 +96,7 @@ struct LosslessParams {
   uint8_t *out_payload;    // decode output
   int64_t skip_ticket;     // test hook: this ticket does not publish
   uint32_t poll_limit;
-  uint32_t pad_;
+  uint32_t fused_offsets;  // decode: the decoder checks the table and computes the chunk offsets itself
   uint8_t header[KVC_HEADER_BYTES];  // decode: expected header
 };
 
@@ -108,5 +108,8 @@ int launch_prologue(const PrologueParams &p, void *stream);
 int launch_lossless_encode(const LosslessParams &p, int sm_count, void *stream);
 int launch_decode_prepare(const LosslessParams &p, void *stream);
 int launch_lossless_decode(const LosslessParams &p, int sm_count, void *stream);
+// Whether launch_lossless_decode can take the prepare step into the decoder for
+// this table size (nothing else needs to run first except the status reset).
+bool lossless_decode_fusable(const LosslessParams &p, int sm_count);
 
 }  // namespace kvc

@@ -1345,24 +1345,95 @@ __global__ void __launch_bounds__(PT) kvc_decode_prepare(const LosslessParams P)
 }
 
 // ---------------------------------------------------------------------------
+// Decode, step 1 inside the decoder (tables of up to kFusedMaxChunks chunks):
+// every CTA checks the header and the whole table exactly as kvc_decode_prepare
+// does and takes the offsets of its own chunks (c = blockIdx.x + k gridDim.x) from
+// one block scan; all CTAs reach the same verdict, CTA 0 reports a corrupt stream.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kFusedMaxChunks = 32 * LT;  // 32 table words per thread
+constexpr uint32_t kFusedMaxOwn = 64;           // chunks per CTA
+
+__device__ bool decode_offsets(const LosslessParams &P, unsigned long long *tmp, unsigned long long *s_off,
+                               int *s_bad) {
+  const uint32_t tid = threadIdx.x, nc = P.n_chunks;
+  const uint32_t *table = reinterpret_cast<const uint32_t *>(P.stream + KVC_HEADER_BYTES);
+  if (tid == 0) *s_bad = 0;
+  __syncthreads();
+  if (tid < KVC_HEADER_BYTES / 4 &&
+      reinterpret_cast<const uint32_t *>(P.stream)[tid] != reinterpret_cast<const uint32_t *>(P.header)[tid])
+    atomicOr(s_bad, 1);
+  // thread tid takes entries [S tid, S tid + S), S a multiple of 4 (16-byte reads;
+  // the table is 16-byte aligned and padded to data_start)
+  const uint32_t S = ((nc + LT - 1) / LT + 3) & ~3u;
+  const uint32_t i0 = min(nc, tid * S), i1 = min(nc, i0 + S);
+  unsigned long long sum = 0;
+  int bad = 0;
+  for (uint32_t i = i0; i < i1; i += 4) {
+    const uint4 q = *reinterpret_cast<const uint4 *>(table + i);
+    const uint32_t e4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (uint32_t k = 0; k < 4; k++) {
+      if (i + k < i1) {
+        const uint32_t e = e4[k], sz = e & 0x7fffffffu;
+        const uint64_t off = (uint64_t)(i + k) * P.chunk_bytes;
+        const uint32_t n = (uint32_t)min((uint64_t)P.chunk_bytes, P.payload_bytes - off);
+        if (e >> 31) bad |= sz != n;  // a stored chunk holds exactly its length, a compressed one less
+        else bad |= sz >= n;
+        sum += align16u(sz);
+      }
+    }
+  }
+  if (bad) atomicOr(s_bad, 1);
+  unsigned long long total;
+  unsigned long long run = P.data_start + block_excl_scan<unsigned long long>(sum, tmp, total);
+  if (tid == 0 && P.data_start + total > P.stream_cap) atomicOr(s_bad, 1);
+  // this CTA's chunks in the thread's range: the first at or after i0, then every gridDim.x
+  const uint32_t b = blockIdx.x, grid = gridDim.x;
+  uint32_t own = i0 <= b ? b : b + (i0 - b + grid - 1) / grid * grid;
+  for (uint32_t i = i0; i < i1; i += 4) {
+    const uint4 q = *reinterpret_cast<const uint4 *>(table + i);
+    const uint32_t e4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (uint32_t k = 0; k < 4; k++) {
+      if (i + k < i1) {
+        if (i + k == own) {
+          s_off[(own - b) / grid] = run;
+          own += grid;
+        }
+        run += align16u(e4[k] & 0x7fffffffu);
+      }
+    }
+  }
+  __syncthreads();
+  if (*s_bad) {
+    if (b == 0 && tid == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CORRUPT);
+    return false;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
 // Decode, step 2: one chunk per CTA iteration back into the payload.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(LT, 3) kvc_lossless_dec(const LosslessParams P, const FastSpec F) {
-  if (*(volatile uint32_t *)(P.ctrl + kCtrlFlags) & KVC_FLAG_CORRUPT) return;
+  if (!P.fused_offsets && (*(volatile uint32_t *)(P.ctrl + kCtrlFlags) & KVC_FLAG_CORRUPT)) return;
   extern __shared__ uint4 smem_u4[];
+  __shared__ unsigned long long s_off[kFusedMaxOwn];
+  __shared__ int s_bad;
   uint8_t *bufA = reinterpret_cast<uint8_t *>(smem_u4);
   uint8_t *bufB = bufA + P.chunk_bytes + 64;
   uint8_t *Bs = bufB + P.chunk_bytes + 64;
   uint32_t *tmp = reinterpret_cast<uint32_t *>(Bs + 8192);
+  if (P.fused_offsets && !decode_offsets(P, reinterpret_cast<unsigned long long *>(tmp), s_off, &s_bad)) return;
   const uint32_t *table = reinterpret_cast<const uint32_t *>(P.stream + KVC_HEADER_BYTES);
   const uint32_t last = P.n_stages - 1;
   const bool has_rze = P.kind[last] == KVC_ST_RZE;
 
-  for (uint32_t c = blockIdx.x; c < P.n_chunks; c += gridDim.x) {
+  for (uint32_t c = blockIdx.x, kc = 0; c < P.n_chunks; c += gridDim.x, kc++) {
     const uint32_t e = table[c], size = e & 0x7fffffffu;
     const uint64_t off = (uint64_t)c * P.chunk_bytes;
     const uint32_t n = (uint32_t)min((uint64_t)P.chunk_bytes, P.payload_bytes - off);
-    const uint4 *src = reinterpret_cast<const uint4 *>(P.stream + P.state[c]);
+    const uint4 *src = reinterpret_cast<const uint4 *>(P.stream + (P.fused_offsets ? s_off[kc] : P.state[c]));
     uint4 *dst = reinterpret_cast<uint4 *>(P.out_payload + off);
     if (e >> 31) {
       for (uint32_t i = threadIdx.x; i < n / 16; i += LT) dst[i] = __ldg(src + i);
@@ -1471,16 +1542,28 @@ int launch_decode_prepare(const LosslessParams &p, void *stream) {
   return (int)cudaGetLastError();
 }
 
-int launch_lossless_decode(const LosslessParams &p, int sm_count, void *stream) {
-  if (p.n_chunks == 0 || p.n_stages == 0) return 0;
+static uint64_t decode_blocks(const LosslessParams &p, int sm_count) {
   const size_t smem = lossless_smem(p.chunk_bytes);
-  cudaError_t e = cudaFuncSetAttribute(kvc_lossless_dec, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return (int)e;
+  if (cudaFuncSetAttribute(kvc_lossless_dec, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 0;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kvc_lossless_dec, LT, smem) != cudaSuccess || per_sm < 1)
     per_sm = 1;
   uint64_t blocks = (uint64_t)sm_count * per_sm;
-  if (blocks > p.n_chunks) blocks = p.n_chunks;
+  return blocks > p.n_chunks ? p.n_chunks : blocks;
+}
+
+bool lossless_decode_fusable(const LosslessParams &p, int sm_count) {
+  if (p.n_stages == 0 || p.n_chunks == 0 || p.n_chunks > kFusedMaxChunks || p.stream_cap < p.data_start) return false;
+  const uint64_t blocks = decode_blocks(p, sm_count);
+  return blocks > 0 && (p.n_chunks + blocks - 1) / blocks <= kFusedMaxOwn;
+}
+
+int launch_lossless_decode(const LosslessParams &p, int sm_count, void *stream) {
+  if (p.n_chunks == 0 || p.n_stages == 0) return 0;
+  const size_t smem = lossless_smem(p.chunk_bytes);
+  const uint64_t blocks = decode_blocks(p, sm_count);
+  if (blocks == 0) return (int)cudaErrorInvalidValue;
   FastSpec f;
   if (!fast_spec(p, f)) f = FastSpec{0, 0, 0, 0};  // rze_w == 0: generic stages for every chunk
   kvc_lossless_dec<<<(unsigned)blocks, LT, smem, (cudaStream_t)stream>>>(p, f);
