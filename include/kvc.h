@@ -137,7 +137,9 @@ void kvc_plan_destroy(kvc_plan_t *plan);
  * (status word, stream size, chunk ticket), per-chunk look-back / offset words and,
  * when lossless stages are on, the quantized payload. */
 size_t kvc_workspace_bytes(const kvc_plan_t *plan);
-/* Worst-case stream size (header + chunk table + every chunk stored raw). */
+/* Worst-case stream size (header + chunk table + every chunk stored raw): the
+ * capacity of the caller's preallocated output buffer ("Beyond Compression
+ * Ratio" §4.1, all-layer output buffer; §4.2, device bitstream). */
 size_t kvc_max_stream_bytes(const kvc_plan_t *plan);
 /* Bytes of the quantized payload Q (all sections, each 16-byte aligned). */
 size_t kvc_payload_bytes(const kvc_plan_t *plan);
@@ -147,17 +149,26 @@ kvc_status kvc_section(const kvc_plan_t *plan, int index, uint64_t *offset, uint
 /* Number of lossless chunks (0 without stages). */
 uint64_t kvc_num_chunks(const kvc_plan_t *plan);
 
-/* Full encode: quantize all layers into the payload, then header + lossless
- * stream into d_stream (capacity stream_cap >= kvc_max_stream_bytes).  The stream
- * size is written to the device word *d_stream_bytes (may be NULL) and to the
- * workspace control block; kvc_query() returns it to the host.  No host sync. */
+/* Full encode ("KVServe" §5.1: BS = C(Q(T(X))); "Beyond Compression Ratio" §4.1
+ * fused transform + quantization into the all-layer buffer, §4.2 device-pointer
+ * encoding API): quantize all layers into the payload, then header + lossless
+ * stream into d_stream (capacity stream_cap >= kvc_max_stream_bytes).  Inputs:
+ * in->k_layers / v_layers as described by the plan's shape (device, read only).
+ * d_workspace: kvc_workspace_bytes(plan) bytes of caller-owned device memory
+ * (16-byte aligned), reused across calls.  The stream size is written to the
+ * device word *d_stream_bytes (may be NULL) and to the workspace control block;
+ * kvc_query() returns it to the host.  No host sync.  Returns INVALID_ARG for
+ * null or misaligned pointers, CAPACITY for a short stream or workspace. */
 kvc_status kvc_encode(kvc_plan_t *plan, const kvc_kv *in, void *d_stream, size_t stream_cap,
                       void *d_workspace, size_t workspace_bytes, uint64_t *d_stream_bytes,
                       kvc_stream_t stream);
 
-/* Full decode of a stream of stream_bytes bytes into the layers of *out (same
- * geometry as the plan).  The header is checked against the plan on the device;
- * a corrupt stream sets KVC_FLAG_CORRUPT and leaves *out untouched. */
+/* Full decode ("Beyond Compression Ratio" §4.2 device-pointer decoding API, §4.1
+ * fused reconstruction: dequantize, inverse Hadamard, normalization, sign
+ * restoration) of a stream of stream_bytes bytes (device) into the layers of
+ * *out (device, same geometry as the plan; written, never read).  The header and
+ * chunk table are checked against the plan on the device; a corrupt stream sets
+ * KVC_FLAG_CORRUPT and leaves *out untouched.  No host sync. */
 kvc_status kvc_decode(kvc_plan_t *plan, const void *d_stream, size_t stream_bytes, const kvc_kv *out,
                       void *d_workspace, size_t workspace_bytes, kvc_stream_t stream);
 
@@ -179,7 +190,9 @@ kvc_status kvc_lossless_decode(kvc_plan_t *plan, const void *d_stream, size_t st
 kvc_status kvc_dequantize(kvc_plan_t *plan, const void *d_payload, const kvc_kv *out, void *d_workspace,
                           size_t workspace_bytes, kvc_stream_t stream);
 
-/* Synchronize `stream`, then read the workspace control block: the stream size of
+/* The compressed-size scalar returned to the host ("Beyond Compression Ratio"
+ * §4.2: only the size crosses to the host, the stream stays on the device).
+ * Synchronize `stream`, then read the workspace control block: the stream size of
  * the last encode (host_stream_bytes, may be NULL) and the status bits
  * (host_flags, may be NULL).  Returns the most severe error the bits encode
  * (CORRUPT > CAPACITY > TIMEOUT > INVALID_ARG (bad page) > NONFINITE > RANGE) or KVC_OK. */
@@ -203,7 +216,9 @@ const char *kvc_status_str(kvc_status status);
  * (device u32, may be NULL) receives the status bits (KVC_FLAG_*); kvc_query does
  * not apply.  Allocates nothing (no cudaMalloc / cudaFree).  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) and caches
- * it; make that first call before any stream capture.  All calls share the one
+ * it for that device's current context; make that first call before any stream
+ * capture.  After the device is reset (cudaDeviceReset) the next call looks the
+ * address up again in the new context (so, again, before any capture).  All calls share the one
  * array (its words are reset at the start of every call), so calls whose GPU work
  * overlaps -- on different streams or from different threads -- race; serialize them. */
 #define KVC_NOALLOC_SCRATCH_BYTES (1u << 20)

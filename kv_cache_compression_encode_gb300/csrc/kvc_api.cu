@@ -650,24 +650,68 @@ extern "C" const char *kvc_status_str(kvc_status s) {
 // word per chunk) lives in this file-scope device array instead of a caller
 // workspace.  Every GPU that loads the library holds the array until the process
 // exits.  In host code `g_noalloc_scratch` only names a host-side stand-in, so
-// its device address is looked up once per device with cudaGetSymbolAddress.
+// its device address is looked up with cudaGetSymbolAddress once per device
+// context: the cache is keyed to the context's unique id (cuCtxGetId), so after a
+// cudaDeviceReset (which destroys the primary context; the runtime makes a new
+// one with a new id on the next call) the address is looked up again instead of
+// pointing into the destroyed context.
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) uint8_t g_noalloc_scratch[KVC_NOALLOC_SCRATCH_BYTES];
 
+typedef CUresult (*PfnCtxGetCurrent)(CUcontext *);
+typedef CUresult (*PfnCtxGetId)(CUcontext, unsigned long long *);
+
 static std::mutex g_noalloc_mutex;
-static void *g_noalloc_addr[256];  // device address of the array, per device ordinal
+struct NoallocSlot {
+  unsigned long long ctx_id;  // id of the context the address belongs to (0 = none yet)
+  void *addr;
+};
+static NoallocSlot g_noalloc_slot[256];  // per device ordinal
+
+// Unique id of the calling thread's current context (0 when there is none or the
+// driver entry points are missing).
+static unsigned long long current_ctx_id() {
+  static std::once_flag once;
+  static PfnCtxGetCurrent get_current = nullptr;
+  static PfnCtxGetId get_id = nullptr;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PfnCtxGetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PfnCtxGetId>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 static kvc_status noalloc_scratch(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVC_ERR_CUDA;
   if (dev < 0 || dev >= 256) return KVC_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_addr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return KVC_ERR_CUDA;
-    g_noalloc_addr[dev] = p;
+  NoallocSlot &slot = g_noalloc_slot[dev];
+  unsigned long long id = current_ctx_id();
+  if (slot.addr && id != 0 && slot.ctx_id == id) {
+    *out = slot.addr;
+    return KVC_OK;
   }
-  *out = g_noalloc_addr[dev];
+  // first call in this context: the lookup also makes the runtime set up the
+  // device's primary context if it has none yet
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return KVC_ERR_CUDA;
+  if (id == 0) id = current_ctx_id();
+  slot.ctx_id = id;    // 0 (no id available): looked up again on every call
+  slot.addr = id ? p : nullptr;
+  *out = p;
   return KVC_OK;
 }
 

@@ -56,6 +56,56 @@ def test_noalloc_matches_workspace_encode_twice():
         assert torch.equal(back[:n], Q), call
 
 
+def test_noalloc_without_stages_and_without_status_word():
+    """No lossless stages: the stream is the header plus the payload, its size set
+    by the prologue; d_status may be NULL."""
+    prof = kvc.make_profile(bits_k=4, bits_v=4, group_k=64, group_v=64, stages=())
+    codec = Codec(prof, kvc.make_shape(2, 300, 4, 128, kvc.BF16))
+    plan = codec.plan
+    n = plan.payload_bytes
+    Q = torch.from_numpy(_payload(n, 21)).cuda()
+    ref = codec.lossless_encode(Q)
+    st, ref_bytes, flags = codec.query()
+    assert st == kvc.KVC_OK and flags == 0 and ref_bytes == 64 + n
+    out = torch.full((plan.max_stream_bytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    d_size = torch.zeros(1, dtype=torch.int64, device="cuda")
+    kvc.kvc_lossless_encode_noalloc(plan, Q.data_ptr(), out.data_ptr(), out.numel(), d_size.data_ptr(), 0,
+                                    torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert int(d_size.item()) == ref_bytes
+    assert torch.equal(out[:ref_bytes], ref[:ref_bytes])
+
+
+def test_noalloc_reports_a_device_timeout_then_recovers():
+    """A device-side error reaches d_status through the shared array: the test hook
+    makes one chunk skip its publication, so its successor's bounded wait runs out
+    (TIMEOUT).  The next call resets the array's words and is clean again."""
+    prof = kvc.make_profile(bits_k=4, bits_v=4, group_k=64, group_v=64, stages=((1, 8), (2, 8), (4, 2)),
+                            chunk_bytes=4096)
+    codec = Codec(prof, kvc.make_shape(1, 512, 2, 128, kvc.BF16))
+    plan = codec.plan
+    n = plan.payload_bytes
+    Q = torch.from_numpy(_payload(n, 31)).cuda()
+    out = torch.empty(plan.max_stream_bytes, dtype=torch.uint8, device="cuda")
+    d_size = torch.zeros(1, dtype=torch.int64, device="cuda")
+    d_status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    kvc.kvc_debug_lookback(plan, 3, 2000)
+    kvc.kvc_lossless_encode_noalloc(plan, Q.data_ptr(), out.data_ptr(), out.numel(), d_size.data_ptr(),
+                                    d_status.data_ptr(), stream)
+    torch.cuda.synchronize()
+    assert int(d_status.item()) & kvc.FLAG_TIMEOUT
+    kvc.kvc_debug_lookback(plan, -1, 0)
+    ref = codec.lossless_encode(Q)
+    st, ref_bytes, flags = codec.query()
+    assert st == kvc.KVC_OK and flags == 0
+    kvc.kvc_lossless_encode_noalloc(plan, Q.data_ptr(), out.data_ptr(), out.numel(), d_size.data_ptr(),
+                                    d_status.data_ptr(), stream)
+    torch.cuda.synchronize()
+    assert int(d_status.item()) == 0
+    assert int(d_size.item()) == ref_bytes and torch.equal(out[:ref_bytes], ref[:ref_bytes])
+
+
 def test_noalloc_rejects_plans_beyond_the_array():
     # 256 + 8 * chunks > 1 MiB: more than 131040 chunks of 256 bytes
     prof = kvc.make_profile(bits_k=8, bits_v=8, group_k=32, group_v=32, stages=((1, 8), (4, 1)), chunk_bytes=256)
