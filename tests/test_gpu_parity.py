@@ -192,12 +192,16 @@ def test_nonfinite_and_range_flags_match_oracle():
             assert np.array_equal(U.to_np(sg, nbytes), so)
 
 
-@pytest.mark.parametrize("chunk", [1024, 4096])
+@pytest.mark.parametrize("chunk", [1024, 4096, 256])
 def test_corrupt_streams_are_rejected_and_outputs_untouched(chunk):
     """1 KiB chunks decode through the generic stage functions, 4 KiB chunks through
-    the fast chunk decoder; both must reject the same corruptions."""
+    the fast chunk decoder; both must reject the same corruptions.  With 256-byte
+    chunks the table has more than 16384 entries, so the stream and table checks
+    run in the separate prepare launch instead of inside the decoder."""
     prof = dict(bits_k=4, bits_v=4, group_k=64, group_v=64, hadamard=True, stages=LC, chunk_bytes=chunk)
-    case = U.Case(L=1, T=300, H=2, dtype="bf16", dist="llama_sink", profile=prof, seed=4).materialize()
+    big = chunk == 256
+    case = U.Case(L=2 if big else 1, T=2048 if big else 300, H=8 if big else 2, dtype="bf16", dist="llama_sink",
+                  profile=prof, seed=4).materialize()
     codec, sg, nbytes, sg_np, so, _, _ = U.encode_both(case)
     lay = O.layout(U.oracle_profile(prof), case.oracle_shape())
     table = so[64:64 + 4 * lay.n_chunks].view(np.uint32)
@@ -222,8 +226,12 @@ def test_corrupt_streams_are_rejected_and_outputs_untouched(chunk):
                       [np.zeros_like(a) for a in case.host_bits(case.v)])
         dev = torch.from_numpy(np.concatenate([s, np.zeros(64, np.uint8)])).cuda()
         ok, ov = case.empty_like_kv(fill=0x1234)
+        kvc.kvc_timing_enable(codec.plan, True)
         codec.decode(dev, s.size, ok, ov)
         st, _, fg = codec.query()
+        names = [n for n, _ in kvc.kvc_timing_read(codec.plan)]
+        kvc.kvc_timing_enable(codec.plan, False)
+        assert ("kvc_decode_prepare" in names) == big, (name, names)
         assert fo & O.FLAG_CORRUPT, name
         assert st == kvc.KVC_ERR_CORRUPT and (fg & kvc.FLAG_CORRUPT), name
         for t in ok + ov:  # nothing written
