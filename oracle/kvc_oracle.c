@@ -28,7 +28,12 @@
  * The pages describe the steps in prose only.  Every choice they leave open is
  * fixed here as "format v1" (the stream layout, rounding of every fp32 step, the
  * smoothing statistic, the sign generator, the packing order and the byte formats
- * of the lossless stages); each such choice is marked READING below.
+ * of the lossless stages); each such choice is marked READING below.  Format v2
+ * adds two optional profile features (a stream that uses neither is a v1 stream,
+ * byte for byte): per-(layer, head) code widths ([KVServe] §5.1 layer- and
+ * head-wise mixed precision; [FastKVComp] §4.1 head-importance-aware mixed
+ * precision) and the token-delta transformer ([KVServe] §5.1 "Delta", after
+ * CacheGen).
  *
  * Arithmetic: IEEE binary32, round-to-nearest-even, one rounding per written
  * operation (build with -ffp-contract=off, no fast-math).  fmaf() is the fused
@@ -82,15 +87,33 @@ typedef struct {
     uint32_t stage_kind[4], stage_param[4];
     uint32_t chunk_bytes;
     uint64_t seed;
+    uint32_t token_delta;        /* v2: anchor-token delta on K and V (see quantize_tensor) */
+    uint32_t pad_;
+    const uint8_t *bits_map_k;   /* v2: [layers][kv_heads] code widths of K, or NULL = bits_k everywhere */
+    const uint8_t *bits_map_v;   /* v2: the same for V, or NULL = bits_v everywhere */
 } kvo_profile;
 
 typedef struct {
-    uint64_t off[6], size[6]; /* S1 K codes, S2 K meta, S3 V codes, S4 V meta, S5 K centres, S6 K exponents */
+    uint64_t off[8], size[8]; /* S1 K codes, S2 K meta, S3 V codes, S4 V meta, S5 K centres, S6 K exponents,
+                                 S7 K anchors, S8 V anchors */
     uint64_t payload_bytes;   /* Q: all sections, each 16-byte aligned */
     uint64_t n_chunks;
     uint64_t data_start;      /* first chunk byte in the stream (stages present) */
     uint64_t max_stream_bytes;
+    uint64_t header_bytes;    /* 64, or 64 + the width map (v2) */
 } kvo_layout;
+
+#define KVO_DELTA_BLOCK 128u      /* READING: one anchor token per 128-token block */
+
+/* Code width of (layer l, head h) of a tensor (0 = K, 1 = V). */
+static uint32_t width_of(const kvo_profile *p, int tensor, uint32_t H, uint32_t l, uint32_t h)
+{
+    const uint8_t *m = tensor ? p->bits_map_v : p->bits_map_k;
+    if (m) return m[(uint64_t)l * H + h];
+    return tensor ? p->bits_v : p->bits_k;
+}
+
+static int has_maps(const kvo_profile *p) { return p->bits_map_k != NULL || p->bits_map_v != NULL; }
 
 static uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
 static uint64_t align16(uint64_t a) { return (a + 15) & ~(uint64_t)15; }
@@ -369,10 +392,11 @@ void kvo_unpack(const uint8_t *in, uint32_t n, uint32_t bits, uint8_t *codes)
 /* Payload layout (READING; "preallocated all-layer output buffer",           */
 /* [FastKVComp] §4.1).  Sections in order, each starting 16-byte aligned:     */
 /*  S1 K codes, S2 K meta {scale, zero}, S3 V codes, S4 V meta,               */
-/*  S5 K smoothing centres (binary16), S6 K smoothing exponents (int8).       */
+/*  S5 K smoothing centres (binary16), S6 K smoothing exponents (int8),       */
+/*  S7 K anchors, S8 V anchors (v2 token delta: element bits, 2 bytes).       */
 /* Groups over tokens: records ordered [layer][head][token group][channel];   */
 /* groups over channels: [layer][token][head][channel group].                 */
-/* Smoothing planes: [layer][head][128-token block][channel].                 */
+/* Smoothing and anchor planes: [layer][head][128-token block][channel].      */
 /* ------------------------------------------------------------------------ */
 static uint64_t n_groups(const kvo_shape *sh, uint32_t axis, uint32_t G)
 {
@@ -381,33 +405,98 @@ static uint64_t n_groups(const kvo_shape *sh, uint32_t axis, uint32_t G)
     return L * T * H * (D / G);
 }
 
+/* Code bytes of one (layer, head) of a tensor: T rows of D codes of its width
+ * (groups over tokens: ceil(T/G) groups of G codes per channel). */
+static uint64_t lh_code_bytes(const kvo_shape *sh, uint32_t axis, uint32_t G, uint32_t bits)
+{
+    uint64_t T = sh->tokens, D = sh->head_dim;
+    if (axis == KVO_AXIS_OVER_TOKENS) return ceil_div(T, G) * D * G * bits / 8;
+    return T * D * bits / 8;
+}
+
+/* READING (v2 layout with per-(layer, head) widths): groups over tokens keep
+ * records [layer][head][token group][channel], the (layer, head) blocks back to
+ * back, each with its own width; groups over channels keep records
+ * [layer][token][head][channel group], a token's row holding its heads' records
+ * back to back, each head with its own width.  With one width everywhere both
+ * are the v1 layout. */
+static uint64_t code_bytes(const kvo_profile *p, const kvo_shape *sh, int tensor)
+{
+    const uint32_t axis = tensor ? p->axis_v : p->axis_k, G = tensor ? p->group_v : p->group_k;
+    uint64_t n = 0;
+    for (uint32_t l = 0; l < sh->layers; l++)
+        for (uint32_t h = 0; h < sh->kv_heads; h++)
+            n += lh_code_bytes(sh, axis, G, width_of(p, tensor, sh->kv_heads, l, h));
+    return n;
+}
+
+/* Bytes of the v2 width map that follows the 64-byte header: 2 bits per entry
+ * (K entries l*H + h, then V entries), padded to 16 bytes. */
+static uint64_t map_bytes(const kvo_profile *p, const kvo_shape *sh)
+{
+    if (!has_maps(p)) return 0;
+    return align16(ceil_div(2 * (uint64_t)sh->layers * sh->kv_heads * 2, 8));
+}
+
 int kvo_layout_of(const kvo_profile *p, const kvo_shape *sh, kvo_layout *lay)
 {
     memset(lay, 0, sizeof *lay);
     uint64_t gk = n_groups(sh, p->axis_k, p->group_k), gv = n_groups(sh, p->axis_v, p->group_v);
     uint64_t nsb = (uint64_t)sh->layers * sh->kv_heads * ceil_div(sh->tokens, KVO_SMOOTH_BLOCK) * sh->head_dim;
-    lay->size[0] = gk * p->group_k * p->bits_k / 8;
+    uint64_t nab = (uint64_t)sh->layers * sh->kv_heads * ceil_div(sh->tokens, KVO_DELTA_BLOCK) * sh->head_dim;
+    lay->size[0] = code_bytes(p, sh, 0);
     lay->size[1] = gk * 4;
-    lay->size[2] = gv * p->group_v * p->bits_v / 8;
+    lay->size[2] = code_bytes(p, sh, 1);
     lay->size[3] = gv * 4;
     lay->size[4] = p->smooth_keys ? nsb * 2 : 0;
     lay->size[5] = p->smooth_keys ? nsb : 0;
+    lay->size[6] = p->token_delta ? nab * 2 : 0;
+    lay->size[7] = p->token_delta ? nab * 2 : 0;
     uint64_t o = 0;
-    for (int i = 0; i < 6; i++) {
+    for (int i = 0; i < 8; i++) {
         lay->off[i] = o;
         o += align16(lay->size[i]);
     }
     lay->payload_bytes = o;
+    lay->header_bytes = KVO_HEADER_BYTES + map_bytes(p, sh);
     if (p->n_stages == 0) {
         lay->n_chunks = 0;
-        lay->data_start = KVO_HEADER_BYTES;
-        lay->max_stream_bytes = KVO_HEADER_BYTES + o;
+        lay->data_start = lay->header_bytes;
+        lay->max_stream_bytes = lay->header_bytes + o;
     } else {
         lay->n_chunks = ceil_div(o, p->chunk_bytes);
-        lay->data_start = align16(KVO_HEADER_BYTES + 4 * lay->n_chunks);
+        lay->data_start = align16(lay->header_bytes + 4 * lay->n_chunks);
         lay->max_stream_bytes = lay->data_start + o; /* every chunk stored raw */
     }
     return 0;
+}
+
+/* Byte offset of (layer l, head h)'s code block (groups over tokens), or of
+ * (layer l, token 0, head h)'s first record plus the layer's row length in
+ * *row_bytes (groups over channels), inside the tensor's code section. */
+static uint64_t code_base(const kvo_profile *p, const kvo_shape *sh, int tensor, uint32_t l, uint32_t h,
+                          uint64_t *row_bytes)
+{
+    const uint32_t H = sh->kv_heads, D = sh->head_dim;
+    const uint32_t axis = tensor ? p->axis_v : p->axis_k, G = tensor ? p->group_v : p->group_k;
+    uint64_t off = 0;
+    if (axis == KVO_AXIS_OVER_TOKENS) {
+        for (uint32_t l2 = 0; l2 < sh->layers; l2++)
+            for (uint32_t h2 = 0; h2 < H; h2++) {
+                if (l2 == l && h2 == h) return off;
+                off += lh_code_bytes(sh, axis, G, width_of(p, tensor, H, l2, h2));
+            }
+        return off;
+    }
+    for (uint32_t l2 = 0; l2 < l; l2++)
+        for (uint32_t h2 = 0; h2 < H; h2++) off += lh_code_bytes(sh, axis, G, width_of(p, tensor, H, l2, h2));
+    uint64_t row = 0, head = 0;
+    for (uint32_t h2 = 0; h2 < H; h2++) {
+        if (h2 == h) head = row;
+        row += (uint64_t)D * width_of(p, tensor, H, l, h2) / 8;
+    }
+    *row_bytes = row;
+    return off + head;
 }
 
 /* Row address of token t of layer `base` (contiguous or through a block table). */
@@ -438,12 +527,11 @@ static uint32_t quantize_tensor(const kvo_profile *p, const kvo_shape *sh, int t
                                 const kvo_layout *lay, uint8_t *Q)
 {
     const uint32_t L = sh->layers, T = sh->tokens, H = sh->kv_heads, D = sh->head_dim;
-    const uint32_t bits = tensor ? p->bits_v : p->bits_k;
     const uint32_t G = tensor ? p->group_v : p->group_k;
     const uint32_t axis = tensor ? p->axis_v : p->axis_k;
     const int smooth = (tensor == 0) && p->smooth_keys;
-    const uint64_t rec = (uint64_t)G * bits / 8;
     uint8_t *codes_sec = Q + lay->off[tensor ? 2 : 0];
+    uint8_t *anchor_sec = Q + lay->off[tensor ? 7 : 6];
     uint8_t *meta_sec = Q + lay->off[tensor ? 3 : 1];
     uint16_t *mu_sec = (uint16_t *)(Q + lay->off[4]);
     int8_t *e_sec = (int8_t *)(Q + lay->off[5]);
@@ -455,6 +543,10 @@ static uint32_t quantize_tensor(const kvo_profile *p, const kvo_shape *sh, int t
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : flags)
     for (int64_t lh = 0; lh < (int64_t)L * H; lh++) {
         const uint32_t l = (uint32_t)(lh / H), h = (uint32_t)(lh % H);
+        const uint32_t bits = width_of(p, tensor, H, l, h);
+        const uint64_t rec = (uint64_t)G * bits / 8;
+        uint64_t row_bytes = 0;
+        const uint64_t cbase = code_base(p, sh, tensor, l, h, &row_bytes);
         float *X = (float *)malloc((size_t)T * D * sizeof(float));
         float *col = (float *)malloc((size_t)(T > 0 ? T : 1) * sizeof(float));
         uint8_t codes[128 * 8];
@@ -465,6 +557,27 @@ static uint32_t quantize_tensor(const kvo_profile *p, const kvo_shape *sh, int t
                 float x = elem_to_f32(r[d], sh->dtype);
                 if (!isfinite(x)) flags |= KVO_FLAG_NONFINITE;
                 X[t * D + d] = x;
+            }
+        }
+        /* transformer stage 0 (v2, optional): token delta ([KVServe] §5.1 "Delta",
+         * after CacheGen).  READING: the first token of every 128-token block is
+         * the block's anchor; every token of the block (the anchor included, which
+         * becomes 0) is replaced by its fp32 difference from the anchor, channel by
+         * channel; the anchor's element bits are kept in the payload. */
+        if (p->token_delta) {
+            const uint64_t nAB = ceil_div(T, KVO_DELTA_BLOCK);
+            for (uint64_t ab = 0; ab < nAB; ab++) {
+                uint64_t t0 = ab * KVO_DELTA_BLOCK, t1 = t0 + KVO_DELTA_BLOCK;
+                if (t1 > T) t1 = T;
+                const uint16_t *ar = row_ptr(bases[l], sh, block_table, t0) + (uint64_t)h * D;
+                for (uint32_t c = 0; c < D; c++) {
+                    uint64_t cell = (((uint64_t)l * H + h) * nAB + ab) * D + c;
+                    put_u16(anchor_sec + 2 * cell, ar[c]);
+                }
+                float a[1024];
+                for (uint32_t c = 0; c < D; c++) a[c] = X[t0 * D + c];
+                for (uint64_t t = t0; t < t1; t++)
+                    for (uint32_t c = 0; c < D; c++) X[t * D + c] = X[t * D + c] - a[c];
             }
         }
         /* transformer stage 1: per-channel key smoothing */
@@ -509,7 +622,7 @@ static uint32_t quantize_tensor(const kvo_profile *p, const kvo_shape *sh, int t
                     kvo_quantize_group(col, (uint32_t)n, bits, &s, &z, codes, &flags);
                     kvo_pack(codes, G, bits, packed); /* tail codes stay 0 */
                     uint64_t g = (((uint64_t)l * H + h) * nTG + tg) * D + c;
-                    memcpy(codes_sec + g * rec, packed, rec);
+                    memcpy(codes_sec + cbase + (tg * D + c) * rec, packed, rec);
                     put_u16(meta_sec + g * 4, s);
                     put_u16(meta_sec + g * 4 + 2, z);
                 }
@@ -521,7 +634,7 @@ static uint32_t quantize_tensor(const kvo_profile *p, const kvo_shape *sh, int t
                     kvo_quantize_group(X + t * D + (uint64_t)cg * G, G, bits, &s, &z, codes, &flags);
                     kvo_pack(codes, G, bits, packed);
                     uint64_t g = (((uint64_t)l * T + t) * H + h) * (D / G) + cg;
-                    memcpy(codes_sec + g * rec, packed, rec);
+                    memcpy(codes_sec + cbase + t * row_bytes + cg * rec, packed, rec);
                     put_u16(meta_sec + g * 4, s);
                     put_u16(meta_sec + g * 4 + 2, z);
                 }
@@ -548,17 +661,17 @@ uint32_t kvo_quantize(const kvo_profile *p, const kvo_shape *sh,
 
 /* Reconstruction ([FastKVComp] §4.1 "Fused Reconstruction"): dequantize, inverse
  * Hadamard, normalization and sign restoration, then (keys) undo the smoothing,
- * then round to the element type and write the row. */
+ * then (v2) add the block's anchor back, then round to the element type and
+ * write the row. */
 static void dequantize_tensor(const kvo_profile *p, const kvo_shape *sh, int tensor, const uint8_t *Q,
                               const kvo_layout *lay, uint8_t *const *bases, const int32_t *block_table)
 {
     const uint32_t L = sh->layers, T = sh->tokens, H = sh->kv_heads, D = sh->head_dim;
-    const uint32_t bits = tensor ? p->bits_v : p->bits_k;
     const uint32_t G = tensor ? p->group_v : p->group_k;
     const uint32_t axis = tensor ? p->axis_v : p->axis_k;
     const int smooth = (tensor == 0) && p->smooth_keys;
-    const uint64_t rec = (uint64_t)G * bits / 8;
     const uint8_t *codes_sec = Q + lay->off[tensor ? 2 : 0];
+    const uint8_t *anchor_sec = Q + lay->off[tensor ? 7 : 6];
     const uint8_t *meta_sec = Q + lay->off[tensor ? 3 : 1];
     const uint8_t *mu_sec = Q + lay->off[4];
     const int8_t *e_sec = (const int8_t *)(Q + lay->off[5]);
@@ -569,6 +682,10 @@ static void dequantize_tensor(const kvo_profile *p, const kvo_shape *sh, int ten
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t lh = 0; lh < (int64_t)L * H; lh++) {
         const uint32_t l = (uint32_t)(lh / H), h = (uint32_t)(lh % H);
+        const uint32_t bits = width_of(p, tensor, H, l, h);
+        const uint64_t rec = (uint64_t)G * bits / 8;
+        uint64_t row_bytes = 0;
+        const uint64_t cbase = code_base(p, sh, tensor, l, h, &row_bytes);
         float *X = (float *)malloc((size_t)T * D * sizeof(float));
         uint8_t codes[1024];
         if (axis == KVO_AXIS_OVER_TOKENS) {
@@ -576,7 +693,7 @@ static void dequantize_tensor(const kvo_profile *p, const kvo_shape *sh, int ten
                 uint64_t t0 = tg * G, n = (t0 + G <= T) ? G : T - t0;
                 for (uint32_t c = 0; c < D; c++) {
                     uint64_t g = (((uint64_t)l * H + h) * nTG + tg) * D + c;
-                    kvo_unpack(codes_sec + g * rec, G, bits, codes);
+                    kvo_unpack(codes_sec + cbase + (tg * D + c) * rec, G, bits, codes);
                     float s = kvo_f16_to_f32(get_u16(meta_sec + g * 4));
                     float z = kvo_f16_to_f32(get_u16(meta_sec + g * 4 + 2));
                     for (uint64_t i = 0; i < n; i++) X[(t0 + i) * D + c] = fmaf((float)codes[i], s, z);
@@ -586,7 +703,7 @@ static void dequantize_tensor(const kvo_profile *p, const kvo_shape *sh, int ten
             for (uint64_t t = 0; t < T; t++)
                 for (uint32_t cg = 0; cg < D / G; cg++) {
                     uint64_t g = (((uint64_t)l * T + t) * H + h) * (D / G) + cg;
-                    kvo_unpack(codes_sec + g * rec, G, bits, codes);
+                    kvo_unpack(codes_sec + cbase + t * row_bytes + cg * rec, G, bits, codes);
                     float s = kvo_f16_to_f32(get_u16(meta_sec + g * 4));
                     float z = kvo_f16_to_f32(get_u16(meta_sec + g * 4 + 2));
                     for (uint32_t i = 0; i < G; i++) X[t * D + (uint64_t)cg * G + i] = fmaf((float)codes[i], s, z);
@@ -604,6 +721,18 @@ static void dequantize_tensor(const kvo_profile *p, const kvo_shape *sh, int ten
                     if (e < -126) e = -126;
                     float sc = ldexpf(1.0f, e);
                     X[t * D + c] = fmaf(X[t * D + c], sc, mu);
+                }
+            }
+        }
+        /* undo the token delta: add the block's anchor back in fp32 */
+        if (p->token_delta) {
+            const uint64_t nAB = ceil_div(T, KVO_DELTA_BLOCK);
+            for (uint64_t t = 0; t < T; t++) {
+                uint64_t ab = t / KVO_DELTA_BLOCK;
+                for (uint32_t c = 0; c < D; c++) {
+                    uint64_t cell = (((uint64_t)l * H + h) * nAB + ab) * D + c;
+                    float a = elem_to_f32(get_u16(anchor_sec + 2 * cell), sh->dtype);
+                    X[t * D + c] = X[t * D + c] + a;
                 }
             }
         }
@@ -844,26 +973,47 @@ int kvo_chunk_decode(const kvo_profile *p, const uint8_t *in, size_t size, int r
 /* Stream container (READING; "GPU-resident compressed bitstream" and a      */
 /* "compressed-size scalar", [FastKVComp] §4.2).                              */
 /*  [0,64)   header (little-endian; see kvo_write_header)                    */
-/*  no stages: Q follows at byte 64.                                         */
-/*  stages:   u32 table[n_chunks] at byte 64 (bit 31 = stored raw, bits 0..30 */
+/*  [64,HB)  v2 width map (only with per-(layer, head) widths; HB = header    */
+/*           bytes, written at header offset 6)                               */
+/*  no stages: Q follows at byte HB.                                         */
+/*  stages:   u32 table[n_chunks] at byte HB (bit 31 = stored raw, bits 0..30 */
 /*            = stored size); chunk i starts at data_start + sum_{j<i}       */
-/*            align16(size_j), data_start = align16(64 + 4 n_chunks);        */
+/*            align16(size_j), data_start = align16(HB + 4 n_chunks);        */
 /*            padding bytes are zero.                                        */
 /* ------------------------------------------------------------------------ */
+/* READING (v2): version 2 when the profile uses the token delta or width maps,
+ * else 1.  Flags byte: bit 0 smoothing, bit 1 Hadamard, bit 2 token delta, bit 3
+ * width map.  With a map the two width bytes are 0 and the map follows the 64
+ * header bytes: entry i takes bits 2i, 2i+1 (least significant first) with the
+ * code 0, 1, 2, 3 for widths 2, 3, 4, 8; K entries l*H + h come first, then V. */
+static uint32_t width_code(uint32_t bits) { return bits == 2 ? 0u : bits == 3 ? 1u : bits == 4 ? 2u : 3u; }
+
 void kvo_write_header(const kvo_profile *p, const kvo_shape *sh, const kvo_layout *lay, uint8_t *h)
 {
-    memset(h, 0, KVO_HEADER_BYTES);
+    memset(h, 0, lay->header_bytes);
+    const int v2 = p->token_delta || has_maps(p);
     h[0] = 'K'; h[1] = 'V'; h[2] = 'C'; h[3] = '1';
-    put_u16(h + 4, 1);                 /* format version */
-    put_u16(h + 6, KVO_HEADER_BYTES);
+    put_u16(h + 4, v2 ? 2 : 1);        /* format version */
+    put_u16(h + 6, (uint16_t)lay->header_bytes);
     put_u32(h + 8, sh->layers);
     put_u32(h + 12, sh->tokens);
     put_u16(h + 16, (uint16_t)sh->kv_heads);
     put_u16(h + 18, (uint16_t)sh->head_dim);
     h[20] = (uint8_t)sh->dtype;
-    h[21] = (uint8_t)((p->smooth_keys ? 1 : 0) | (p->hadamard ? 2 : 0));
-    h[22] = (uint8_t)p->bits_k;
-    h[23] = (uint8_t)p->bits_v;
+    h[21] = (uint8_t)((p->smooth_keys ? 1 : 0) | (p->hadamard ? 2 : 0) | (p->token_delta ? 4 : 0) |
+                      (has_maps(p) ? 8 : 0));
+    h[22] = has_maps(p) ? 0 : (uint8_t)p->bits_k;
+    h[23] = has_maps(p) ? 0 : (uint8_t)p->bits_v;
+    if (has_maps(p)) {
+        const uint64_t n = (uint64_t)sh->layers * sh->kv_heads;
+        for (int tensor = 0; tensor < 2; tensor++)
+            for (uint64_t i = 0; i < n; i++) {
+                uint64_t e = tensor * n + i;
+                uint32_t w = width_code(width_of(p, tensor, sh->kv_heads, (uint32_t)(i / sh->kv_heads),
+                                                 (uint32_t)(i % sh->kv_heads)));
+                h[KVO_HEADER_BYTES + e / 4] |= (uint8_t)(w << (2 * (e % 4)));
+            }
+    }
     put_u16(h + 24, (uint16_t)p->group_k);
     put_u16(h + 26, (uint16_t)p->group_v);
     h[28] = (uint8_t)p->axis_k;
@@ -882,9 +1032,10 @@ void kvo_write_header(const kvo_profile *p, const kvo_shape *sh, const kvo_layou
 /* Lossless-encode Q into stream (after the header).  Returns the total stream size. */
 uint64_t kvo_lossless_encode(const kvo_profile *p, const kvo_layout *lay, const uint8_t *Q, uint8_t *stream)
 {
+    const uint64_t HB = lay->header_bytes;
     if (p->n_stages == 0) {
-        memcpy(stream + KVO_HEADER_BYTES, Q, lay->payload_bytes);
-        return KVO_HEADER_BYTES + lay->payload_bytes;
+        memcpy(stream + HB, Q, lay->payload_bytes);
+        return HB + lay->payload_bytes;
     }
     const uint64_t nc = lay->n_chunks, cb = p->chunk_bytes, P = lay->payload_bytes;
     uint8_t *tmp = (uint8_t *)malloc(nc * cb + 16);
@@ -897,9 +1048,9 @@ uint64_t kvo_lossless_encode(const kvo_profile *p, const kvo_layout *lay, const 
         sizes[i] = (uint32_t)sz | (raw ? 0x80000000u : 0u);
     }
     uint64_t pos = lay->data_start;
-    memset(stream + KVO_HEADER_BYTES, 0, lay->data_start - KVO_HEADER_BYTES);
+    memset(stream + HB, 0, lay->data_start - HB);
     for (uint64_t i = 0; i < nc; i++) {
-        put_u32(stream + KVO_HEADER_BYTES + 4 * i, sizes[i]);
+        put_u32(stream + HB + 4 * i, sizes[i]);
         uint64_t sz = sizes[i] & 0x7fffffffu;
         memcpy(stream + pos, tmp + i * cb, sz);
         memset(stream + pos + sz, 0, align16(sz) - sz);
@@ -935,12 +1086,15 @@ uint32_t kvo_lossless_decode(const kvo_profile *p, const kvo_shape *sh, const ui
 {
     kvo_layout lay;
     kvo_layout_of(p, sh, &lay);
-    uint8_t want[KVO_HEADER_BYTES];
+    const uint64_t HB = lay.header_bytes;
+    uint8_t *want = (uint8_t *)malloc(HB);
     kvo_write_header(p, sh, &lay, want);
-    if (stream_bytes < KVO_HEADER_BYTES || memcmp(want, stream, KVO_HEADER_BYTES) != 0) return KVO_FLAG_CORRUPT;
+    int hdr_bad = stream_bytes < HB || memcmp(want, stream, HB) != 0;
+    free(want);
+    if (hdr_bad) return KVO_FLAG_CORRUPT;
     if (p->n_stages == 0) {
-        if (stream_bytes < KVO_HEADER_BYTES + lay.payload_bytes) return KVO_FLAG_CORRUPT;
-        memcpy(Q, stream + KVO_HEADER_BYTES, lay.payload_bytes);
+        if (stream_bytes < HB + lay.payload_bytes) return KVO_FLAG_CORRUPT;
+        memcpy(Q, stream + HB, lay.payload_bytes);
         return 0;
     }
     const uint64_t nc = lay.n_chunks, cb = p->chunk_bytes, P = lay.payload_bytes;
@@ -949,7 +1103,7 @@ uint32_t kvo_lossless_decode(const kvo_profile *p, const kvo_shape *sh, const ui
     uint64_t pos = lay.data_start;
     int bad = 0;
     for (uint64_t i = 0; i < nc; i++) {
-        uint32_t e = get_u32(stream + KVO_HEADER_BYTES + 4 * i);
+        uint32_t e = get_u32(stream + HB + 4 * i);
         uint64_t sz = e & 0x7fffffffu;
         offs[i] = pos;
         pos += align16(sz);
@@ -958,7 +1112,7 @@ uint32_t kvo_lossless_decode(const kvo_profile *p, const kvo_shape *sh, const ui
     if (!bad) {
 #pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
         for (int64_t i = 0; i < (int64_t)nc; i++) {
-            uint32_t e = get_u32(stream + KVO_HEADER_BYTES + 4 * i);
+            uint32_t e = get_u32(stream + HB + 4 * i);
             uint64_t off = (uint64_t)i * cb, n = (off + cb <= P) ? cb : P - off;
             if (kvo_chunk_decode(p, stream + offs[i], e & 0x7fffffffu, (int)(e >> 31), n, Q + off) != 0) bad = 1;
         }

@@ -67,12 +67,14 @@ class Profile(C.Structure):
                 ("bits_k", C.c_uint32), ("bits_v", C.c_uint32), ("group_k", C.c_uint32),
                 ("group_v", C.c_uint32), ("axis_k", C.c_uint32), ("axis_v", C.c_uint32),
                 ("n_stages", C.c_uint32), ("stage_kind", C.c_uint32 * 4), ("stage_param", C.c_uint32 * 4),
-                ("chunk_bytes", C.c_uint32), ("seed", C.c_uint64)]
+                ("chunk_bytes", C.c_uint32), ("seed", C.c_uint64), ("token_delta", C.c_uint32),
+                ("pad_", C.c_uint32), ("bits_map_k", C.c_void_p), ("bits_map_v", C.c_void_p)]
 
 
 class Layout(C.Structure):
-    _fields_ = [("off", C.c_uint64 * 6), ("size", C.c_uint64 * 6), ("payload_bytes", C.c_uint64),
-                ("n_chunks", C.c_uint64), ("data_start", C.c_uint64), ("max_stream_bytes", C.c_uint64)]
+    _fields_ = [("off", C.c_uint64 * 8), ("size", C.c_uint64 * 8), ("payload_bytes", C.c_uint64),
+                ("n_chunks", C.c_uint64), ("data_start", C.c_uint64), ("max_stream_bytes", C.c_uint64),
+                ("header_bytes", C.c_uint64)]
 
 
 def lib():
@@ -141,8 +143,17 @@ def set_threads(n: int) -> int:
 # ----------------------------------------------------------------------------
 def make_profile(*, smooth_keys=True, hadamard=False, bits_k=4, bits_v=4, group_k=64, group_v=64,
                  axis_k=AXIS_OVER_TOKENS, axis_v=AXIS_OVER_CHANNELS, stages=(), chunk_bytes=16384,
-                 seed=0x5EED) -> Profile:
+                 seed=0x5EED, token_delta=False, bits_map_k=None, bits_map_v=None) -> Profile:
+    """bits_map_k / bits_map_v: optional [layers][kv_heads] code widths (format v2);
+    token_delta: the anchor-token delta transformer (format v2)."""
     p = Profile()
+    p.token_delta = int(bool(token_delta))
+    p._maps = []  # keeps the width maps alive as long as the profile
+    for name, m in (("bits_map_k", bits_map_k), ("bits_map_v", bits_map_v)):
+        if m is not None:
+            arr = np.ascontiguousarray(np.asarray(m, dtype=np.uint8).reshape(-1))
+            p._maps.append(arr)
+            setattr(p, name, arr.ctypes.data)
     p.smooth_keys, p.hadamard = int(bool(smooth_keys)), int(bool(hadamard))
     p.bits_k, p.bits_v, p.group_k, p.group_v = bits_k, bits_v, group_k, group_v
     p.axis_k, p.axis_v = axis_k, axis_v

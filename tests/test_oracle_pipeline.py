@@ -56,7 +56,7 @@ def test_payload_closed_form_llama8b(oracle):
     codes = 32 * 4096 * 8 * 128 // 2                 # 4 bits per element, K and V each
     meta = 32 * 4096 * 8 * 128 // 128 * 4            # 4 bytes per group of 128
     smooth = 32 * 8 * (4096 // 128) * 128 * 3        # centre (2 B) + exponent (1 B) per cell
-    assert list(lay.size) == [codes, meta, codes, meta, smooth // 3 * 2, smooth // 3]
+    assert list(lay.size) == [codes, meta, codes, meta, smooth // 3 * 2, smooth // 3, 0, 0]
     assert lay.payload_bytes == 2 * codes + 2 * meta + smooth
 
 
@@ -64,7 +64,7 @@ def test_sections_are_16_byte_aligned_and_ordered(oracle):
     prof = oracle.make_profile(bits_k=3, bits_v=3, group_k=32, group_v=32)
     shape = oracle.make_shape(1, 37, 3, 128, 2)
     lay = oracle.layout(prof, shape)
-    for i in range(6):
+    for i in range(8):
         assert lay.off[i] % 16 == 0
         if i:
             assert lay.off[i] == lay.off[i - 1] + (lay.size[i - 1] + 15) // 16 * 16
