@@ -12,8 +12,9 @@
 // look-back over per-chunk words (chunks are taken in ticket order, so a CTA only
 // ever waits for CTAs that are already running; every wait is bounded).
 //
-// Stream: 64-byte header | u32 table[n_chunks] (bit 31 = stored raw, bits 0..30 =
-// stored size) | chunk i at data_start + sum_{j<i} align16(size_j), zero padded.
+// Stream: header (64 bytes, plus the width map of a mixed-width profile) |
+// u32 table[n_chunks] (bit 31 = stored raw, bits 0..30 = stored size) | chunk i
+// at data_start + sum_{j<i} align16(size_j), zero padded.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -353,9 +354,10 @@ __global__ void kvc_prologue(const PrologueParams P) {
     if (!keep) P.ctrl[tid] = 0u;
   }
   for (uint64_t i = tid; i < P.n_state; i += nt) P.state[i] = 0ull;
-  if (P.write_header && tid < KVC_HEADER_BYTES) P.stream[tid] = P.header[tid];
+  if (P.write_header)
+    for (uint32_t i = tid; i < P.header_bytes; i += nt) P.stream[i] = P.header[i];
   if (P.write_header && tid < P.gap_len) P.stream[P.gap_off + tid] = 0;
-  if (P.payload && tid < 6 * 16) {
+  if (P.payload && tid < kSections * 16) {
     const int s = tid / 16, b = tid % 16;
     if ((uint32_t)b < P.pad_len[s]) P.payload[P.pad_off[s] + b] = 0;
   }
@@ -478,7 +480,7 @@ __global__ void __launch_bounds__(LT) kvc_lossless_enc(const LosslessParams P) {
         s_excl = excl;
         const uint64_t dst = P.data_start + excl;
         if (dst + asz > P.stream_cap) atomicOr(ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CAPACITY);
-        reinterpret_cast<uint32_t *>(P.stream + KVC_HEADER_BYTES)[ticket] = size | (raw ? 0x80000000u : 0u);
+        reinterpret_cast<uint32_t *>(P.stream + P.header_bytes)[ticket] = size | (raw ? 0x80000000u : 0u);
         if (ticket == P.n_chunks - 1) {
           const uint64_t total = dst + asz;
           reinterpret_cast<uint64_t *>(ctrl)[kCtrlStreamBytes] = total;
@@ -990,7 +992,7 @@ __global__ void __launch_bounds__(FW, kFastCtasPerSm) kvc_lossless_enc_fast(cons
       if (lane == 0) {
         if (t && (int64_t)t != P.skip_ticket) st_word64(P.state + t, kFlagIncl | (excl + asz));
         if (dst + asz > P.stream_cap) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CAPACITY);
-        reinterpret_cast<uint32_t *>(P.stream + KVC_HEADER_BYTES)[t] = word;
+        reinterpret_cast<uint32_t *>(P.stream + P.header_bytes)[t] = word;
         if (t == nc - 1) {
           const uint64_t total = dst + asz;
           reinterpret_cast<uint64_t *>(P.ctrl)[kCtrlStreamBytes] = total;
@@ -1261,16 +1263,16 @@ __global__ void __launch_bounds__(PT) kvc_decode_prepare(const LosslessParams P)
   }
   __syncthreads();
   const uint64_t stream_bytes = P.stream_cap;
-  if (stream_bytes < KVC_HEADER_BYTES) {
+  if (stream_bytes < P.header_bytes) {
     if (tid == 0) s_bad = 1;
-  } else if (tid < KVC_HEADER_BYTES / 4) {
+  } else if (tid < P.header_bytes / 4) {
     if (reinterpret_cast<const uint32_t *>(P.stream)[tid] != reinterpret_cast<const uint32_t *>(P.header)[tid])
       atomicOr(&s_bad, 1);
   }
   __syncthreads();
   if (!s_bad) {
     if (P.n_stages == 0) {
-      if (tid == 0 && stream_bytes < KVC_HEADER_BYTES + P.payload_bytes) s_bad = 1;
+      if (tid == 0 && stream_bytes < P.header_bytes + P.payload_bytes) s_bad = 1;
     } else if (stream_bytes < P.data_start) {
       if (tid == 0) s_bad = 1;
     } else {
@@ -1279,7 +1281,7 @@ __global__ void __launch_bounds__(PT) kvc_decode_prepare(const LosslessParams P)
       const uint32_t nc = P.n_chunks;
       const uint32_t S = ((nc + PT - 1) / PT + 3) & ~3u;
       const uint32_t i0 = min(nc, tid * S), i1 = min(nc, i0 + S);
-      const uint32_t *table = reinterpret_cast<const uint32_t *>(P.stream + KVC_HEADER_BYTES);
+      const uint32_t *table = reinterpret_cast<const uint32_t *>(P.stream + P.header_bytes);
       unsigned long long sum = 0;
       int bad = 0;
       for (uint32_t i = i0; i < i1; i += 4) {
@@ -1356,12 +1358,12 @@ constexpr uint32_t kFusedMaxOwn = 64;           // chunks per CTA
 __device__ bool decode_offsets(const LosslessParams &P, unsigned long long *tmp, unsigned long long *s_off,
                                int *s_bad) {
   const uint32_t tid = threadIdx.x, nc = P.n_chunks;
-  const uint32_t *table = reinterpret_cast<const uint32_t *>(P.stream + KVC_HEADER_BYTES);
+  const uint32_t *table = reinterpret_cast<const uint32_t *>(P.stream + P.header_bytes);
   if (tid == 0) *s_bad = 0;
   __syncthreads();
-  if (tid < KVC_HEADER_BYTES / 4 &&
-      reinterpret_cast<const uint32_t *>(P.stream)[tid] != reinterpret_cast<const uint32_t *>(P.header)[tid])
-    atomicOr(s_bad, 1);
+  for (uint32_t w = tid; w < P.header_bytes / 4; w += LT)
+    if (reinterpret_cast<const uint32_t *>(P.stream)[w] != reinterpret_cast<const uint32_t *>(P.header)[w])
+      atomicOr(s_bad, 1);
   // thread tid takes entries [S tid, S tid + S), S a multiple of 4 (16-byte reads;
   // the table is 16-byte aligned and padded to data_start)
   const uint32_t S = ((nc + LT - 1) / LT + 3) & ~3u;
@@ -1416,16 +1418,24 @@ __device__ bool decode_offsets(const LosslessParams &P, unsigned long long *tmp,
 // Decode, step 2: one chunk per CTA iteration back into the payload.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(LT, 3) kvc_lossless_dec(const LosslessParams P, const FastSpec F) {
-  if (!P.fused_offsets && (*(volatile uint32_t *)(P.ctrl + kCtrlFlags) & KVC_FLAG_CORRUPT)) return;
   extern __shared__ uint4 smem_u4[];
   __shared__ unsigned long long s_off[kFusedMaxOwn];
   __shared__ int s_bad;
+  if (!P.fused_offsets) {
+    // A stream the prepare step found corrupt is skipped.  The whole CTA takes one
+    // decision from one read: other CTAs of this launch may set CORRUPT while it
+    // starts, and a CTA split between warps that return and warps that go on
+    // would leave the named barriers of the stage functions waiting.
+    if (threadIdx.x == 0) s_bad = (*(volatile uint32_t *)(P.ctrl + kCtrlFlags) & KVC_FLAG_CORRUPT) != 0;
+    __syncthreads();
+    if (s_bad) return;
+  }
   uint8_t *bufA = reinterpret_cast<uint8_t *>(smem_u4);
   uint8_t *bufB = bufA + P.chunk_bytes + 64;
   uint8_t *Bs = bufB + P.chunk_bytes + 64;
   uint32_t *tmp = reinterpret_cast<uint32_t *>(Bs + 8192);
   if (P.fused_offsets && !decode_offsets(P, reinterpret_cast<unsigned long long *>(tmp), s_off, &s_bad)) return;
-  const uint32_t *table = reinterpret_cast<const uint32_t *>(P.stream + KVC_HEADER_BYTES);
+  const uint32_t *table = reinterpret_cast<const uint32_t *>(P.stream + P.header_bytes);
   const uint32_t last = P.n_stages - 1;
   const bool has_rze = P.kind[last] == KVC_ST_RZE;
 
