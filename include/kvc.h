@@ -70,7 +70,7 @@ enum { KVC_ST_TUPL = 1, KVC_ST_BIT = 2, KVC_ST_DELTA = 3, KVC_ST_RZE = 4 };
 
 #define KVC_MAX_STAGES 4
 #define KVC_MAX_LAYERS 256
-#define KVC_HEADER_BYTES 64
+#define KVC_HEADER_BYTES 64 /* fixed part; a v2 width map follows it (kvc_header_bytes) */
 
 /* One lossless stage: TUPL param k in {2,4,8} (k-byte tuples -> k byte columns);
  * BIT param 8 (bit planes of bytes); DELTA param w in {1,2,4} (w-byte words,
@@ -81,9 +81,11 @@ typedef struct kvc_stage {
     uint8_t param;
 } kvc_stage;
 
-/* A compression profile, chosen per request and fixed for it ("KVServe" §3.1). */
+/* A compression profile, chosen per request and fixed for it ("KVServe" §3.1).
+ * struct_size versions the struct: sizeof(kvc_profile), or KVC_PROFILE_V1_SIZE for
+ * callers built before the format-v2 fields (they read as 0 / NULL). */
 typedef struct kvc_profile {
-    uint32_t struct_size;   /* = sizeof(kvc_profile) */
+    uint32_t struct_size;   /* = sizeof(kvc_profile) (or KVC_PROFILE_V1_SIZE) */
     uint8_t smooth_keys;    /* per-channel key smoothing (128-token blocks) */
     uint8_t hadamard;       /* randomized Hadamard rotation along head_dim (K and V) */
     uint8_t bits_k, bits_v; /* code width: 2, 3, 4 or 8 */
@@ -95,7 +97,23 @@ typedef struct kvc_profile {
     uint32_t chunk_bytes;      /* lossless chunk size: multiple of 256 in [256, 65536] */
     uint32_t reserved1;
     uint64_t hadamard_seed;    /* seed of the +-1 sign vector (SplitMix64) */
+    /* ---- format v2 (optional; a profile that uses neither writes v1 streams) ---- */
+    /* Token delta ("KVServe" §5.1, the Delta transformer, after CacheGen): the first
+     * token of every 128-token block is the anchor; K and V rows become their fp32
+     * differences from it before smoothing and the Hadamard rotation, the anchors'
+     * element bits go to payload sections 6 (K) and 7 (V). */
+    uint8_t token_delta;
+    uint8_t reserved2[7];
+    /* Per-(layer, head) code widths ("KVServe" §5.1 layer- and head-wise mixed
+     * precision; "Beyond Compression Ratio" §4.1 head-importance-aware mixed
+     * precision): HOST arrays of layers * kv_heads widths in {2, 3, 4, 8}, entry
+     * l * kv_heads + h, read (copied) by kvc_plan only; NULL = bits_k / bits_v for
+     * every head.  With either map: layers * kv_heads <= KVC_MAX_MAP_ENTRIES. */
+    const uint8_t *bits_map_k;
+    const uint8_t *bits_map_v;
 } kvc_profile;
+#define KVC_PROFILE_V1_SIZE 40
+#define KVC_MAX_MAP_ENTRIES 2048
 
 /* KV tensor geometry.  Each layer's K (and V) is addressed as rows of
  * kv_heads*head_dim elements: token t lives at
@@ -144,10 +162,15 @@ size_t kvc_max_stream_bytes(const kvc_plan_t *plan);
 /* Bytes of the quantized payload Q (all sections, each 16-byte aligned). */
 size_t kvc_payload_bytes(const kvc_plan_t *plan);
 /* Offset and size of payload section i: 0 K codes, 1 K scale/zero, 2 V codes,
- * 3 V scale/zero, 4 K smoothing centres (fp16), 5 K smoothing exponents (int8). */
+ * 3 V scale/zero, 4 K smoothing centres (fp16), 5 K smoothing exponents (int8),
+ * 6 K delta anchors, 7 V delta anchors (element bits). */
 kvc_status kvc_section(const kvc_plan_t *plan, int index, uint64_t *offset, uint64_t *size);
 /* Number of lossless chunks (0 without stages). */
 uint64_t kvc_num_chunks(const kvc_plan_t *plan);
+/* Bytes of the stream header: 64, plus the 2-bit width map (padded to 16 bytes)
+ * when the profile has per-(layer, head) widths.  The chunk table (or, without
+ * stages, the payload) starts there. */
+size_t kvc_header_bytes(const kvc_plan_t *plan);
 
 /* Full encode ("KVServe" §5.1: BS = C(Q(T(X))); "Beyond Compression Ratio" §4.1
  * fused transform + quantization into the all-layer buffer, §4.2 device-pointer

@@ -4,11 +4,14 @@
 // Compression Ratio: High-Throughput KV Compression for Disaggregated LLM
 // Serving", §4.1), sections in this order, each starting 16-byte aligned:
 //   0 K codes, 1 K {scale, zero}, 2 V codes, 3 V {scale, zero},
-//   4 K smoothing centres (fp16), 5 K smoothing exponents (int8).
+//   4 K smoothing centres (fp16), 5 K smoothing exponents (int8),
+//   6 K delta anchors, 7 V delta anchors (element bits; token delta only).
 // Groups over tokens: records [layer][head][token group][channel]; groups over
-// channels: records [layer][token][head][channel group]; smoothing cells
-// [layer][head][128-token block][channel].  A record holds G codes of b bits,
-// least significant bit first.
+// channels: records [layer][token][head][channel group]; smoothing and anchor
+// cells [layer][head][128-token block][channel].  A record holds G codes of b
+// bits, least significant bit first.  With per-(layer, head) widths ("KVServe"
+// §5.1 mixed precision) each (layer, head) -- or each head of a token row --
+// keeps its own record size; the offsets follow from prefix sums of the widths.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -29,13 +32,17 @@ struct TimingRec {
 };
 
 struct kvc_plan_s {
-  kvc_profile prof;
+  kvc_profile prof;  // bits_map_* cleared: the plan keeps its own copies below
   kvc_shape shape;
-  uint64_t off[6], size[6];
+  uint64_t off[kSections], size[kSections];
   uint64_t payload_bytes, n_chunks, data_start, max_stream_bytes, workspace_bytes;
   uint64_t n_tg_k, n_tg_v, n_sb;
   uint32_t sign[4];
-  uint8_t header[KVC_HEADER_BYTES];
+  uint32_t header_bytes;
+  uint8_t header[kMaxHeaderBytes];
+  bool mixed;                    // per-(layer, head) widths
+  std::vector<uint8_t> width[2]; // K, V: width of entry l * H + h (mixed only)
+  WidthTable *wt[2];             // prefix sums of the widths (mixed only)
   int sm_count;
   uint64_t launches;
   // host-side tensor maps for the key-tile encoder's TMA loads, per tensor, and the
@@ -68,9 +75,19 @@ static uint64_t splitmix64(uint64_t &state) {
 static bool valid_bits(uint32_t b) { return b == 2 || b == 3 || b == 4 || b == 8; }
 static bool valid_group(uint32_t g) { return g == 32 || g == 64 || g == 128; }
 
+// Copy a caller's profile of either struct version into a full one.
+static kvc_status read_profile(const kvc_profile *in, kvc_profile *out) {
+  memset(out, 0, sizeof *out);
+  if (in->struct_size == sizeof(kvc_profile)) memcpy(out, in, sizeof *out);
+  else if (in->struct_size == KVC_PROFILE_V1_SIZE) memcpy(out, in, KVC_PROFILE_V1_SIZE);
+  else return KVC_ERR_INVALID_ARG;
+  out->struct_size = sizeof(kvc_profile);
+  return KVC_OK;
+}
+
 static kvc_status check_profile(const kvc_profile *p) {
-  if (p->struct_size != sizeof(kvc_profile)) return KVC_ERR_INVALID_ARG;
   if (!valid_bits(p->bits_k) || !valid_bits(p->bits_v)) return KVC_ERR_INVALID_ARG;
+  if (p->token_delta > 1) return KVC_ERR_INVALID_ARG;
   if (!valid_group(p->group_k) || !valid_group(p->group_v)) return KVC_ERR_INVALID_ARG;
   if (p->axis_k > 1 || p->axis_v > 1) return KVC_ERR_INVALID_ARG;
   if (p->smooth_keys > 1 || p->hadamard > 1) return KVC_ERR_INVALID_ARG;
@@ -94,26 +111,42 @@ static uint64_t groups(const kvc_shape &s, uint32_t axis, uint32_t G) {
   return axis == KVC_AXIS_OVER_TOKENS ? L * H * ceil_div(T, G) * D : L * T * H * (D / G);
 }
 
+// Width code of the v2 header map: 2, 3, 4, 8 -> 0, 1, 2, 3.
+static uint32_t width_code(uint32_t b) { return b == 2 ? 0u : b == 3 ? 1u : b == 4 ? 2u : 3u; }
+
 static void put16(uint8_t *p, uint32_t v) { p[0] = (uint8_t)v; p[1] = (uint8_t)(v >> 8); }
 static void put32(uint8_t *p, uint32_t v) { for (int i = 0; i < 4; i++) p[i] = (uint8_t)(v >> (8 * i)); }
 static void put64(uint8_t *p, uint64_t v) { for (int i = 0; i < 8; i++) p[i] = (uint8_t)(v >> (8 * i)); }
 
-// Stream header, 64 bytes little-endian: magic "KVC1", version 1, header size,
-// geometry, profile, chunking, seed and payload size.
+// Stream header, 64 bytes little-endian: magic "KVC1", version (2 when the token
+// delta or per-(layer, head) widths are used, else 1), header size, geometry,
+// profile (flags: 1 smoothing, 2 Hadamard, 4 token delta, 8 width map), chunking,
+// seed and payload size; with a width map, the map follows (2 bits per entry,
+// entry i at bits 2i..2i+1, K entries then V entries, padded to 16 bytes).
 static void build_header(kvc_plan_s *P) {
   uint8_t *h = P->header;
-  memset(h, 0, KVC_HEADER_BYTES);
+  memset(h, 0, sizeof P->header);
+  const bool v2 = P->prof.token_delta || P->mixed;
   h[0] = 'K'; h[1] = 'V'; h[2] = 'C'; h[3] = '1';
-  put16(h + 4, 1);
-  put16(h + 6, KVC_HEADER_BYTES);
+  put16(h + 4, v2 ? 2 : 1);
+  put16(h + 6, P->header_bytes);
   put32(h + 8, P->shape.layers);
   put32(h + 12, P->shape.tokens);
   put16(h + 16, P->shape.kv_heads);
   put16(h + 18, P->shape.head_dim);
   h[20] = (uint8_t)P->shape.dtype;
-  h[21] = (uint8_t)((P->prof.smooth_keys ? 1 : 0) | (P->prof.hadamard ? 2 : 0));
-  h[22] = P->prof.bits_k;
-  h[23] = P->prof.bits_v;
+  h[21] = (uint8_t)((P->prof.smooth_keys ? 1 : 0) | (P->prof.hadamard ? 2 : 0) | (P->prof.token_delta ? 4 : 0) |
+                    (P->mixed ? 8 : 0));
+  h[22] = P->mixed ? 0 : P->prof.bits_k;
+  h[23] = P->mixed ? 0 : P->prof.bits_v;
+  if (P->mixed) {
+    const uint64_t n = (uint64_t)P->shape.layers * P->shape.kv_heads;
+    for (int t = 0; t < 2; t++)
+      for (uint64_t i = 0; i < n; i++) {
+        const uint64_t e = t * n + i;
+        h[KVC_HEADER_BYTES + e / 4] |= (uint8_t)(width_code(P->width[t][i]) << (2 * (e % 4)));
+      }
+  }
   put16(h + 24, P->prof.group_k);
   put16(h + 26, P->prof.group_v);
   h[28] = P->prof.axis_k;
@@ -129,11 +162,14 @@ static void build_header(kvc_plan_s *P) {
   put64(h + 56, P->payload_bytes);
 }
 
-extern "C" kvc_status kvc_plan(const kvc_profile *profile, const kvc_shape *shape, kvc_plan_t **out) {
-  if (!profile || !shape || !out) return KVC_ERR_INVALID_ARG;
+extern "C" kvc_status kvc_plan(const kvc_profile *profile_in, const kvc_shape *shape, kvc_plan_t **out) {
+  if (!profile_in || !shape || !out) return KVC_ERR_INVALID_ARG;
   *out = nullptr;
-  kvc_status st = check_profile(profile);
+  kvc_profile prof;
+  kvc_status st = read_profile(profile_in, &prof);
   if (st != KVC_OK) return st;
+  const kvc_profile *profile = &prof;
+  if ((st = check_profile(profile)) != KVC_OK) return st;
   kvc_shape s = *shape;
   if (s.struct_size != sizeof(kvc_shape)) return KVC_ERR_INVALID_ARG;
   if (s.dtype != KVC_F16 && s.dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
@@ -150,34 +186,81 @@ extern "C" kvc_status kvc_plan(const kvc_profile *profile, const kvc_shape *shap
     if (s.page_stride < (uint64_t)s.page_size * s.token_stride) return KVC_ERR_INVALID_ARG;
   }
 
+  const bool mixed = profile->bits_map_k || profile->bits_map_v;
+  const uint64_t n_lh = (uint64_t)s.layers * s.kv_heads;
+  // the format-v2 features are built into the key-tile and row kernels; smoothed
+  // keys grouped over channels (the generic tile kernels) stay format v1
+  if ((mixed || profile->token_delta) && profile->smooth_keys && profile->axis_k == KVC_AXIS_OVER_CHANNELS)
+    return KVC_ERR_UNSUPPORTED;
+  if (mixed && n_lh > KVC_MAX_MAP_ENTRIES) return KVC_ERR_UNSUPPORTED;
+  if (mixed)
+    for (int t = 0; t < 2; t++) {
+      const uint8_t *m = t ? profile->bits_map_v : profile->bits_map_k;
+      if (m)
+        for (uint64_t i = 0; i < n_lh; i++)
+          if (!valid_bits(m[i])) return KVC_ERR_INVALID_ARG;
+    }
+
   kvc_plan_s *P = new (std::nothrow) kvc_plan_s();
   if (!P) return KVC_ERR_INVALID_ARG;
   P->prof = *profile;
+  P->prof.bits_map_k = P->prof.bits_map_v = nullptr;
   P->shape = s;
+  P->mixed = mixed;
+  // code bytes per unit of width: one (layer, head) block of n_tg groups over
+  // tokens, or one head of one token row (groups over channels)
+  const uint64_t unit_k = profile->axis_k == KVC_AXIS_OVER_TOKENS ? 16 * ceil_div(s.tokens, profile->group_k) * profile->group_k
+                                                                   : 16 * (uint64_t)s.tokens;
+  const uint64_t unit_v = profile->axis_v == KVC_AXIS_OVER_TOKENS ? 16 * ceil_div(s.tokens, profile->group_v) * profile->group_v
+                                                                   : 16 * (uint64_t)s.tokens;
+  uint64_t wtot[2] = {n_lh * profile->bits_k, n_lh * profile->bits_v};
+  if (mixed) {
+    for (int t = 0; t < 2; t++) {
+      const uint8_t *m = t ? profile->bits_map_v : profile->bits_map_k;
+      const uint8_t def = t ? profile->bits_v : profile->bits_k;
+      P->width[t].assign(n_lh, def);
+      if (m) memcpy(P->width[t].data(), m, n_lh);
+      P->wt[t] = new (std::nothrow) WidthTable();
+      if (!P->wt[t]) {
+        kvc_plan_destroy(P);
+        return KVC_ERR_INVALID_ARG;
+      }
+      uint32_t acc = 0;
+      for (uint64_t i = 0; i < n_lh; i++) {
+        P->wt[t]->wsum[i] = (uint16_t)acc;
+        acc += P->width[t][i];
+      }
+      P->wt[t]->wsum[n_lh] = (uint16_t)acc;
+      wtot[t] = acc;
+    }
+  }
   const uint64_t gk = groups(s, profile->axis_k, profile->group_k), gv = groups(s, profile->axis_v, profile->group_v);
   const uint64_t nsb = (uint64_t)s.layers * s.kv_heads * ceil_div(s.tokens, kSmoothBlock) * s.head_dim;
-  P->size[0] = gk * profile->group_k * profile->bits_k / 8;
+  P->size[0] = unit_k * wtot[0];
   P->size[1] = gk * 4;
-  P->size[2] = gv * profile->group_v * profile->bits_v / 8;
+  P->size[2] = unit_v * wtot[1];
   P->size[3] = gv * 4;
   P->size[4] = profile->smooth_keys ? nsb * 2 : 0;
   P->size[5] = profile->smooth_keys ? nsb : 0;
+  P->size[6] = profile->token_delta ? nsb * 2 : 0;
+  P->size[7] = profile->token_delta ? nsb * 2 : 0;
   uint64_t o = 0;
-  for (int i = 0; i < 6; i++) {
+  for (int i = 0; i < kSections; i++) {
     P->off[i] = o;
     o += align_up(P->size[i], 16);
   }
   P->payload_bytes = o;
+  P->header_bytes = (uint32_t)(KVC_HEADER_BYTES + (mixed ? align_up(ceil_div(4 * n_lh, 8), 16) : 0));
   if (profile->n_stages) {
     P->n_chunks = ceil_div(o, profile->chunk_bytes);
     if (P->n_chunks >= (1ull << 31)) {
-      delete P;
+      kvc_plan_destroy(P);
       return KVC_ERR_UNSUPPORTED;
     }
-    P->data_start = align_up(KVC_HEADER_BYTES + 4 * P->n_chunks, 16);
+    P->data_start = align_up(P->header_bytes + 4 * P->n_chunks, 16);
   } else {
     P->n_chunks = 0;
-    P->data_start = KVC_HEADER_BYTES;
+    P->data_start = P->header_bytes;
   }
   P->max_stream_bytes = P->data_start + o;
   P->workspace_bytes = kCtrlBytes + align_up(8 * P->n_chunks, 256) + (profile->n_stages ? o : 0);
@@ -214,6 +297,8 @@ extern "C" void kvc_plan_destroy(kvc_plan_t *plan) {
   for (cudaEvent_t e : plan->pool) cudaEventDestroy(e);
   delete plan->tm[0];
   delete plan->tm[1];
+  delete plan->wt[0];
+  delete plan->wt[1];
   delete plan;
 }
 
@@ -222,9 +307,10 @@ extern "C" size_t kvc_max_stream_bytes(const kvc_plan_t *p) { return p ? (size_t
 extern "C" size_t kvc_payload_bytes(const kvc_plan_t *p) { return p ? (size_t)p->payload_bytes : 0; }
 extern "C" uint64_t kvc_num_chunks(const kvc_plan_t *p) { return p ? p->n_chunks : 0; }
 extern "C" uint64_t kvc_launch_count(const kvc_plan_t *p) { return p ? p->launches : 0; }
+extern "C" size_t kvc_header_bytes(const kvc_plan_t *p) { return p ? (size_t)p->header_bytes : 0; }
 
 extern "C" kvc_status kvc_section(const kvc_plan_t *p, int index, uint64_t *offset, uint64_t *size) {
-  if (!p || index < 0 || index > 5) return KVC_ERR_INVALID_ARG;
+  if (!p || index < 0 || index >= kSections) return KVC_ERR_INVALID_ARG;
   if (offset) *offset = p->off[index];
   if (size) *size = p->size[index];
   return KVC_OK;
@@ -411,13 +497,17 @@ static kvc_status run_quant(kvc_plan_s *P, const kvc_kv *kv, uint8_t *Q, void *w
     q.ex = reinterpret_cast<int8_t *>(Q + P->off[5]);
     q.status = ctrl_of(ws) + kCtrlFlags;
     q.check_corrupt = check_corrupt;
+    q.delta = P->prof.token_delta;
+    q.anchors = Q + P->off[tensor ? 7 : 6];
+    q.mixed = P->mixed;
+    const WidthTable *wt = P->mixed ? P->wt[tensor] : nullptr;
     const TmaMaps *maps = nullptr;
     if (enc && q.axis == KVC_AXIS_OVER_TOKENS && !kv->block_table) maps = tensor_maps(P, tensor, src);
     q.tma = maps != nullptr;
     Bracket br(P, st);
     const char *name = "";
-    const int rc = enc ? launch_quantize(q, maps, P->sm_count, st, &P->launches, &name)
-                       : launch_dequantize(q, P->sm_count, st, &P->launches, &name);
+    const int rc = enc ? launch_quantize(q, maps, wt, P->sm_count, st, &P->launches, &name)
+                       : launch_dequantize(q, wt, P->sm_count, st, &P->launches, &name);
     br.done(name);
     if (rc) return KVC_ERR_CUDA;
   }
@@ -434,18 +524,19 @@ static kvc_status run_prologue(kvc_plan_s *P, void *ws, bool zero_flags, bool ze
   pp.zero_flags = zero_flags;
   pp.write_header = stream != nullptr;
   pp.stream = stream;
-  memcpy(pp.header, P->header, KVC_HEADER_BYTES);
+  pp.header_bytes = P->header_bytes;
+  memcpy(pp.header, P->header, P->header_bytes);
   if (stream) {
     if (P->prof.n_stages == 0 || P->n_chunks == 0) pp.static_size = P->data_start + (P->prof.n_stages ? 0 : P->payload_bytes);
     pp.d_stream_bytes = d_stream_bytes;
     if (P->prof.n_stages) {
-      pp.gap_off = KVC_HEADER_BYTES + 4 * P->n_chunks;
+      pp.gap_off = P->header_bytes + 4 * P->n_chunks;
       pp.gap_len = (uint32_t)(P->data_start - pp.gap_off);
     }
   }
   pp.payload = payload;
   if (payload)
-    for (int i = 0; i < 6; i++) {
+    for (int i = 0; i < kSections; i++) {
       pp.pad_off[i] = P->off[i] + P->size[i];
       pp.pad_len[i] = (uint32_t)(align_up(P->size[i], 16) - P->size[i]);
     }
@@ -471,14 +562,15 @@ static void fill_lossless(kvc_plan_s *P, LosslessParams &lp, void *ws) {
   lp.ctrl = ctrl_of(ws);
   lp.skip_ticket = P->skip_ticket;
   lp.poll_limit = P->poll_limit;
-  memcpy(lp.header, P->header, KVC_HEADER_BYTES);
+  lp.header_bytes = P->header_bytes;
+  memcpy(lp.header, P->header, P->header_bytes);
 }
 
 static kvc_status lossless_encode_impl(kvc_plan_s *P, const uint8_t *Q, void *d_stream, size_t cap, void *ws,
                                        uint64_t *d_stream_bytes, cudaStream_t st) {
   if (P->prof.n_stages == 0) {
     if (P->payload_bytes &&
-        cudaMemcpyAsync(static_cast<uint8_t *>(d_stream) + KVC_HEADER_BYTES, Q, P->payload_bytes,
+        cudaMemcpyAsync(static_cast<uint8_t *>(d_stream) + P->header_bytes, Q, P->payload_bytes,
                         cudaMemcpyDeviceToDevice, st) != cudaSuccess)
       return KVC_ERR_CUDA;
     return KVC_OK;
@@ -536,7 +628,7 @@ extern "C" kvc_status kvc_encode(kvc_plan_t *plan, const kvc_kv *in, void *d_str
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t *out = static_cast<uint8_t *>(d_stream);
   // without lossless stages the payload is written in place after the header
-  uint8_t *Q = plan->prof.n_stages ? ws_payload(plan, d_workspace) : out + KVC_HEADER_BYTES;
+  uint8_t *Q = plan->prof.n_stages ? ws_payload(plan, d_workspace) : out + plan->header_bytes;
   if ((s = run_prologue(plan, d_workspace, true, true, out, d_stream_bytes, Q, st)) != KVC_OK) return s;
   if ((s = run_quant(plan, in, Q, d_workspace, true, false, st)) != KVC_OK) return s;
   if (plan->prof.n_stages == 0) return KVC_OK;
@@ -562,8 +654,8 @@ static kvc_status lossless_decode_impl(kvc_plan_s *P, const void *d_stream, size
   }
   if (P->prof.n_stages == 0) {
     // the payload sits after the header; copy only when the caller wants it elsewhere
-    if (copy_plain && P->payload_bytes && stream_bytes >= KVC_HEADER_BYTES + P->payload_bytes &&
-        cudaMemcpyAsync(Q, static_cast<const uint8_t *>(d_stream) + KVC_HEADER_BYTES, P->payload_bytes,
+    if (copy_plain && P->payload_bytes && stream_bytes >= P->header_bytes + P->payload_bytes &&
+        cudaMemcpyAsync(Q, static_cast<const uint8_t *>(d_stream) + P->header_bytes, P->payload_bytes,
                         cudaMemcpyDeviceToDevice, st) != cudaSuccess)
       return KVC_ERR_CUDA;
     return KVC_OK;
@@ -605,7 +697,7 @@ extern "C" kvc_status kvc_decode(kvc_plan_t *plan, const void *d_stream, size_t 
   if ((s = check_ws(plan, d_workspace, workspace_bytes)) != KVC_OK) return s;
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t *Q = plan->prof.n_stages ? ws_payload(plan, d_workspace)
-                                   : static_cast<uint8_t *>(const_cast<void *>(d_stream)) + KVC_HEADER_BYTES;
+                                   : static_cast<uint8_t *>(const_cast<void *>(d_stream)) + plan->header_bytes;
   if ((s = lossless_decode_impl(plan, d_stream, stream_bytes, Q, d_workspace, false, st)) != KVC_OK) return s;
   return run_quant(plan, out, Q, d_workspace, false, true, st);
 }

@@ -21,6 +21,10 @@ constexpr uint32_t kCtrlBytes = 256;
 constexpr int kCtrlFlags = 0;       // u32 index
 constexpr int kCtrlStreamBytes = 1; // u64 index
 constexpr int kCtrlTicket = 4;      // u32 index
+constexpr int kSections = 8;        // payload sections (kvc_section)
+// largest stream header: 64 bytes + a 2-bit width map of KVC_MAX_MAP_ENTRIES
+// (layer, head) entries for each of K and V
+constexpr int kMaxHeaderBytes = KVC_HEADER_BYTES + 2 * KVC_MAX_MAP_ENTRIES * 2 / 8;
 
 // Geometry of one KV tensor (K or V) of every layer.
 struct KvGeom {
@@ -49,6 +53,19 @@ struct QuantParams {
   uint32_t check_corrupt;        // dequantize: skip when the status word carries CORRUPT
   uint32_t hadamard;             // randomized Hadamard on
   uint32_t tma;                  // key-tile encoder: tiles arrive through the tensor maps (TmaMaps)
+  uint32_t delta;                // token delta: subtract (add back) each 128-token block's first row
+  uint32_t mixed;                // per-(layer, head) widths: the launch also takes a WidthTable
+  uint8_t *anchors;              // token delta: anchor element bits [layer][head][block][channel]
+};
+
+// Per-(layer, head) widths of one tensor: wsum[i] = sum of the widths of entries
+// 0 .. i-1 (entry = layer * H + head), i = 0 .. L*H; the width of entry i is
+// wsum[i + 1] - wsum[i].  Code offsets follow from it: groups over tokens, the
+// (layer, head) block starts at 16 * n_tg * G * wsum[lh] bytes; groups over
+// channels, layer l starts at 16 * T * wsum[l*H], token t of it at
+// + 16 * t * (wsum[(l+1)*H] - wsum[l*H]) and head h at + 16 * (wsum[lh] - wsum[l*H]).
+struct WidthTable {
+  uint16_t wsum[KVC_MAX_MAP_ENTRIES + 1];
 };
 
 // Tensor maps of one tensor's layers for the key-tile encoder's TMA loads: rank 2
@@ -69,7 +86,8 @@ struct PrologueParams {
   uint32_t zero_flags;  // also clear the status word
   uint32_t write_header;
   uint8_t *stream;
-  uint8_t header[KVC_HEADER_BYTES];
+  uint32_t header_bytes;
+  uint8_t header[kMaxHeaderBytes];
   uint64_t static_size; // nonzero: the stream size is known now (no lossless chunks)
   uint64_t gap_off;     // zero padding between the chunk table and the first chunk
   uint32_t gap_len;
@@ -77,8 +95,8 @@ struct PrologueParams {
   uint64_t *d_stream_bytes;
   // zero padding bytes of the payload sections
   uint8_t *payload;
-  uint64_t pad_off[6];
-  uint32_t pad_len[6];
+  uint64_t pad_off[kSections];
+  uint32_t pad_len[kSections];
 };
 
 struct LosslessParams {
@@ -97,13 +115,15 @@ struct LosslessParams {
   int64_t skip_ticket;     // test hook: this ticket does not publish
   uint32_t poll_limit;
   uint32_t fused_offsets;  // decode: the decoder checks the table and computes the chunk offsets itself
-  uint8_t header[KVC_HEADER_BYTES];  // decode: expected header
+  uint32_t header_bytes;   // the chunk table starts here
+  uint8_t header[kMaxHeaderBytes];  // decode: expected header (header_bytes of it)
 };
 
 // Launchers (return cudaError_t as int).  `occ_grid` = resident-grid size to use.
-int launch_quantize(const QuantParams &p, const TmaMaps *maps, int sm_count, void *stream, uint64_t *launches,
-                    const char **name);
-int launch_dequantize(const QuantParams &p, int sm_count, void *stream, uint64_t *launches, const char **name);
+int launch_quantize(const QuantParams &p, const TmaMaps *maps, const WidthTable *widths, int sm_count, void *stream,
+                    uint64_t *launches, const char **name);
+int launch_dequantize(const QuantParams &p, const WidthTable *widths, int sm_count, void *stream, uint64_t *launches,
+                      const char **name);
 int launch_prologue(const PrologueParams &p, void *stream);
 int launch_lossless_encode(const LosslessParams &p, int sm_count, void *stream);
 int launch_decode_prepare(const LosslessParams &p, void *stream);

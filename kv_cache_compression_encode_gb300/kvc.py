@@ -20,11 +20,13 @@ F16, BF16 = 1, 2
 AXIS_OVER_TOKENS, AXIS_OVER_CHANNELS = 0, 1
 ST_TUPL, ST_BIT, ST_DELTA, ST_RZE = 1, 2, 3, 4
 MAX_STAGES, MAX_LAYERS, HEADER_BYTES = 4, 256, 64
+PROFILE_V1_SIZE, MAX_MAP_ENTRIES = 40, 2048
 
 EXPORTS = ["kvc_plan", "kvc_plan_destroy", "kvc_workspace_bytes", "kvc_max_stream_bytes", "kvc_payload_bytes",
            "kvc_section", "kvc_num_chunks", "kvc_encode", "kvc_decode", "kvc_quantize", "kvc_lossless_encode",
            "kvc_lossless_decode", "kvc_dequantize", "kvc_query", "kvc_status_str", "kvc_launch_count",
-           "kvc_timing_enable", "kvc_timing_read", "kvc_debug_lookback", "kvc_lossless_encode_noalloc"]
+           "kvc_timing_enable", "kvc_timing_read", "kvc_debug_lookback", "kvc_lossless_encode_noalloc",
+           "kvc_header_bytes"]
 
 
 class KvcError(RuntimeError):
@@ -42,7 +44,8 @@ class Profile(C.Structure):
                 ("bits_k", C.c_uint8), ("bits_v", C.c_uint8), ("group_k", C.c_uint16), ("group_v", C.c_uint16),
                 ("axis_k", C.c_uint8), ("axis_v", C.c_uint8), ("n_stages", C.c_uint8), ("reserved0", C.c_uint8),
                 ("stages", Stage * MAX_STAGES), ("chunk_bytes", C.c_uint32), ("reserved1", C.c_uint32),
-                ("hadamard_seed", C.c_uint64)]
+                ("hadamard_seed", C.c_uint64), ("token_delta", C.c_uint8), ("reserved2", C.c_uint8 * 7),
+                ("bits_map_k", C.c_void_p), ("bits_map_v", C.c_void_p)]
 
 
 class Shape(C.Structure):
@@ -61,7 +64,7 @@ class Timing(C.Structure):
     _fields_ = [("kernel", C.c_char_p), ("ms", C.c_float)]
 
 
-assert C.sizeof(Profile) == 40 and C.sizeof(Shape) == 48 and C.sizeof(KV) == 24
+assert C.sizeof(Profile) == 64 and C.sizeof(Shape) == 48 and C.sizeof(KV) == 24
 
 _lock = threading.Lock()
 _lib = None
@@ -106,6 +109,7 @@ def load(build_if_missing: bool = True):
             "kvc_timing_read": (C.c_int, [P, C.POINTER(Timing), C.c_int]),
             "kvc_debug_lookback": (st, [P, C.c_int64, C.c_uint32]),
             "kvc_lossless_encode_noalloc": (st, [P, vp, vp, sz, vp, vp, vp]),
+            "kvc_header_bytes": (sz, [P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -132,9 +136,18 @@ def _check(status: int, what: str):
 # ----------------------------------------------------------------------------
 def make_profile(*, smooth_keys=True, hadamard=False, bits_k=4, bits_v=4, group_k=64, group_v=64,
                  axis_k=AXIS_OVER_TOKENS, axis_v=AXIS_OVER_CHANNELS, stages=(), chunk_bytes=16384,
-                 seed=0x5EED) -> Profile:
+                 seed=0x5EED, token_delta=False, bits_map_k=None, bits_map_v=None) -> Profile:
+    """bits_map_k / bits_map_v: optional [layers][kv_heads] code widths (kept alive by
+    the returned profile, copied by kvc_plan); token_delta: the anchor-token delta."""
     p = Profile()
     p.struct_size = C.sizeof(Profile)
+    p.token_delta = int(bool(token_delta))
+    p._maps = []
+    for name, m in (("bits_map_k", bits_map_k), ("bits_map_v", bits_map_v)):
+        if m is not None:
+            arr = (C.c_uint8 * len(_flat(m)))(*_flat(m))
+            p._maps.append(arr)
+            setattr(p, name, C.cast(arr, C.c_void_p).value)
     p.smooth_keys, p.hadamard = int(bool(smooth_keys)), int(bool(hadamard))
     p.bits_k, p.bits_v, p.group_k, p.group_v = bits_k, bits_v, group_k, group_v
     p.axis_k, p.axis_v = axis_k, axis_v
@@ -144,6 +157,16 @@ def make_profile(*, smooth_keys=True, hadamard=False, bits_k=4, bits_v=4, group_
     p.chunk_bytes = chunk_bytes
     p.hadamard_seed = seed
     return p
+
+
+def _flat(m):
+    out = []
+    for row in m:
+        if hasattr(row, "__iter__"):
+            out.extend(int(x) for x in row)
+        else:
+            out.append(int(row))
+    return out
 
 
 def make_shape(layers, tokens, kv_heads, head_dim, dtype, page_size=0, num_pages=0, token_stride=0,
@@ -218,6 +241,10 @@ class Plan:
     @property
     def n_chunks(self) -> int:
         return self.lib.kvc_num_chunks(self.handle)
+
+    @property
+    def header_bytes(self) -> int:
+        return self.lib.kvc_header_bytes(self.handle)
 
     @property
     def launches(self) -> int:

@@ -46,10 +46,19 @@ WORKLOADS = {
 
 
 def profile_kwargs(smooth_keys=True, hadamard=False, bits_k=4, bits_v=4, group_k=64, group_v=64,
-                   stages=(), chunk_bytes=16384, axis_k=0, axis_v=1, seed=HADAMARD_SEED):
+                   stages=(), chunk_bytes=16384, axis_k=0, axis_v=1, seed=HADAMARD_SEED, **v2):
+    """v2: optional token_delta, bits_map_k, bits_map_v (format-v2 profile fields)."""
     return dict(smooth_keys=smooth_keys, hadamard=hadamard, bits_k=bits_k, bits_v=bits_v, group_k=group_k,
                 group_v=group_v, axis_k=axis_k, axis_v=axis_v, stages=tuple(stages), chunk_bytes=chunk_bytes,
-                seed=seed)
+                seed=seed, **v2)
+
+
+def mixhq_map(layers, kv_heads, retrieval=(0, 5), hi=8, lo=2):
+    """A head-wise width map in the manner of MixHQ ("KVServe" §5.1): the heads listed
+    as retrieval heads keep `hi` bits in every layer, the streaming heads get `lo`.
+    Which heads are retrieval heads is the caller's labelling (a fixed synthetic
+    choice here; scoring heads needs a model)."""
+    return [[hi if h in retrieval else lo for h in range(kv_heads)] for _ in range(layers)]
 
 
 PROFILES = {
@@ -61,6 +70,15 @@ PROFILES = {
     "llama8b_32k": profile_kwargs(True, False, 2, 2, 32, 32, LC_PIPELINE),
     # Hadamard + 8-bit group 128; the decode side is the headline
     "llama70b": profile_kwargs(True, True, 8, 8, 128, 128, LC_PIPELINE),
+}
+
+# Format-v2 variants of the Llama-8B workload: head-wise mixed precision (two
+# retrieval heads of eight at 8 bits, the rest at 2, for K and V) and the token
+# delta on top of the llama8b profile.
+V2_PROFILES = {
+    "llama8b_mixhq": profile_kwargs(True, True, 4, 4, 128, 128, LC_PIPELINE, bits_map_k=mixhq_map(32, 8),
+                                    bits_map_v=mixhq_map(32, 8)),
+    "llama8b_delta": profile_kwargs(True, True, 4, 4, 128, 128, FULL_PIPELINE, token_delta=True),
 }
 
 

@@ -47,8 +47,10 @@ def test_struct_layouts_match_c(tmp_path):
 #include "{HEADER}"
 int main(void) {{
   printf("%zu %zu %zu %zu\\n", sizeof(kvc_profile), sizeof(kvc_shape), sizeof(kvc_kv), sizeof(kvc_timing));
-  printf("%zu %zu %zu %zu %zu\\n", offsetof(kvc_profile, group_k), offsetof(kvc_profile, stages),
-         offsetof(kvc_profile, chunk_bytes), offsetof(kvc_profile, hadamard_seed), offsetof(kvc_profile, n_stages));
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %d\\n", offsetof(kvc_profile, group_k), offsetof(kvc_profile, stages),
+         offsetof(kvc_profile, chunk_bytes), offsetof(kvc_profile, hadamard_seed), offsetof(kvc_profile, n_stages),
+         offsetof(kvc_profile, token_delta), offsetof(kvc_profile, bits_map_k), offsetof(kvc_profile, bits_map_v),
+         KVC_PROFILE_V1_SIZE);
   printf("%zu %zu %zu\\n", offsetof(kvc_shape, num_pages), offsetof(kvc_shape, token_stride),
          offsetof(kvc_shape, page_stride));
   return 0;
@@ -60,7 +62,9 @@ int main(void) {{
                                                     C.sizeof(kvc.Timing)]
     P = kvc.Profile
     assert [int(x) for x in lines[1].split()] == [P.group_k.offset, P.stages.offset, P.chunk_bytes.offset,
-                                                    P.hadamard_seed.offset, P.n_stages.offset]
+                                                    P.hadamard_seed.offset, P.n_stages.offset, P.token_delta.offset,
+                                                    P.bits_map_k.offset, P.bits_map_v.offset, kvc.PROFILE_V1_SIZE]
+    assert P.token_delta.offset == kvc.PROFILE_V1_SIZE  # the v2 fields extend the v1 struct
     S = kvc.Shape
     assert [int(x) for x in lines[2].split()] == [S.num_pages.offset, S.token_stride.offset, S.page_stride.offset]
 
@@ -75,6 +79,13 @@ CASES = [
     (dict(bits_k=3, bits_v=2, group_k=32, group_v=64, axis_k=1, axis_v=0, stages=((4, 4),), chunk_bytes=1024),
      (2, 77, 3)),
     (dict(bits_k=4, bits_v=4, group_k=64, group_v=64, stages=((1, 8), (4, 1))), (1, 0, 8)),
+    # format v2: token delta; per-(layer, head) widths (both axes); both
+    (dict(bits_k=4, bits_v=4, group_k=128, group_v=128, hadamard=True, token_delta=True,
+          stages=((1, 8), (2, 8), (3, 1), (4, 2))), (4, 300, 8)),
+    (dict(bits_k=4, bits_v=4, group_k=64, group_v=32, bits_map_k=[[2, 3, 4, 8]] * 3, bits_map_v=[[8, 8, 2, 2]] * 3,
+          stages=((1, 8), (4, 2)), chunk_bytes=4096), (3, 200, 4)),
+    (dict(bits_k=4, bits_v=4, group_k=32, group_v=64, smooth_keys=False, axis_k=1, axis_v=0,
+          bits_map_k=[[2, 8]] * 5, token_delta=True), (5, 129, 2)),
 ]
 
 
@@ -89,7 +100,8 @@ def test_plan_layout_equals_oracle_layout(lib, oracle, kw, geom):
     assert plan.payload_bytes == lay.payload_bytes
     assert plan.max_stream_bytes == lay.max_stream_bytes
     assert plan.n_chunks == lay.n_chunks
-    for i in range(6):
+    assert plan.header_bytes == lay.header_bytes
+    for i in range(8):
         assert plan.section(i) == (lay.off[i], lay.size[i])
     assert plan.workspace_bytes >= 256 + 8 * plan.n_chunks + (plan.payload_bytes if kw.get("stages") else 0)
     plan.close()
@@ -109,6 +121,39 @@ def test_plan_rejects_bad_profiles(lib, bad, status):
     kw.update(bad)
     with pytest.raises(kvc.KvcError) as e:
         kvc.Plan(kvc.make_profile(**kw), kvc.make_shape(1, 16, 1, 128, kvc.BF16))
+    assert e.value.status == status
+
+
+def test_plan_accepts_the_v1_profile_struct(lib, oracle):
+    """A caller built against the 40-byte profile (before the format-v2 fields) gets
+    the same plan as one passing the full struct with the v2 fields unset."""
+    full = kvc.make_profile(bits_k=3, bits_v=4, group_k=64, group_v=32, hadamard=True, stages=((1, 8), (4, 2)))
+    v1 = kvc.make_profile(bits_k=3, bits_v=4, group_k=64, group_v=32, hadamard=True, stages=((1, 8), (4, 2)))
+    v1.struct_size = kvc.PROFILE_V1_SIZE
+    v1.token_delta = 1            # beyond the v1 size: must be ignored
+    shape = kvc.make_shape(2, 100, 3, 128, kvc.BF16)
+    a, b = kvc.Plan(full, shape), kvc.Plan(v1, shape)
+    assert (a.payload_bytes, a.header_bytes, a.max_stream_bytes) == (b.payload_bytes, b.header_bytes,
+                                                                     b.max_stream_bytes)
+    assert b.section(6) == (b.payload_bytes, 0)
+    bad = kvc.make_profile()
+    bad.struct_size = 44
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.Plan(bad, shape)
+    assert e.value.status == kvc.KVC_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,geom,status", [
+    (dict(bits_map_k=[[2, 5]]), (1, 16, 2), kvc.KVC_ERR_INVALID_ARG),            # width 5
+    (dict(bits_map_v=[[4] * 8] * 257), (257, 16, 8), kvc.KVC_ERR_INVALID_ARG),  # too many layers anyway
+    (dict(bits_map_k=[[4] * 64] * 33), (33, 16, 64), kvc.KVC_ERR_UNSUPPORTED),  # > 2048 map entries
+    (dict(token_delta=True, smooth_keys=True, axis_k=1), (1, 16, 2), kvc.KVC_ERR_UNSUPPORTED),
+    (dict(bits_map_k=[[2, 4]], smooth_keys=True, axis_k=1), (1, 16, 2), kvc.KVC_ERR_UNSUPPORTED),
+])
+def test_plan_rejects_bad_v2_profiles(lib, kw, geom, status):
+    L, T, H = geom
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.Plan(kvc.make_profile(**kw), kvc.make_shape(L, T, H, 128, kvc.BF16))
     assert e.value.status == status
 
 

@@ -1,7 +1,8 @@
 """Full-size parity: the five workloads at their real sizes, in the configuration
 the benchmark times (default 16 KiB chunks, all layers in one call).
 
-* tiny, llama8b, llama8b_32k, llama70b: the whole stream and the whole
+* tiny, llama8b, llama8b_32k, llama70b, and the format-v2 variants of llama8b
+  (head-wise mixed widths; token delta): the whole stream and the whole
   reconstruction equal the oracle's, byte for byte.
 * paged8b_128k (48 profiles, 17 GB of KV each): every run is encoded on the GPU
   through the paged gather; the payload slices of two sampled layers per profile
@@ -17,7 +18,7 @@ import torch
 
 from kv_cache_compression_encode_gb300 import kvc, synth
 from kv_cache_compression_encode_gb300.codec import Codec
-from kv_cache_compression_encode_gb300.workloads import PROFILES, WORKLOADS, paged_sweep
+from kv_cache_compression_encode_gb300.workloads import PROFILES, V2_PROFILES, WORKLOADS, paged_sweep
 from oracle import oracle as O
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -36,10 +37,11 @@ def _bits(tensors):
     return [synth.to_bits_numpy(t) for t in tensors]
 
 
-@pytest.mark.parametrize("name", ["tiny", "llama8b", "llama8b_32k", "llama70b"])
+@pytest.mark.parametrize("name", ["tiny", "llama8b", "llama8b_32k", "llama70b", "llama8b_mixhq", "llama8b_delta"])
 def test_workload_stream_and_reconstruction(name):
-    w = WORKLOADS[name]
-    prof = PROFILES[name]
+    # the format-v2 variants run on the Llama-8B workload
+    w = WORKLOADS[name if name in WORKLOADS else "llama8b"]
+    prof = PROFILES[name] if name in PROFILES else V2_PROFILES[name]
     dk, do = _dt(w)
     k, v = [], []
     for l in range(w.layers):
