@@ -119,14 +119,35 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------- workload
+def workload_and_profile(name: str):
+    """A workload name, or a format-v2 variant of the Llama-8B workload (V2_PROFILES)."""
+    from kv_cache_compression_encode_gb300.workloads import PROFILES, V2_PROFILES, WORKLOADS
+
+    if name in V2_PROFILES:
+        return WORKLOADS["llama8b"], V2_PROFILES[name]
+    return WORKLOADS[name], PROFILES[name]
+
+
+def json_profile(prof: dict) -> dict:
+    out = {}
+    for k_, v_ in prof.items():
+        if k_ == "stages":
+            out[k_] = [list(x) for x in v_]
+        elif k_.startswith("bits_map"):
+            rows = [list(map(int, r)) for r in v_]
+            # one row repeated for every layer is written once
+            out[k_] = f"{len(rows)} layers x {rows[0]}" if all(r == rows[0] for r in rows) else rows
+        else:
+            out[k_] = v_
+    return out
+
+
 def workload_setup(name: str, device):
     import torch
 
     from kv_cache_compression_encode_gb300 import kvc, synth
-    from kv_cache_compression_encode_gb300.workloads import PROFILES, WORKLOADS
 
-    w = WORKLOADS[name]
-    prof = PROFILES[name]
+    w, prof = workload_and_profile(name)
     k, v = [], []
     for l in range(w.layers):
         a, b = synth.layer_kv(w.dist, l, w.tokens, w.kv_heads, w.head_dim, w.dtype, w.seed, device)
@@ -140,9 +161,9 @@ def workload_setup(name: str, device):
 def kernel_bytes(plan, w, name: str, stream_bytes: int) -> int:
     """Algorithmic bytes one launch of `name` must move (read + write)."""
     raw_tensor = w.layers * w.tokens * w.kv_heads * w.head_dim * 2
-    sec = [plan.section(i)[1] for i in range(6)]
-    k_out = sec[0] + sec[1] + sec[4] + sec[5]
-    v_out = sec[2] + sec[3]
+    sec = [plan.section(i)[1] for i in range(8)]
+    k_out = sec[0] + sec[1] + sec[4] + sec[5] + sec[6]
+    v_out = sec[2] + sec[3] + sec[7]
     Q = plan.payload_bytes
     table = 4 * plan.n_chunks
     return {
@@ -153,7 +174,9 @@ def kernel_bytes(plan, w, name: str, stream_bytes: int) -> int:
         "kvc_dec_ktile": raw_tensor + k_out,
         "kvc_dec_rows": raw_tensor + v_out,
         "kvc_lossless_enc": Q + stream_bytes,
+        "kvc_lossless_enc_fast": Q + stream_bytes,
         "kvc_lossless_dec": stream_bytes + Q,
+        "kvc_lossless_dec_fast": stream_bytes + Q,
         "kvc_decode_prepare": table + 8 * plan.n_chunks,
         "kvc_prologue": 64 + 8 * plan.n_chunks,
     }.get(name, 0)
@@ -288,6 +311,10 @@ def run_kvc(args):
         top_avg = per[top][0] / per[top][1]
         achieved = kernel_bytes(codec.plan, w, top, nbytes) / (top_avg * 1e-3) / 1e9
         e2e = run_e2e(codec, k, v, ok, ov, w, args, device) if args.e2e else None
+        # free this workload before the other configurations are set up
+        del k, v, ok, ov, stream_buf
+        torch.cuda.empty_cache()
+        configs = other_configs(args, device) if args.configs else None
         cpu = cpu_baseline(w, prof, args) if not args.no_cpu_baseline else None
         clocks = clk.summary()
         line = {
@@ -296,7 +323,7 @@ def run_kvc(args):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "layers": w.layers, "tokens": w.tokens, "kv_heads": w.kv_heads,
                        "head_dim": w.head_dim, "elt": w.dtype, "distribution": w.dist,
-                       "profile": {k_: (list(map(list, v_)) if k_ == "stages" else v_) for k_, v_ in prof.items()},
+                       "profile": json_profile(prof),
                        "raw_bytes": raw, "stream_bytes": nbytes, "compression_ratio": round(raw / nbytes, 4),
                        "step": "kvc_encode + kvc_decode", "l2": "inputs larger than L2 (no flush needed)",
                        "parallelism": f"replicas x{world}"},
@@ -307,11 +334,66 @@ def run_kvc(args):
                          else "fallback", "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": ncu_traffic(top, w.name)},
             "kernels": kernels,
+            "configs": configs,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": launches,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+OTHER_CONFIGS = ("llama70b", "llama8b_32k", "llama8b_mixhq", "llama8b_delta")
+
+
+def other_configs(args, device):
+    """Encode and decode GB/s of the other workloads (the 70B one is quoted on its
+    decode side) and of the format-v2 variants of Llama-8B: CUDA events on the
+    launching stream, after a checked round trip and warm-up, inputs larger than L2.
+    Reported beside `value`, which stays the metric's llama8b configuration."""
+    import torch
+
+    from kv_cache_compression_encode_gb300 import kvc
+    from kv_cache_compression_encode_gb300.codec import Codec
+
+    out = {}
+    cs = torch.cuda.current_stream(device)
+    for name in OTHER_CONFIGS:
+        w, prof, shape, k, v = workload_setup(name, device)
+        codec = Codec(kvc.make_profile(**prof), shape, device)
+        sbuf = codec.new_stream_buffer()
+        ok = [torch.empty_like(x) for x in k]
+        ov = [torch.empty_like(x) for x in v]
+        codec.encode(k, v, out=sbuf)
+        st, nbytes, _ = codec.query()
+        codec.decode(sbuf, nbytes, ok, ov)
+        st2, _, _ = codec.query()
+
+        def loop(fn, n):
+            for _ in range(3):
+                fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cs)
+            for _ in range(n):
+                fn()
+            b.record(cs)
+            b.synchronize()
+            return a.elapsed_time(b) / n
+
+        n = max(5, min(50, args.steps // 40))
+        enc_ms = loop(lambda: codec.encode(k, v, out=sbuf), n)
+        dec_ms = loop(lambda: codec.decode(sbuf, nbytes, ok, ov), n)
+        out[name] = {"workload": w.name, "raw_bytes": w.raw_bytes, "stream_bytes": nbytes,
+                     "compression_ratio": round(w.raw_bytes / nbytes, 4), "encode_ms": round(enc_ms, 4),
+                     "decode_ms": round(dec_ms, 4), "encode_gbs": round(w.raw_bytes / (enc_ms * 1e-3) / 1e9, 1),
+                     "decode_gbs": round(w.raw_bytes / (dec_ms * 1e-3) / 1e9, 1), "steps": n,
+                     "status": kvc.status_str(st) if st != kvc.KVC_OK else kvc.status_str(st2)}
+        if name == "llama70b":
+            out[name]["headline"] = "decode"
+        if prof.get("bits_map_k") is not None or prof.get("token_delta"):
+            out[name]["profile"] = json_profile(prof)
+        del k, v, ok, ov, sbuf, codec
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(codec, k, v, ok, ov, w, args, device):
@@ -438,14 +520,12 @@ def cpu_baseline(w, prof, args):
 
 def run_reference(args):
     """The reference arm for this build is the oracle itself, on the host cores."""
-    from kv_cache_compression_encode_gb300.workloads import PROFILES, WORKLOADS
     from oracle import oracle as O
 
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    w = WORKLOADS[args.workload]
-    prof = PROFILES[args.workload]
+    w, prof = workload_and_profile(args.workload)
     cores = len(os.sched_getaffinity(0))
     O.set_threads(cores)
     layers = oracle_layers(w, args)
@@ -482,7 +562,13 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-inputs", action="store_true")
+    ap.add_argument("--no-configs", dest="configs", action="store_false")
     args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != world:
+        # one process per GPU: N > 1 runs under torchrun, which sets WORLD_SIZE = N
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch N > 1 with "
+                         f"python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py --gpus {args.gpus}")
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

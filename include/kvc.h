@@ -268,6 +268,14 @@ int kvc_timing_read(kvc_plan_t *plan, kvc_timing *out, int max);
  * out after `poll_limit` polls and sets KVC_FLAG_TIMEOUT.  ticket < 0 disables it;
  * poll_limit = 0 restores the default limit. */
 kvc_status kvc_debug_lookback(kvc_plan_t *plan, int64_t ticket, uint32_t poll_limit);
+/* Measurement hook for comparing stage lists on equal terms ("Beyond Compression
+ * Ratio" §4.2, offline pipeline search): enable != 0 makes this plan's lossless
+ * encode and decode use the generic stage kernels even for the stage lists and
+ * chunk sizes that have a fast kernel (TUPL_8 [BIT_8] [DELTA_1] RZE_1/2, chunks of
+ * 4, 8, 12 or 16 KiB).  Streams are identical either way.  Measurements name the
+ * launches kvc_lossless_enc / kvc_lossless_dec (generic) or kvc_lossless_enc_fast /
+ * kvc_lossless_dec_fast. */
+kvc_status kvc_debug_generic_stages(kvc_plan_t *plan, int enable);
 
 #ifdef __cplusplus
 }

@@ -57,6 +57,7 @@ struct kvc_plan_s {
   // test hooks
   int64_t skip_ticket;
   uint32_t poll_limit;
+  bool generic_stages;
 };
 
 static constexpr uint32_t kDefaultPollLimit = 1u << 22;
@@ -374,6 +375,12 @@ extern "C" int kvc_timing_read(kvc_plan_t *plan, kvc_timing *out, int max) {
   return n;
 }
 
+extern "C" kvc_status kvc_debug_generic_stages(kvc_plan_t *plan, int enable) {
+  if (!plan) return KVC_ERR_INVALID_ARG;
+  plan->generic_stages = enable != 0;
+  return KVC_OK;
+}
+
 extern "C" kvc_status kvc_debug_lookback(kvc_plan_t *plan, int64_t ticket, uint32_t poll_limit) {
   if (!plan) return KVC_ERR_INVALID_ARG;
   plan->skip_ticket = ticket < 0 ? -1 : ticket;
@@ -562,6 +569,7 @@ static void fill_lossless(kvc_plan_s *P, LosslessParams &lp, void *ws) {
   lp.ctrl = ctrl_of(ws);
   lp.skip_ticket = P->skip_ticket;
   lp.poll_limit = P->poll_limit;
+  lp.generic_only = P->generic_stages ? 1u : 0u;
   lp.header_bytes = P->header_bytes;
   memcpy(lp.header, P->header, P->header_bytes);
 }
@@ -583,7 +591,7 @@ static kvc_status lossless_encode_impl(kvc_plan_s *P, const uint8_t *Q, void *d_
   lp.d_stream_bytes = d_stream_bytes;
   Bracket br(P, st);
   const int rc = launch_lossless_encode(lp, P->sm_count, st);
-  br.done("kvc_lossless_enc");
+  br.done(lossless_encode_is_fast(lp) ? "kvc_lossless_enc_fast" : "kvc_lossless_enc");
   if (P->n_chunks) P->launches++;
   return cuda_status(rc);
 }
@@ -662,7 +670,7 @@ static kvc_status lossless_decode_impl(kvc_plan_s *P, const void *d_stream, size
   }
   Bracket br(P, st);
   const int rc = launch_lossless_decode(lp, P->sm_count, st);
-  br.done("kvc_lossless_dec");
+  br.done(lossless_decode_is_fast(lp) ? "kvc_lossless_dec_fast" : "kvc_lossless_dec");
   if (P->n_chunks) P->launches++;
   return cuda_status(rc);
 }

@@ -116,6 +116,7 @@ struct LosslessParams {
   uint32_t poll_limit;
   uint32_t fused_offsets;  // decode: the decoder checks the table and computes the chunk offsets itself
   uint32_t header_bytes;   // the chunk table starts here
+  uint32_t generic_only;   // measurement hook: the generic stage kernels even where a fast one exists
   uint8_t header[kMaxHeaderBytes];  // decode: expected header (header_bytes of it)
 };
 
@@ -131,5 +132,9 @@ int launch_lossless_decode(const LosslessParams &p, int sm_count, void *stream);
 // Whether launch_lossless_decode can take the prepare step into the decoder for
 // this table size (nothing else needs to run first except the status reset).
 bool lossless_decode_fusable(const LosslessParams &p, int sm_count);
+// Whether the encoder / decoder launch for these parameters takes the fast path
+// (worker/publisher encoder; fast chunk decode), for naming measurements.
+bool lossless_encode_is_fast(const LosslessParams &p);
+bool lossless_decode_is_fast(const LosslessParams &p);
 
 }  // namespace kvc

@@ -1522,7 +1522,7 @@ static size_t fast_smem(uint32_t cb) { return (1 + kRing) * ((size_t)cb + 64) + 
 int launch_lossless_encode(const LosslessParams &p, int sm_count, void *stream) {
   if (p.n_chunks == 0) return 0;
   FastSpec f;
-  if (fast_spec(p, f)) {
+  if (!p.generic_only && fast_spec(p, f)) {
     const size_t smem = fast_smem(p.chunk_bytes);
     cudaError_t e = cudaFuncSetAttribute(kvc_lossless_enc_fast, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
@@ -1545,6 +1545,16 @@ int launch_lossless_encode(const LosslessParams &p, int sm_count, void *stream) 
   if (blocks > p.n_chunks) blocks = p.n_chunks;
   kvc_lossless_enc<<<(unsigned)blocks, LT, smem, (cudaStream_t)stream>>>(p);
   return (int)cudaGetLastError();
+}
+
+bool lossless_encode_is_fast(const LosslessParams &p) {
+  FastSpec f;
+  return p.n_chunks != 0 && !p.generic_only && fast_spec(p, f);
+}
+
+bool lossless_decode_is_fast(const LosslessParams &p) {
+  FastSpec f;
+  return p.n_chunks != 0 && p.n_stages != 0 && !p.generic_only && fast_spec(p, f);
 }
 
 int launch_decode_prepare(const LosslessParams &p, void *stream) {
@@ -1575,7 +1585,7 @@ int launch_lossless_decode(const LosslessParams &p, int sm_count, void *stream) 
   const uint64_t blocks = decode_blocks(p, sm_count);
   if (blocks == 0) return (int)cudaErrorInvalidValue;
   FastSpec f;
-  if (!fast_spec(p, f)) f = FastSpec{0, 0, 0, 0};  // rze_w == 0: generic stages for every chunk
+  if (p.generic_only || !fast_spec(p, f)) f = FastSpec{0, 0, 0, 0};  // rze_w == 0: generic stages for every chunk
   kvc_lossless_dec<<<(unsigned)blocks, LT, smem, (cudaStream_t)stream>>>(p, f);
   return (int)cudaGetLastError();
 }

@@ -26,7 +26,7 @@ EXPORTS = ["kvc_plan", "kvc_plan_destroy", "kvc_workspace_bytes", "kvc_max_strea
            "kvc_section", "kvc_num_chunks", "kvc_encode", "kvc_decode", "kvc_quantize", "kvc_lossless_encode",
            "kvc_lossless_decode", "kvc_dequantize", "kvc_query", "kvc_status_str", "kvc_launch_count",
            "kvc_timing_enable", "kvc_timing_read", "kvc_debug_lookback", "kvc_lossless_encode_noalloc",
-           "kvc_header_bytes"]
+           "kvc_header_bytes", "kvc_debug_generic_stages"]
 
 
 class KvcError(RuntimeError):
@@ -110,6 +110,7 @@ def load(build_if_missing: bool = True):
             "kvc_debug_lookback": (st, [P, C.c_int64, C.c_uint32]),
             "kvc_lossless_encode_noalloc": (st, [P, vp, vp, sz, vp, vp, vp]),
             "kvc_header_bytes": (sz, [P]),
+            "kvc_debug_generic_stages": (st, [P, C.c_int]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -314,6 +315,10 @@ def kvc_timing_read(plan: Plan, max_records: int = 4096):
     arr = (Timing * max_records)()
     n = plan.lib.kvc_timing_read(plan.handle, arr, max_records)
     return [(arr[i].kernel.decode(), arr[i].ms) for i in range(n)]
+
+
+def kvc_debug_generic_stages(plan: Plan, enable: bool):
+    _check(plan.lib.kvc_debug_generic_stages(plan.handle, int(bool(enable))), "kvc_debug_generic_stages")
 
 
 def kvc_debug_lookback(plan: Plan, ticket: int, poll_limit: int = 0):

@@ -7,8 +7,10 @@ the benchmark times (default 16 KiB chunks, all layers in one call).
 * paged8b_128k (48 profiles, 17 GB of KV each): every run is encoded on the GPU
   through the paged gather; the payload slices of two sampled layers per profile
   equal the oracle's (run on those layers through the same block table), the
-  GPU lossless round trip returns the payload, and two profiles are compared on
-  the whole stream.
+  GPU lossless round trip returns the payload, and four profiles (2, 3 and 8
+  bits; groups 32, 64 and 128) are compared on the whole stream; one profile is
+  decoded at full size and scattered through the block table, and sampled layers
+  equal the oracle's reconstruction.
 """
 import os
 
@@ -92,7 +94,8 @@ def paged_kv():
 
 
 SWEEP = paged_sweep()
-FULL_STREAM = {"b2g32_lc", "b8g128h_lc"}
+# whole streams against the oracle: 2-, 3- and 8-bit, groups of 32, 64 and 128, Hadamard on and off
+FULL_STREAM = {"b2g32_lc", "b8g128h_lc", "b3g64h_lc", "b3g32_lc"}
 
 
 @pytest.mark.parametrize("idx", range(len(SWEEP)), ids=[n for n, _ in SWEEP])
@@ -139,3 +142,42 @@ def test_paged_sweep(paged_kv, idx):
                               [synth.to_bits_numpy(x) for x in v], bt.numpy())
             assert fo == 0 and so.size == nbytes
             assert np.array_equal(sg[:nbytes].cpu().numpy(), so)
+
+
+@pytest.mark.parametrize("name", ["b4g128h_lc", "b3g64_lc"])
+def test_paged_decode_scatter_full_size(paged_kv, name):
+    """Full-size decode through the 131072-token block table: every page the table
+    maps is written, and two sampled layers equal the oracle's reconstruction of
+    the same payload through the same table."""
+    prof = dict(SWEEP)[name]
+    w, k, v, bt, n_pages = paged_kv
+    P = w.page_size
+    shape = kvc.make_shape(w.layers, w.tokens, w.kv_heads, w.head_dim, kvc.BF16, page_size=P, num_pages=n_pages,
+                           page_stride=P * w.kv_heads * w.head_dim * 2)
+    codec = Codec(kvc.make_profile(**prof), shape)
+    btd = bt.cuda()
+    sg = codec.encode(k, v, btd)
+    st, nbytes, flags = codec.query()
+    assert st == kvc.KVC_OK and flags == 0
+    ok = [torch.full_like(x, 0).view(torch.int16).fill_(0x7E7E).view(x.dtype) for x in k]
+    ov = [torch.full_like(x, 0).view(torch.int16).fill_(0x7E7E).view(x.dtype) for x in v]
+    codec.decode(sg, nbytes, ok, ov, btd)
+    st, _, flags = codec.query()
+    assert st == kvc.KVC_OK and flags == 0
+    del sg
+    layers = [5, 26]
+    oprof = O.make_profile(**prof)
+    oshape = O.make_shape(len(layers), w.tokens, w.kv_heads, w.head_dim, 2, page_size=P,
+                          page_stride=P * w.kv_heads * w.head_dim * 2)
+    Qo, fo = O.quantize(oprof, oshape, [synth.to_bits_numpy(k[l]) for l in layers],
+                        [synth.to_bits_numpy(v[l]) for l in layers], bt.numpy())
+    assert fo == 0
+    rk = [np.zeros_like(synth.to_bits_numpy(k[l])) for l in layers]
+    rv = [np.zeros_like(synth.to_bits_numpy(v[l])) for l in layers]
+    O.dequantize(oprof, oshape, Qo, rk, rv, bt.numpy())
+    for j, l in enumerate(layers):
+        assert np.array_equal(synth.to_bits_numpy(ok[l]), rk[j]), f"K layer {l}"
+        assert np.array_equal(synth.to_bits_numpy(ov[l]), rv[j]), f"V layer {l}"
+    # the table is a permutation of every page: no canary may survive anywhere
+    for t in ok + ov:
+        assert not bool((t.view(torch.int16) == 0x7E7E).all(dim=-1).any())

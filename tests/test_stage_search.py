@@ -59,3 +59,22 @@ def test_search_on_a_quantized_payload():
         assert codec.query()[1] == c.stream_bytes
     front = [c for c in cands if c.pareto]
     assert front and min(c.stream_bytes for c in cands) == min(c.stream_bytes for c in front)
+    assert any(c.pareto_generic for c in cands)
+    # kernels named per candidate: the pages' pipeline at 4 KiB chunks has the fast pair, RZE_4 lists do not
+    lc = [c for c in cands if c.stages == ((TUPL, 8), (BIT, 8), (RZE, 2))][0]
+    assert (lc.enc_kernel, lc.dec_kernel) == ("kvc_lossless_enc_fast", "kvc_lossless_dec_fast")
+    assert lc.enc_ms_generic > 0 and lc.dec_ms_generic > 0
+    for c in cands:
+        if c.stages[-1] == (RZE, 4):
+            assert (c.enc_kernel, c.dec_kernel) == ("kvc_lossless_enc", "kvc_lossless_dec")
+    # every candidate's stream equals the oracle's lossless encode of the same payload
+    from oracle import oracle as O
+    Qh = payload[:n].cpu().numpy()
+    ok_shape = O.make_shape(L, T, H, 128, 2)
+    for c in cands:
+        so = O.lossless_encode(O.make_profile(**{**prof, "stages": c.stages}), ok_shape, Qh)
+        codec = Codec(kvc.make_profile(**{**prof, "stages": c.stages}), shape)
+        kvc.kvc_debug_generic_stages(codec.plan, True)
+        sg = codec.lossless_encode(payload)
+        st, nb, _ = codec.query()
+        assert st == kvc.KVC_OK and nb == so.size and np.array_equal(sg[:nb].cpu().numpy(), so), c.stages
