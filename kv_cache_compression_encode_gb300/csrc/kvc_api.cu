@@ -189,10 +189,6 @@ extern "C" kvc_status kvc_plan(const kvc_profile *profile_in, const kvc_shape *s
 
   const bool mixed = profile->bits_map_k || profile->bits_map_v;
   const uint64_t n_lh = (uint64_t)s.layers * s.kv_heads;
-  // the format-v2 features are built into the key-tile and row kernels; smoothed
-  // keys grouped over channels (the generic tile kernels) stay format v1
-  if ((mixed || profile->token_delta) && profile->smooth_keys && profile->axis_k == KVC_AXIS_OVER_CHANNELS)
-    return KVC_ERR_UNSUPPORTED;
   if (mixed && n_lh > KVC_MAX_MAP_ENTRIES) return KVC_ERR_UNSUPPORTED;
   if (mixed)
     for (int t = 0; t < 2; t++) {

@@ -47,7 +47,7 @@ __device__ __forceinline__ uint32_t width_of(const WidthsArg<MIXED> &W, uint32_t
 
 constexpr int kThreads = 256;
 constexpr int kTS = 144;  // floats per shared-memory tile row (128 + 16: conflict-free row and column access)
-constexpr size_t kTileSmem = (size_t)(128 * kTS + 2 * 8 * 128 + 2 * 128) * sizeof(float);
+constexpr size_t kTileSmem = (size_t)(128 * kTS + 2 * 8 * 128 + 3 * 128) * sizeof(float);
 
 // ---------------------------------------------------------------------------
 // rows: encode.  Two lanes own a row (token, head): lane half h holds channels
@@ -615,13 +615,49 @@ __device__ __forceinline__ void tile_row_store(float *Y, int r, int part, const 
 // ---------------------------------------------------------------------------
 // tile: encode
 // ---------------------------------------------------------------------------
-template <int BITS, bool HAD>
-__global__ void __launch_bounds__(kThreads) kvc_enc_tile(const QuantParams P) {
+// Per-token groups of one row part (32 channels) of the tile kernel's row pass:
+// parameters, codes, packing, one record store (and the metadata word by the
+// group's first part).
+template <int BITS>
+__device__ __forceinline__ void tile_row_groups(const QuantParams &P, const float (&v)[32], int part, int gl,
+                                                bool store, uint8_t *rec, size_t R, uint32_t &flags) {
+  float mn = v[0], mx = v[0];
+#pragma unroll
+  for (int i = 1; i < 32; i++) {
+    mn = fminf(mn, v[i]);
+    mx = fmaxf(mx, v[i]);
+  }
+  if (gl >= 2) {
+    mn = fminf(mn, __shfl_xor_sync(kFull, mn, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+  }
+  if (gl >= 4) {
+    mn = fminf(mn, __shfl_xor_sync(kFull, mn, 2));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+  }
+  float s, z, rr;
+  uint32_t fl = 0;
+  const uint32_t meta = quant_params<BITS>(mn, mx, s, z, rr, fl);
+  uint32_t q[32], wds[BITS];
+#pragma unroll
+  for (int i = 0; i < 32; i++) q[i] = quant_code<BITS>(v[i], z, s, rr);
+  pack32<BITS>(q, wds);
+  if (store) {
+    flags |= fl;
+    store_words<BITS>(rec + 4 * BITS * part, wds);
+    if ((part & (gl - 1)) == 0)
+      *reinterpret_cast<uint32_t *>(P.meta + (R * (kHeadDim / P.group) + part / gl) * 4) = meta;
+  }
+}
+
+template <int BITS, bool HAD, bool DELTA = false, bool MIXED = false>
+__global__ void __launch_bounds__(kThreads) kvc_enc_tile(const QuantParams P, const __grid_constant__ WidthsArg<MIXED> W) {
   extern __shared__ float4 smem_f4[];
   float *Y = reinterpret_cast<float *>(smem_f4);  // [128][kTS]
   float *red = Y + 128 * kTS;                     // [2][8][128]
   float *mu_s = red + 2 * 8 * 128;                // [128]
   float *inv_s = mu_s + 128;                      // [128]
+  float *anc_s = inv_s + 128;                     // [128] token delta: the block's anchor row
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool bf16 = P.g.bf16 != 0;
   const uint32_t H = P.g.H, T = P.g.T, n_sb = P.n_sb;
@@ -652,6 +688,20 @@ __global__ void __launch_bounds__(kThreads) kvc_enc_tile(const QuantParams P) {
     for (int i = 0; i < 8; i++) {
       unpack8(w[i], bf16, x[i]);
       if (!all_finite8(x[i])) flags |= KVC_FLAG_NONFINITE;
+    }
+    if constexpr (DELTA) {  // every row minus the block's first row (the anchor), whose bits are kept
+      if (rg == 0) {
+#pragma unroll
+        for (int j = 0; j < 8; j++) anc_s[8 * c8 + j] = x[0][j];
+        *reinterpret_cast<uint4 *>(P.anchors + (((size_t)lh * n_sb + sb) * kHeadDim + 8 * c8) * 2) = w[0];
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        const float a = anc_s[8 * c8 + j];
+#pragma unroll
+        for (int i = 0; i < 8; i++) x[i][j] = __fsub_rn(x[i][j], a);
+      }
     }
 
     if (P.smooth) {
@@ -732,33 +782,18 @@ __global__ void __launch_bounds__(kThreads) kvc_enc_tile(const QuantParams P) {
           scale_all(v, hadamard_scale());
         }
         if (P.axis == KVC_AXIS_OVER_CHANNELS) {
-          float mn = v[0], mx = v[0];
-#pragma unroll
-          for (int i = 1; i < 32; i++) {
-            mn = fminf(mn, v[i]);
-            mx = fmaxf(mx, v[i]);
-          }
-          if (gl >= 2) {
-            mn = fminf(mn, __shfl_xor_sync(kFull, mn, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-          }
-          if (gl >= 4) {
-            mn = fminf(mn, __shfl_xor_sync(kFull, mn, 2));
-            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-          }
-          float s, z, rr;
-          uint32_t fl = 0;
-          const uint32_t meta = quant_params<BITS>(mn, mx, s, z, rr, fl);
-          uint32_t q[32], wds[BITS];
-#pragma unroll
-          for (int i = 0; i < 32; i++) q[i] = quant_code<BITS>(v[i], z, s, rr);
-          pack32<BITS>(q, wds);
-          if ((uint32_t)r < nvalid) {
-            flags |= fl;
-            const size_t R = ((size_t)l * T + t0 + r) * H + h;
-            store_words<BITS>(P.codes + R * (kHeadDim * BITS / 8) + 4 * BITS * part, wds);
-            if ((part & (gl - 1)) == 0)
-              *reinterpret_cast<uint32_t *>(P.meta + (R * (kHeadDim / P.group) + part / gl) * 4) = meta;
+          const bool store = (uint32_t)r < nvalid;
+          const size_t R = ((size_t)l * T + t0 + r) * H + h;
+          if constexpr (MIXED) {
+            uint8_t *rec = P.codes + (store ? row_code_offset<0, MIXED>(W, T, H, l, t0 + r, h, (uint32_t)R) : 0);
+            switch (width_of<MIXED>(W, lh)) {  // one width per (layer, head): uniform over the CTA
+              case 2: tile_row_groups<2>(P, v, part, gl, store, rec, R, flags); break;
+              case 3: tile_row_groups<3>(P, v, part, gl, store, rec, R, flags); break;
+              case 4: tile_row_groups<4>(P, v, part, gl, store, rec, R, flags); break;
+              default: tile_row_groups<8>(P, v, part, gl, store, rec, R, flags); break;
+            }
+          } else {
+            tile_row_groups<BITS>(P, v, part, gl, store, P.codes + R * (kHeadDim * BITS / 8), R, flags);
           }
         } else {
           tile_row_store(Y, r, part, v);
@@ -767,8 +802,9 @@ __global__ void __launch_bounds__(kThreads) kvc_enc_tile(const QuantParams P) {
       __syncthreads();
     }
 
-    // ---- D: columns -- groups of G tokens per channel
-    if (P.axis == KVC_AXIS_OVER_TOKENS) {
+    // ---- D: columns -- groups of G tokens per channel (format v1 only: groups
+    // over tokens otherwise run in the key-tile kernel)
+    if constexpr (!MIXED) if (P.axis == KVC_AXIS_OVER_TOKENS) {
       const int c = tid & 127, half = tid >> 7, pcol = phys_col(c);
       const uint32_t G = P.group;
       float gmn[2], gmx[2];
@@ -1673,13 +1709,28 @@ __global__ void __launch_bounds__(kKD, 3) kvc_dec_ktile(const QuantParams P, con
 // ---------------------------------------------------------------------------
 // tile: decode
 // ---------------------------------------------------------------------------
-template <int BITS, bool HAD>
-__global__ void __launch_bounds__(kThreads) kvc_dec_tile(const QuantParams P) {
+// Dequantized per-token groups of one row part (32 channels) of the tile decoder.
+template <int BITS>
+__device__ __forceinline__ void tile_row_dequant(const QuantParams &P, float (&v)[32], int part, int gl,
+                                                 const uint8_t *rec, size_t R) {
+  uint32_t wds[BITS], q[32];
+  load_words<BITS>(rec + 4 * BITS * part, wds);
+  const uint32_t meta = *reinterpret_cast<const uint32_t *>(P.meta + (R * (kHeadDim / P.group) + part / gl) * 4);
+  const float s = __half2float(__ushort_as_half((unsigned short)(meta & 0xffffu)));
+  const float z = __half2float(__ushort_as_half((unsigned short)(meta >> 16)));
+  unpack32<BITS>(wds, q);
+#pragma unroll
+  for (int i = 0; i < 32; i++) v[i] = __fmaf_rn((float)q[i], s, z);
+}
+
+template <int BITS, bool HAD, bool DELTA = false, bool MIXED = false>
+__global__ void __launch_bounds__(kThreads) kvc_dec_tile(const QuantParams P, const __grid_constant__ WidthsArg<MIXED> W) {
   if (P.check_corrupt && (*(volatile uint32_t *)P.status & KVC_FLAG_CORRUPT)) return;
   extern __shared__ float4 smem_f4[];
   float *Y = reinterpret_cast<float *>(smem_f4);
   float *mu_s = Y + 128 * kTS + 2 * 8 * 128;
   float *sc_s = mu_s + 128;
+  float *anc_s = sc_s + 128;  // token delta: the block's anchor row
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool bf16 = P.g.bf16 != 0;
   const uint32_t H = P.g.H, T = P.g.T, n_sb = P.n_sb;
@@ -1700,9 +1751,12 @@ __global__ void __launch_bounds__(kThreads) kvc_dec_tile(const QuantParams P) {
       mu_s[tid] = __half2float(__ushort_as_half(mub));
       sc_s[tid] = pow2i(e);
     }
+    if (DELTA && tid < 128)
+      anc_s[tid] = elt_to_f32(reinterpret_cast<const uint16_t *>(P.anchors)[((size_t)lh * n_sb + sb) * kHeadDim + tid], bf16);
 
     // ---- D': columns -- dequantize each channel's token groups into the tile
-    if (P.axis == KVC_AXIS_OVER_TOKENS) {
+    // (format v1 only: groups over tokens otherwise run in the key-tile kernel)
+    if constexpr (!MIXED) if (P.axis == KVC_AXIS_OVER_TOKENS) {
       const int c = tid & 127, half = tid >> 7, pcol = phys_col(c);
       const uint32_t G = P.group;
 #pragma unroll
@@ -1737,15 +1791,17 @@ __global__ void __launch_bounds__(kThreads) kvc_dec_tile(const QuantParams P) {
           for (int i = 0; i < 32; i++) v[i] = 0.0f;
           if ((uint32_t)r < nvalid) {
             const size_t R = ((size_t)l * T + t0 + r) * H + h;
-            uint32_t wds[BITS], q[32];
-            load_words<BITS>(P.codes + R * (kHeadDim * BITS / 8) + 4 * BITS * part, wds);
-            const uint32_t meta =
-                *reinterpret_cast<const uint32_t *>(P.meta + (R * (kHeadDim / P.group) + part / gl) * 4);
-            const float s = __half2float(__ushort_as_half((unsigned short)(meta & 0xffffu)));
-            const float z = __half2float(__ushort_as_half((unsigned short)(meta >> 16)));
-            unpack32<BITS>(wds, q);
-#pragma unroll
-            for (int i = 0; i < 32; i++) v[i] = __fmaf_rn((float)q[i], s, z);
+            if constexpr (MIXED) {
+              const uint8_t *rec = P.codes + row_code_offset<0, MIXED>(W, T, H, l, t0 + r, h, (uint32_t)R);
+              switch (width_of<MIXED>(W, lh)) {
+                case 2: tile_row_dequant<2>(P, v, part, gl, rec, R); break;
+                case 3: tile_row_dequant<3>(P, v, part, gl, rec, R); break;
+                case 4: tile_row_dequant<4>(P, v, part, gl, rec, R); break;
+                default: tile_row_dequant<8>(P, v, part, gl, rec, R); break;
+              }
+            } else {
+              tile_row_dequant<BITS>(P, v, part, gl, P.codes + R * (kHeadDim * BITS / 8), R);
+            }
           }
         } else {
           tile_row_load(Y, r, part, v);
@@ -1778,6 +1834,10 @@ __global__ void __launch_bounds__(kThreads) kvc_dec_tile(const QuantParams P) {
         if (P.smooth) {
 #pragma unroll
           for (int j = 0; j < 8; j++) xv[j] = __fmaf_rn(xv[j], s8[j], m8[j]);
+        }
+        if constexpr (DELTA) {
+#pragma unroll
+          for (int j = 0; j < 8; j++) xv[j] = __fadd_rn(xv[j], anc_s[8 * c8 + j]);
         }
         const uint64_t ro = row_offset(P.g, t0 + r);
         if (ro == ~0ull) flags |= KVC_FLAG_BAD_PAGE;
@@ -1818,9 +1878,7 @@ static int run_k(K kernel, size_t smem, int threads, int sm_count, void *stream,
 static bool use_tile(const QuantParams &p) { return p.smooth || p.axis == KVC_AXIS_OVER_TOKENS; }
 
 // The kernel for one tensor of one profile.  BITS is the code width of a uniform
-// launch (ignored, 0, when MIXED).  The generic tile kernels (smoothed keys
-// grouped over channels) exist for format v1 only; the plan refuses v2 profiles
-// that would need them.
+// launch (ignored, 0, when MIXED).
 template <int BITS, bool DELTA, bool MIXED>
 static int dispatch_v(const QuantParams &p, const TmaMaps *maps, const WidthsArg<MIXED> &W, bool enc, int sm,
                       void *st, const char **name) {
@@ -1844,16 +1902,14 @@ static int dispatch_v(const QuantParams &p, const TmaMaps *maps, const WidthsArg
     return run_k(k, kdec_smem<SB>(p.group, DELTA), kKD, sm, st, units, p, W);
   }
   if (tile) {
-    if constexpr (DELTA || MIXED) {
-      return (int)cudaErrorNotSupported;
-    } else {
-      if (enc) {
-        *name = "kvc_enc_tile";
-        return run_k(had ? kvc_enc_tile<BITS, true> : kvc_enc_tile<BITS, false>, kTileSmem, kThreads, sm, st, units, p);
-      }
-      *name = "kvc_dec_tile";
-      return run_k(had ? kvc_dec_tile<BITS, true> : kvc_dec_tile<BITS, false>, kTileSmem, kThreads, sm, st, units, p);
+    if (enc) {
+      *name = "kvc_enc_tile";
+      return run_k(had ? kvc_enc_tile<BITS, true, DELTA, MIXED> : kvc_enc_tile<BITS, false, DELTA, MIXED>, kTileSmem,
+                   kThreads, sm, st, units, p, W);
     }
+    *name = "kvc_dec_tile";
+    return run_k(had ? kvc_dec_tile<BITS, true, DELTA, MIXED> : kvc_dec_tile<BITS, false, DELTA, MIXED>, kTileSmem,
+                 kThreads, sm, st, units, p, W);
   }
   if (enc) {
     *name = "kvc_enc_rows";

@@ -147,8 +147,6 @@ def test_plan_accepts_the_v1_profile_struct(lib, oracle):
     (dict(bits_map_k=[[2, 5]]), (1, 16, 2), kvc.KVC_ERR_INVALID_ARG),            # width 5
     (dict(bits_map_v=[[4] * 8] * 257), (257, 16, 8), kvc.KVC_ERR_INVALID_ARG),  # too many layers anyway
     (dict(bits_map_k=[[4] * 64] * 33), (33, 16, 64), kvc.KVC_ERR_UNSUPPORTED),  # > 2048 map entries
-    (dict(token_delta=True, smooth_keys=True, axis_k=1), (1, 16, 2), kvc.KVC_ERR_UNSUPPORTED),
-    (dict(bits_map_k=[[2, 4]], smooth_keys=True, axis_k=1), (1, 16, 2), kvc.KVC_ERR_UNSUPPORTED),
 ])
 def test_plan_rejects_bad_v2_profiles(lib, kw, geom, status):
     L, T, H = geom

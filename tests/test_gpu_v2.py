@@ -38,8 +38,6 @@ def test_token_delta(had, dtype, bits, group):
 @pytest.mark.parametrize("smooth", [False, True])
 def test_token_delta_axes_and_paging(smooth):
     for axis_k, axis_v in ((0, 1), (0, 0), (1, 1)):
-        if smooth and axis_k == 1:
-            continue  # smoothed keys grouped over channels stay format v1
         prof = dict(smooth_keys=smooth, hadamard=True, bits_k=4, bits_v=3, group_k=64, group_v=32, axis_k=axis_k,
                     axis_v=axis_v, stages=LC, chunk_bytes=2048, token_delta=True)
         _run_full(U.Case(L=2, T=200, H=2, dtype="bf16", dist="llama_sink", seed=7, profile=prof))
@@ -57,10 +55,12 @@ def test_mixed_widths(T, had):
     _run_full(U.Case(L=L, T=T, H=H, dtype="bf16", dist="llama", seed=T, profile=prof))
 
 
-@pytest.mark.parametrize("axes", [(0, 0), (1, 1), (0, 1)])
-def test_mixed_widths_axes_with_delta(axes):
+@pytest.mark.parametrize("axes,smooth", [((0, 0), False), ((1, 1), False), ((0, 1), False), ((1, 1), True),
+                                         ((1, 0), True)])
+def test_mixed_widths_axes_with_delta(axes, smooth):
+    """Smoothed keys grouped over channels take the generic tile kernels."""
     L, H = 2, 4
-    prof = dict(smooth_keys=False, hadamard=True, bits_k=4, bits_v=4, group_k=32, group_v=64, axis_k=axes[0],
+    prof = dict(smooth_keys=smooth, hadamard=True, bits_k=4, bits_v=4, group_k=32, group_v=64, axis_k=axes[0],
                 axis_v=axes[1], bits_map_k=_map(L, H, 3), bits_map_v=_map(L, H, 4), stages=LC, chunk_bytes=1024,
                 token_delta=True)
     _run_full(U.Case(L=L, T=333, H=H, dtype="f16", dist="gauss_outlier", seed=9, profile=prof))
@@ -95,3 +95,12 @@ def test_stream_with_another_width_map_is_rejected():
     assert st == kvc.KVC_ERR_CORRUPT and flags & kvc.FLAG_CORRUPT
     for t in ok + ov:
         assert bool((t.view(torch.int16) == 0x1234).all())
+
+
+@pytest.mark.parametrize("delta", [False, True])
+def test_tile_kernels_mixed_widths_ragged(delta):
+    L, H = 3, 3
+    prof = dict(smooth_keys=True, hadamard=False, bits_k=4, bits_v=4, group_k=64, group_v=32, axis_k=1, axis_v=1,
+                bits_map_k=_map(L, H, 21), bits_map_v=_map(L, H, 22), stages=FULL, chunk_bytes=1024,
+                token_delta=delta)
+    _run_full(U.Case(L=L, T=201, H=H, dtype="bf16", dist="llama_sink", seed=13, profile=prof))
