@@ -64,6 +64,13 @@ __device__ __forceinline__ uint32_t pair_sign_mask(uint32_t sbits, int j) {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+__device__ __forceinline__ void cp_async16_q(void *smem, const void *gmem) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_q() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all_q() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ float2 unpack_pair(uint32_t u, bool bf16) {
   if (bf16) return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
   return __half22float2(*reinterpret_cast<const __half2 *>(&u));
@@ -409,14 +416,20 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_enc_rows(const QuantParams P,
 // rows: decode
 // ---------------------------------------------------------------------------
 constexpr size_t kDecRowsSmem = (size_t)(kThreads / 32) * 16 * 512;  // the row slots of kvc_dec_rows
+// Input staging of kvc_dec_rows (one code width): per warp two buffers of 16 rows'
+// codes (16 BITS bytes each) and metadata (up to 4 words each).
+__host__ __device__ constexpr size_t dec_rows_stage_bytes(int bits) { return (size_t)16 * (16 * bits + 16); }
+constexpr size_t dec_rows_smem(int bits) { return kDecRowsSmem + (size_t)(kThreads / 32) * 2 * dec_rows_stage_bytes(bits); }
 
 // One step of the rows decoder for the 16 rows of a warp: lanes rsub and
 // rsub + 16 reconstruct row (l, t, h) if `valid` (codes at `csrc`, metadata by R)
 // and send it out through the row's slot by one bulk copy.  Every lane runs it.
-template <int BITS, bool HAD, bool BF16, bool DELTA>
+// Codes at `csrc` and metadata words at `mrow`: global memory, or (STAGED) this
+// warp's shared staging buffer.
+template <int BITS, bool HAD, bool BF16, bool DELTA, bool STAGED = false>
 __device__ __forceinline__ void dec_row(const QuantParams &P, const uint32_t (*fsign)[64], uint4 *oslot, int half,
                                         bool valid, uint32_t l, uint32_t t, uint32_t h, uint32_t R,
-                                        const uint8_t *csrc, uint32_t &flags) {
+                                        const uint8_t *csrc, const uint32_t *mrow, uint32_t &flags) {
   const uint32_t G = P.group;
   const float sg = half ? -1.0f : 1.0f;  // stride 64: lower lane a + b, upper lane a - b = -b + a
   float2 w[32];  // channels 64 half + 2i, +1
@@ -430,23 +443,26 @@ __device__ __forceinline__ void dec_row(const QuantParams &P, const uint32_t (*f
       if constexpr ((2 * BITS) % 4 == 0) {
 #pragma unroll
         for (int k = 0; k < 2 * BITS; k += 4) {
-          const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src + 4 * k));
+          const uint4 *p4 = reinterpret_cast<const uint4 *>(src + 4 * k);
+          const uint4 a = STAGED ? *p4 : __ldg(p4);
           cw[k] = a.x; cw[k + 1] = a.y; cw[k + 2] = a.z; cw[k + 3] = a.w;
         }
       } else {
 #pragma unroll
         for (int k = 0; k < 2 * BITS; k += 2) {
-          const uint2 a = __ldg(reinterpret_cast<const uint2 *>(src + 4 * k));
+          const uint2 *p2 = reinterpret_cast<const uint2 *>(src + 4 * k);
+          const uint2 a = STAGED ? *p2 : __ldg(p2);
           cw[k] = a.x; cw[k + 1] = a.y;
         }
       }
-      const uint32_t *mp = reinterpret_cast<const uint32_t *>(P.meta);
       if (G == 32) {
-        const uint2 mm = __ldg(reinterpret_cast<const uint2 *>(mp + (size_t)R * 4 + 2 * half));
+        const uint2 *p2 = reinterpret_cast<const uint2 *>(mrow + 2 * half);
+        const uint2 mm = STAGED ? *p2 : __ldg(p2);
         m0 = mm.x;
         m1 = mm.y;
       } else {
-        m0 = m1 = __ldg(mp + (G == 64 ? (size_t)R * 2 + half : (size_t)R));
+        const uint32_t *p1 = mrow + (G == 64 ? half : 0);
+        m0 = m1 = STAGED ? *p1 : __ldg(p1);
       }
     }
 #pragma unroll
@@ -563,22 +579,60 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_dec_rows(const QuantParams P,
   RowPos pos;
   pos.init(R0, na, nb);
   const uint32_t da = dR % na, db = (dR / na) % nb, dl = dR / na / nb;
-  for (uint32_t it = it0; it < n_it; it += it_step) {
-    const bool valid = it * 16 + rsub < NR;
-    const uint32_t l = pos.l, t = MIXED ? pos.a : pos.b, h = MIXED ? pos.b : pos.a;
-    pos.advance(da, db, dl, na, nb);
-    const uint32_t R = (l * T + t) * H + h;
-    if constexpr (MIXED) {
+  if constexpr (MIXED) {
+    for (uint32_t it = it0; it < n_it; it += it_step) {
+      const bool valid = it * 16 + rsub < NR;
+      const uint32_t l = pos.l, t = pos.a, h = pos.b;
+      pos.advance(da, db, dl, na, nb);
+      const uint32_t R = (l * T + t) * H + h;
       const uint32_t b = valid ? width_of<MIXED>(W, l * H + h) : 0u;
       const uint8_t *csrc = valid ? P.codes + row_code_offset<0, MIXED>(W, T, H, l, t, h, R) : P.codes;
-      if (__any_sync(kFull, b == 2)) dec_row<2, HAD, BF16, DELTA>(P, fsign, oslot, half, b == 2, l, t, h, R, csrc, flags);
-      if (__any_sync(kFull, b == 3)) dec_row<3, HAD, BF16, DELTA>(P, fsign, oslot, half, b == 3, l, t, h, R, csrc, flags);
-      if (__any_sync(kFull, b == 4)) dec_row<4, HAD, BF16, DELTA>(P, fsign, oslot, half, b == 4, l, t, h, R, csrc, flags);
-      if (__any_sync(kFull, b == 8)) dec_row<8, HAD, BF16, DELTA>(P, fsign, oslot, half, b == 8, l, t, h, R, csrc, flags);
-    } else {
-      dec_row<BITS, HAD, BF16, DELTA>(P, fsign, oslot, half, valid, l, t, h, R,
-                                      P.codes + row_code_offset<BITS, MIXED>(W, T, H, l, t, h, R), flags);
+      const uint32_t *mrow = reinterpret_cast<const uint32_t *>(P.meta) + (valid ? (size_t)R * (kHeadDim / P.group) : 0);
+      if (__any_sync(kFull, b == 2)) dec_row<2, HAD, BF16, DELTA>(P, fsign, oslot, half, b == 2, l, t, h, R, csrc, mrow, flags);
+      if (__any_sync(kFull, b == 3)) dec_row<3, HAD, BF16, DELTA>(P, fsign, oslot, half, b == 3, l, t, h, R, csrc, mrow, flags);
+      if (__any_sync(kFull, b == 4)) dec_row<4, HAD, BF16, DELTA>(P, fsign, oslot, half, b == 4, l, t, h, R, csrc, mrow, flags);
+      if (__any_sync(kFull, b == 8)) dec_row<8, HAD, BF16, DELTA>(P, fsign, oslot, half, b == 8, l, t, h, R, csrc, mrow, flags);
     }
+  } else {
+    // One code width: a warp step's 16 rows are consecutive records, so their codes
+    // (16 x 16 BITS bytes) and metadata words are two contiguous runs.  They are
+    // copied into this warp's staging buffer one step ahead (cp.async), so the
+    // loads of step k + 1 are in flight while step k is reconstructed.
+    constexpr uint32_t kStage = (uint32_t)dec_rows_stage_bytes(BITS);
+    uint8_t *stage0 = reinterpret_cast<uint8_t *>(rows_out) + kDecRowsSmem + (size_t)warp * 2 * kStage;
+    const uint32_t wpr = kHeadDim / P.group;  // metadata words per row
+    auto issue = [&](uint32_t itn, uint8_t *buf) {
+      const uint32_t r0 = itn * 16;
+      const uint32_t nrow = NR - r0 < 16u ? NR - r0 : 16u;
+      const uint8_t *cg = P.codes + (size_t)r0 * (16 * BITS);
+      for (uint32_t u = lane; u < nrow * BITS; u += 32)  // 16-byte units, BITS per row
+        cp_async16_q(buf + 16 * u, cg + 16 * (size_t)u);
+      const uint32_t *mg = reinterpret_cast<const uint32_t *>(P.meta) + (size_t)r0 * wpr;
+      uint32_t *mb = reinterpret_cast<uint32_t *>(buf + 16 * 16 * BITS);
+      for (uint32_t u = lane; u < nrow * wpr; u += 32) {
+        const uint32_t d = (uint32_t)__cvta_generic_to_shared(mb + (u / wpr) * 4 + u % wpr);
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(mg + u) : "memory");
+      }
+      cp_async_commit_q();
+    };
+    uint32_t k = 0;
+    if (it0 < n_it) issue(it0, stage0);
+    for (uint32_t it = it0; it < n_it; it += it_step, k ^= 1u) {
+      const bool valid = it * 16 + rsub < NR;
+      const uint32_t l = pos.l, t = pos.b, h = pos.a;
+      pos.advance(da, db, dl, na, nb);
+      const uint32_t R = (l * T + t) * H + h;
+      if (it + it_step < n_it) issue(it + it_step, stage0 + (k ^ 1u) * kStage);
+      else cp_async_commit_q();  // an empty group keeps the wait count below uniform
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      __syncwarp();
+      const uint8_t *buf = stage0 + k * kStage;
+      dec_row<BITS, HAD, BF16, DELTA, true>(P, fsign, oslot, half, valid, l, t, h, R, buf + 16 * BITS * rsub,
+                                            reinterpret_cast<const uint32_t *>(buf + 16 * 16 * BITS) + 4 * rsub,
+                                            flags);
+      __syncwarp();  // every lane is done with this buffer before the next step refills it
+    }
+    cp_async_wait_all_q();
   }
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   if (flags) atomicOr(P.status, flags);
@@ -900,12 +954,6 @@ __device__ __forceinline__ uint32_t ycol4(uint32_t k, uint32_t r) {
   return k ^ (r & 1u) ^ (((k >> 3) & 3u) << 1) ^ (((r >> 5) & 3u) << 1);
 }
 
-__device__ __forceinline__ void cp_async16_q(void *smem, const void *gmem) {
-  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit_q() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all_q() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // The tile's two boxes by TMA (one thread): the mbarrier expects their 32 KiB.
 __device__ __forceinline__ void ktile_tma(const CUtensorMap *map, uint32_t h, uint32_t t0, uint8_t *stage,
@@ -1920,7 +1968,7 @@ static int dispatch_v(const QuantParams &p, const TmaMaps *maps, const WidthsArg
   *name = "kvc_dec_rows";
   auto k = had ? (bf ? kvc_dec_rows<BITS, true, true, DELTA, MIXED> : kvc_dec_rows<BITS, true, false, DELTA, MIXED>)
                : (bf ? kvc_dec_rows<BITS, false, true, DELTA, MIXED> : kvc_dec_rows<BITS, false, false, DELTA, MIXED>);
-  return run_k(k, kDecRowsSmem, kThreads, sm, st, units, p, W);
+  return run_k(k, MIXED ? kDecRowsSmem : dec_rows_smem(BITS), kThreads, sm, st, units, p, W);
 }
 
 // Format-v2 launches (kvc_quant_delta.cu: token delta, uniform widths;
