@@ -61,6 +61,12 @@ def ncu_traffic(kernel: str, workload: str):
         return None
     with open(path) as f:
         d = json.load(f)
+    if kernel in PAIRS:  # a pair's traffic: its two kernels' captures together
+        parts = [d.get(workload, {}).get(k) for k, pair in PAIRED.items() if pair == kernel]
+        parts = [r for r in parts if r]
+        if len(parts) != 2 or any(r.get("source_sha") != source_sha() for r in parts):
+            return None
+        return sum(r["dram_bytes_per_launch"] for r in parts)
     rec = d.get(workload, {}).get(kernel)
     if not rec or rec.get("source_sha") != source_sha():
         return None
@@ -158,8 +164,15 @@ def workload_setup(name: str, device):
     return w, prof, shape, k, v
 
 
+# the two kernels of a quantize / dequantize pair and the pair's timing name
+PAIRED = {"kvc_enc_ktile": "kvc_quantize_kv", "kvc_enc_tile": "kvc_quantize_kv", "kvc_enc_rows": "kvc_quantize_kv",
+          "kvc_dec_ktile": "kvc_dequantize_kv", "kvc_dec_tile": "kvc_dequantize_kv", "kvc_dec_rows": "kvc_dequantize_kv"}
+PAIRS = {"kvc_quantize_kv", "kvc_dequantize_kv"}
+
+
 def kernel_bytes(plan, w, name: str, stream_bytes: int) -> int:
-    """Algorithmic bytes one launch of `name` must move (read + write)."""
+    """Algorithmic bytes one launch of `name` must move (read + write); a pair moves
+    both tensors' bytes."""
     raw_tensor = w.layers * w.tokens * w.kv_heads * w.head_dim * 2
     sec = [plan.section(i)[1] for i in range(8)]
     k_out = sec[0] + sec[1] + sec[4] + sec[5] + sec[6]
@@ -179,6 +192,8 @@ def kernel_bytes(plan, w, name: str, stream_bytes: int) -> int:
         "kvc_lossless_dec_fast": stream_bytes + Q,
         "kvc_decode_prepare": table + 8 * plan.n_chunks,
         "kvc_prologue": 64 + 8 * plan.n_chunks,
+        "kvc_quantize_kv": 2 * raw_tensor + k_out + v_out,
+        "kvc_dequantize_kv": 2 * raw_tensor + k_out + v_out,
     }.get(name, 0)
 
 
@@ -267,7 +282,7 @@ def run_kvc(args):
 
     # ---- timed region
     launches0 = codec.plan.launches
-    kvc.kvc_timing_enable(codec.plan, True, capacity=args.steps * 8 + 64)
+    kvc.kvc_timing_enable(codec.plan, True, capacity=args.steps * 12 + 64)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(device)
@@ -283,7 +298,7 @@ def run_kvc(args):
         dist.barrier()
     total_ms = ev0.elapsed_time(ev1)
     launches = codec.plan.launches - launches0
-    recs = kvc.kvc_timing_read(codec.plan, args.steps * 8 + 64)
+    recs = kvc.kvc_timing_read(codec.plan, args.steps * 12 + 64)
     kvc.kvc_timing_enable(codec.plan, False)
     total_ms = max_over_ranks(total_ms, world, device)
     st, _, flags = codec.query()
@@ -293,20 +308,31 @@ def run_kvc(args):
     if rank == 0:
         ms_step = total_ms / args.steps
         value = job_throughput(raw, world, args.steps, total_ms)
-        # per-kernel live timings
+        # per-kernel live timings.  The K and V reconstruction kernels run side by
+        # side (two streams); their pair is also timed as one unit
+        # (kvc_dequantize_kv, from fork to join on the caller's stream), and the
+        # units that partition the step -- not the overlapping kernels -- give the
+        # shares and the roofline's dominant unit.
         per = {}
         for name, ms in recs:
             d = per.setdefault(name, [0.0, 0])
             d[0] += ms
             d[1] += 1
-        step_kernel_ms = sum(d[0] for d in per.values())
+        inner = {n for n in per if PAIRED.get(n) in per}  # kernels timed inside an overlapped pair
+        units = {n: d for n, d in per.items() if n not in inner}
+        step_kernel_ms = sum(d[0] for d in units.values())
         kernels = {}
         for name, (ms_sum, n) in sorted(per.items(), key=lambda kv: -kv[1][0]):
             avg = ms_sum / n
             b = kernel_bytes(codec.plan, w, name, nbytes)
-            kernels[name] = {"launches": n, "avg_ms": round(avg, 5), "share": round(ms_sum / step_kernel_ms, 4),
-                             "alg_bytes": b, "gbs": round(b / (avg * 1e-3) / 1e9, 1) if avg > 0 else None}
-        top = max(per.items(), key=lambda kv: kv[1][0])[0]
+            rec = {"launches": n, "avg_ms": round(avg, 5), "alg_bytes": b,
+                   "gbs": round(b / (avg * 1e-3) / 1e9, 1) if avg > 0 else None}
+            if name in units:
+                rec["share"] = round(ms_sum / step_kernel_ms, 4)
+            else:
+                rec["runs_beside"] = [o for o in PAIRED if o != name and o in per and PAIRED[o] == PAIRED[name]]
+            kernels[name] = rec
+        top = max(units.items(), key=lambda kv: kv[1][0])[0]
         peak, peak_src = peaks()
         top_avg = per[top][0] / per[top][1]
         achieved = kernel_bytes(codec.plan, w, top, nbytes) / (top_avg * 1e-3) / 1e9
@@ -332,7 +358,8 @@ def run_kvc(args):
             "roofline": {"bound": "hbm", "kernel": top, "achieved": round(achieved, 1), "peak": peak,
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                          else "fallback", "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": ncu_traffic(top, w.name)},
+                         "traffic": ncu_traffic(top, w.name),
+                         **({"kernels": sorted(n for n in per if PAIRED.get(n) == top)} if top in PAIRS else {})},
             "kernels": kernels,
             "configs": configs,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": launches,

@@ -121,10 +121,12 @@ struct LosslessParams {
 };
 
 // Launchers (return cudaError_t as int).  `occ_grid` = resident-grid size to use.
-int launch_quantize(const QuantParams &p, const TmaMaps *maps, const WidthTable *widths, int sm_count, void *stream,
-                    uint64_t *launches, const char **name);
-int launch_dequantize(const QuantParams &p, const WidthTable *widths, int sm_count, void *stream, uint64_t *launches,
-                      const char **name);
+// max_per_sm > 0 caps the resident CTAs per SM of the launch (so that a kernel
+// launched beside it on another stream finds room on every SM).
+int launch_quantize(const QuantParams &p, const TmaMaps *maps, const WidthTable *widths, int sm_count, int max_per_sm,
+                    void *stream, uint64_t *launches, const char **name);
+int launch_dequantize(const QuantParams &p, const WidthTable *widths, int sm_count, int max_per_sm, void *stream,
+                      uint64_t *launches, const char **name);
 int launch_prologue(const PrologueParams &p, void *stream);
 int launch_lossless_encode(const LosslessParams &p, int sm_count, void *stream);
 int launch_decode_prepare(const LosslessParams &p, void *stream);

@@ -7,13 +7,14 @@
 
 namespace kvc {
 
-int launch_quant_delta(const QuantParams &p, const TmaMaps *maps, bool enc, int sm, void *st, const char **name) {
+int launch_quant_delta(const QuantParams &p, const TmaMaps *maps, bool enc, int sm, int cap, void *st,
+                       const char **name) {
   const NoWidths W = {0u};
   switch (p.bits) {
-    case 2: return dispatch_v<2, true, false>(p, maps, W, enc, sm, st, name);
-    case 3: return dispatch_v<3, true, false>(p, maps, W, enc, sm, st, name);
-    case 4: return dispatch_v<4, true, false>(p, maps, W, enc, sm, st, name);
-    default: return dispatch_v<8, true, false>(p, maps, W, enc, sm, st, name);
+    case 2: return dispatch_v<2, true, false>(p, maps, W, enc, sm, cap, st, name);
+    case 3: return dispatch_v<3, true, false>(p, maps, W, enc, sm, cap, st, name);
+    case 4: return dispatch_v<4, true, false>(p, maps, W, enc, sm, cap, st, name);
+    default: return dispatch_v<8, true, false>(p, maps, W, enc, sm, cap, st, name);
   }
 }
 

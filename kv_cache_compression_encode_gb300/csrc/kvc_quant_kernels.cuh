@@ -1900,6 +1900,7 @@ __global__ void __launch_bounds__(kThreads) kvc_dec_tile(const QuantParams P, co
 // ---------------------------------------------------------------------------
 // launchers (instantiated by kvc_quant.cu and the format-v2 translation units)
 // ---------------------------------------------------------------------------
+
 template <typename K>
 static int resident_blocks(K kernel, size_t smem, int threads = kThreads) {
   int n = 0;
@@ -1908,15 +1909,17 @@ static int resident_blocks(K kernel, size_t smem, int threads = kThreads) {
 }
 
 // One launch of `kernel` with `smem` dynamic shared bytes on a grid of at most the
-// resident CTAs (and at most `work_units`).
+// resident CTAs (at most `cap` per SM when cap > 0) and at most `work_units`.
 template <typename K, typename... Args>
-static int run_k(K kernel, size_t smem, int threads, int sm_count, void *stream, uint64_t work_units,
+static int run_k(K kernel, size_t smem, int threads, int sm_count, int cap, void *stream, uint64_t work_units,
                  const Args &...args) {
   if (smem > 0) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
   }
-  uint64_t blocks = (uint64_t)sm_count * resident_blocks(kernel, smem, threads);
+  int per_sm = resident_blocks(kernel, smem, threads);
+  if (cap > 0 && per_sm > cap) per_sm = cap;
+  uint64_t blocks = (uint64_t)sm_count * per_sm;
   if (work_units < blocks) blocks = work_units;
   if (blocks == 0) return 0;
   kernel<<<(unsigned)blocks, threads, smem, (cudaStream_t)stream>>>(args...);
@@ -1929,7 +1932,7 @@ static bool use_tile(const QuantParams &p) { return p.smooth || p.axis == KVC_AX
 // launch (ignored, 0, when MIXED).
 template <int BITS, bool DELTA, bool MIXED>
 static int dispatch_v(const QuantParams &p, const TmaMaps *maps, const WidthsArg<MIXED> &W, bool enc, int sm,
-                      void *st, const char **name) {
+                      int cap, void *st, const char **name) {
   static const TmaMaps no_maps = {};
   const bool had = p.hadamard != 0, bf = p.g.bf16 != 0;
   const bool tile = use_tile(p);
@@ -1941,40 +1944,41 @@ static int dispatch_v(const QuantParams &p, const TmaMaps *maps, const WidthsArg
       *name = "kvc_enc_ktile";
       auto k = had ? (bf ? kvc_enc_ktile<BITS, true, true, DELTA, MIXED> : kvc_enc_ktile<BITS, true, false, DELTA, MIXED>)
                    : (bf ? kvc_enc_ktile<BITS, false, true, DELTA, MIXED> : kvc_enc_ktile<BITS, false, false, DELTA, MIXED>);
-      return run_k(k, kKtileSmem, kKT, sm, st, units, p, M, W);
+      return run_k(k, kKtileSmem, kKT, sm, cap, st, units, p, M, W);
     }
     *name = "kvc_dec_ktile";
     constexpr int SB = MIXED ? 8 : BITS;
     auto k = had ? (bf ? kvc_dec_ktile<BITS, true, true, DELTA, MIXED> : kvc_dec_ktile<BITS, true, false, DELTA, MIXED>)
                  : (bf ? kvc_dec_ktile<BITS, false, true, DELTA, MIXED> : kvc_dec_ktile<BITS, false, false, DELTA, MIXED>);
-    return run_k(k, kdec_smem<SB>(p.group, DELTA), kKD, sm, st, units, p, W);
+    return run_k(k, kdec_smem<SB>(p.group, DELTA), kKD, sm, cap, st, units, p, W);
   }
   if (tile) {
     if (enc) {
       *name = "kvc_enc_tile";
       return run_k(had ? kvc_enc_tile<BITS, true, DELTA, MIXED> : kvc_enc_tile<BITS, false, DELTA, MIXED>, kTileSmem,
-                   kThreads, sm, st, units, p, W);
+                   kThreads, sm, cap, st, units, p, W);
     }
     *name = "kvc_dec_tile";
     return run_k(had ? kvc_dec_tile<BITS, true, DELTA, MIXED> : kvc_dec_tile<BITS, false, DELTA, MIXED>, kTileSmem,
-                 kThreads, sm, st, units, p, W);
+                 kThreads, sm, cap, st, units, p, W);
   }
   if (enc) {
     *name = "kvc_enc_rows";
     auto k = had ? (bf ? kvc_enc_rows<BITS, true, true, DELTA, MIXED> : kvc_enc_rows<BITS, true, false, DELTA, MIXED>)
                  : (bf ? kvc_enc_rows<BITS, false, true, DELTA, MIXED> : kvc_enc_rows<BITS, false, false, DELTA, MIXED>);
-    return run_k(k, 0, kThreads, sm, st, units, p, W);
+    return run_k(k, 0, kThreads, sm, cap, st, units, p, W);
   }
   *name = "kvc_dec_rows";
   auto k = had ? (bf ? kvc_dec_rows<BITS, true, true, DELTA, MIXED> : kvc_dec_rows<BITS, true, false, DELTA, MIXED>)
                : (bf ? kvc_dec_rows<BITS, false, true, DELTA, MIXED> : kvc_dec_rows<BITS, false, false, DELTA, MIXED>);
-  return run_k(k, MIXED ? kDecRowsSmem : dec_rows_smem(BITS), kThreads, sm, st, units, p, W);
+  return run_k(k, MIXED ? kDecRowsSmem : dec_rows_smem(BITS), kThreads, sm, cap, st, units, p, W);
 }
 
 // Format-v2 launches (kvc_quant_delta.cu: token delta, uniform widths;
 // kvc_quant_mixed.cu: per-(layer, head) widths, with or without the delta).
-int launch_quant_delta(const QuantParams &p, const TmaMaps *maps, bool enc, int sm, void *st, const char **name);
-int launch_quant_mixed(const QuantParams &p, const TmaMaps *maps, const WidthTable *widths, bool enc, int sm,
+int launch_quant_delta(const QuantParams &p, const TmaMaps *maps, bool enc, int sm, int cap, void *st,
+                       const char **name);
+int launch_quant_mixed(const QuantParams &p, const TmaMaps *maps, const WidthTable *widths, bool enc, int sm, int cap,
                        void *st, const char **name);
 
 }  // namespace kvc

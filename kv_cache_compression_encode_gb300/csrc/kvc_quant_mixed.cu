@@ -10,10 +10,10 @@
 
 namespace kvc {
 
-int launch_quant_mixed(const QuantParams &p, const TmaMaps *maps, const WidthTable *widths, bool enc, int sm,
+int launch_quant_mixed(const QuantParams &p, const TmaMaps *maps, const WidthTable *widths, bool enc, int sm, int cap,
                        void *st, const char **name) {
-  return p.delta ? dispatch_v<0, true, true>(p, maps, *widths, enc, sm, st, name)
-                 : dispatch_v<0, false, true>(p, maps, *widths, enc, sm, st, name);
+  return p.delta ? dispatch_v<0, true, true>(p, maps, *widths, enc, sm, cap, st, name)
+                 : dispatch_v<0, false, true>(p, maps, *widths, enc, sm, cap, st, name);
 }
 
 }  // namespace kvc
