@@ -402,6 +402,20 @@ extern "C" kvc_status kvc_debug_generic_stages(kvc_plan_t *plan, int enable) {
   return KVC_OK;
 }
 
+extern "C" kvc_status kvc_debug_quotient_check(uint32_t seed, uint32_t rounds, unsigned long long *counts,
+                                               void *stream) {
+  if (!counts) return KVC_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned long long *d = nullptr;
+  if (cudaMalloc(&d, 3 * sizeof(unsigned long long)) != cudaSuccess) return KVC_ERR_CUDA;
+  bool ok = cudaMemsetAsync(d, 0, 3 * sizeof(unsigned long long), st) == cudaSuccess;
+  for (uint32_t i = 0; ok && i < rounds; i++) ok = kvc::launch_quotient_check(seed + i, d, st) == (int)cudaSuccess;
+  ok = ok && cudaMemcpyAsync(counts, d, 3 * sizeof(unsigned long long), cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
+  cudaFree(d);
+  return ok ? KVC_OK : KVC_ERR_CUDA;
+}
+
 extern "C" kvc_status kvc_debug_lookback(kvc_plan_t *plan, int64_t ticket, uint32_t poll_limit) {
   if (!plan) return KVC_ERR_INVALID_ARG;
   plan->skip_ticket = ticket < 0 ? -1 : ticket;

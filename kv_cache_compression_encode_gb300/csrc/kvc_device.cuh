@@ -154,7 +154,7 @@ __device__ __forceinline__ uint32_t quant_params(float mn, float mx, float &s, f
   const float v = __fdiv_rn(w, Qf);
   const uint32_t sb = saturate_f16(__half_as_ushort(__float2half_ru(v)), flags);
   s = __half2float(__ushort_as_half((unsigned short)sb));
-  r = __frcp_rn(s);
+  r = s == 0.0f ? 0.0f : __frcp_rn(s);  // 0: every code of the group is 0
   return sb | (zb << 16);
 }
 
@@ -328,43 +328,31 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a
 __device__ __forceinline__ float2 bcast2(float a) { return make_float2(a, a); }
 
 // ---------------------------------------------------------------------------
-// Branch-free codes for a pair.  d = (y - z)/s < 2^BITS, p = RN(RN(y - z) * RN(1/s))
-// lies within 2^(BITS-23) of d and RN(d) within 2^(BITS-25); rint(p) therefore
-// equals rint(RN(d)) whenever p is farther than 2^(BITS-22) from a half-integer.
-// rint(p) comes from adding 1.5 * 2^23 (round half to even); the code is the low
-// mantissa bits of that sum.  `bad` is raised for pairs near a half-integer, for
-// s = 0 (p not finite) -- the caller then takes the exact path.
+// Branch-free codes for a pair, from the correctly rounded quotient.  With
+// t = RN(y - z) >= 0, r = RN(1/s) and q = RN(t r) (within one ulp of t / s), the
+// residual e = t - q s is exact in one fma and RN(q + e r) is the correctly
+// rounded t / s: the quotient correction step of P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Develop. 34(1), 1990.  The step assumes nothing underflows; a quotient that can
+// round to code 1 or more has t >= s / 2 >= 2^-25 and a residual far above
+// 2^-126, and a smaller one gives code 0 either way.  rint comes from adding
+// 1.5 * 2^23 (round half to even); the code is the low mantissa bits of the sum.
+// r = 0 when s = 0 makes every code 0, as the rule says.  Valid for finite
+// y >= z and a finite s: a group with a saturated or non-finite parameter, where
+// the rule's clamp is needed, takes qexact instead.
 // ---------------------------------------------------------------------------
 constexpr float kRintMagic = 12582912.0f;  // 1.5 * 2^23
 
-template <int BITS>
-__device__ __forceinline__ float tie_threshold() {
-  return 0.5f - __int_as_float((uint32_t)(127 + BITS - 22) << 23);
+// The corrected quotients t / s of a pair (r2 = RN(1/s), ns2 = -s in both halves).
+__device__ __forceinline__ float2 qdiv2(float2 t, float2 r2, float2 ns2) {
+  const float2 q = mul2(t, r2);
+  const float2 e = __ffma2_rn(q, ns2, t);
+  return __ffma2_rn(e, r2, q);
 }
 
-// Returns the raw sums; the code of element e is (bits of u.e) & (2^BITS - 1).
-template <int BITS>
-__device__ __forceinline__ float2 qfast2(float2 y, float2 z2, float2 r2, bool &bad) {
-  const float2 t = sub2(y, z2);
-  const float2 p = mul2(t, r2);
-  const float2 u = add2(p, bcast2(kRintMagic));
-  const float2 k = sub2(u, bcast2(kRintMagic));
-  const float2 d = sub2(p, k);
-  const float thr = tie_threshold<BITS>();
-  bad |= !(fabsf(d.x) < thr) || !(fabsf(d.y) < thr);
-  return u;
-}
-
-// qfast2 that keeps the largest |p - rint(p)| seen in dm instead of a flag: the
-// pair is safe while dm < tie_threshold<BITS>() (a NaN dm fails that test too).
-__device__ __forceinline__ float2 qfast2m(float2 y, float2 z2, float2 r2, float &dm) {
-  const float2 t = sub2(y, z2);
-  const float2 p = mul2(t, r2);
-  const float2 u = add2(p, bcast2(kRintMagic));
-  const float2 k = sub2(u, bcast2(kRintMagic));
-  const float2 d = sub2(p, k);
-  dm = fmax3_n(fabsf(d.x), fabsf(d.y), dm);
-  return u;
+// Returns the sums of a pair; the code of a half is its low BITS bits.
+__device__ __forceinline__ float2 qsum2(float2 y, float2 z2, float2 r2, float2 ns2) {
+  return add2(qdiv2(sub2(y, z2), r2, ns2), bcast2(kRintMagic));
 }
 
 // The exact rule: clamp(rint_even(RN(RN(y - z) / s)), 0, 2^BITS - 1), 0 when s == 0.
@@ -376,7 +364,7 @@ __device__ __forceinline__ uint32_t qexact(float y, float z, float s) {
   return (uint32_t)k;
 }
 
-// Code bits of a qfast2 sum, already masked to BITS.
+// Code bits of a qsum2 sum, already masked to BITS.
 template <int BITS>
 __device__ __forceinline__ uint32_t code_of(float u) { return __float_as_uint(u) & ((1u << BITS) - 1u); }
 

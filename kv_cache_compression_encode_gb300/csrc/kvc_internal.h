@@ -120,6 +120,9 @@ struct LosslessParams {
   uint8_t header[kMaxHeaderBytes];  // decode: expected header (header_bytes of it)
 };
 
+// Self-check of the encoders' quotient step (one round, counts in device memory).
+int launch_quotient_check(uint32_t seed, unsigned long long *d_counts, void *stream);
+
 // Launchers (return cudaError_t as int).  `occ_grid` = resident-grid size to use.
 // max_per_sm > 0 caps the resident CTAs per SM of the launch (so that a kernel
 // launched beside it on another stream finds room on every SM).

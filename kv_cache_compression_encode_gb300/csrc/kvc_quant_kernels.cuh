@@ -151,7 +151,7 @@ __device__ __forceinline__ void codes_to_f2(const uint32_t (&w)[BITS], float2 (&
   for (int i = 0; i < 16; i++) q[i] = sub2(make_float2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1])), e2);
 }
 
-// Codes of 32 qfast2 sums (bits 0x4B400000 + code, the code in the low byte) into
+// Codes of 32 qsum2 sums (bits 0x4B400000 + code, the code in the low byte) into
 // BITS words, LSB first.  2 and 4 bits: the codes of a byte are gathered with
 // integer multiply-adds (the magic's low byte is 0, so the low byte of
 // u1 * 2^BITS + u0 is code0 | code1 << BITS), bytes into words by byte_perm.
@@ -296,15 +296,15 @@ __device__ __forceinline__ void enc_row(const QuantParams &P, const uint32_t (*s
     r1 = r0;
   }
   uint32_t wds[2 * BITS];
-  float dm = 0.0f;
   {
     const float2 za = bcast2(z0), ra = bcast2(r0), zb = bcast2(z1), rb = bcast2(r1);
+    const float2 na = bcast2(-s0), nb = bcast2(-s1);
 #pragma unroll
     for (int hh = 0; hh < 2; hh++) {  // codes 32 hh .. 32 hh + 31
       uint32_t u[32];
 #pragma unroll
       for (int i = 0; i < 16; i++) {
-        const float2 s2 = qfast2m(w[16 * hh + i], hh ? zb : za, hh ? rb : ra, dm);
+        const float2 s2 = qsum2(w[16 * hh + i], hh ? zb : za, hh ? rb : ra, hh ? nb : na);
         u[2 * i] = __float_as_uint(s2.x);
         u[2 * i + 1] = __float_as_uint(s2.y);
       }
@@ -314,7 +314,8 @@ __device__ __forceinline__ void enc_row(const QuantParams &P, const uint32_t (*s
       for (int k = 0; k < BITS; k++) wds[hh * BITS + k] = cw[k];
     }
   }
-  bool bad = f0 != 0 || f1 != 0 || !(dm < tie_threshold<BITS>());
+  // a saturated or non-finite group takes the exact rule
+  const bool bad = f0 != 0 || f1 != 0 || !finite2(mn0, mx0) || !finite2(mn1, mx1);
   if (__any_sync(kFull, bad)) {
     if (bad) {
 #pragma unroll
@@ -1077,35 +1078,37 @@ struct TilePos {
 };
 
 // D phase of kvc_enc_ktile for one (channel, 32-row quarter): the group
-// parameters from the group's minimum and maximum, 32 codes (exact division on a
-// near-tie or a saturated group, warp-wide), codes of rows past the end zeroed,
-// one store into the channel's record segment `dst` (and the metadata word at
-// `meta` by the quarter that starts the group).
+// parameters from the group's minimum and maximum, 32 codes from the correctly
+// rounded quotients (the exact rule with its clamp for a saturated or non-finite
+// group, warp-wide), codes of rows past the end zeroed, one store into the
+// channel's record segment `dst` (and the metadata word at `meta` by the quarter
+// that starts the group).
 template <int BITS>
 __device__ __forceinline__ void ktile_columns(const float (&v)[32], int nv, float mn, float mx, bool active,
                                               bool d_first, uint8_t *dst, uint8_t *meta, uint32_t &flags) {
   float sc = 0.0f, z = 0.0f, rr = 0.0f;
   uint32_t mword = 0, fl = 0;
+  bool finite = true;
   if (active) {
-    if (!finite2(mn, mx)) flags |= KVC_FLAG_NONFINITE;
+    finite = finite2(mn, mx);
+    if (!finite) flags |= KVC_FLAG_NONFINITE;
     mword = quant_params<BITS>(mn, mx, sc, z, rr, fl);
     flags |= fl;
   }
   uint32_t cw[BITS];
-  float dm = 0.0f;
   {
-    const float2 z2 = bcast2(z), r2 = bcast2(rr);
+    const float2 z2 = bcast2(z), r2 = bcast2(rr), ns2 = bcast2(-sc);
     uint32_t u[32];
 #pragma unroll
     for (int i = 0; i < 16; i++) {
-      const float2 s2 = qfast2m(make_float2(v[2 * i], v[2 * i + 1]), z2, r2, dm);
+      const float2 s2 = qsum2(make_float2(v[2 * i], v[2 * i + 1]), z2, r2, ns2);
       u[2 * i] = __float_as_uint(s2.x);
       u[2 * i + 1] = __float_as_uint(s2.y);
     }
     pack_sums32<BITS>(u, cw);
   }
-  // a near-tie or a saturated group takes the exact path
-  const bool bad = active && (fl != 0 || !(dm < tie_threshold<BITS>()));
+  // a saturated or non-finite group takes the exact rule
+  const bool bad = active && (fl != 0 || !finite);
   if (__any_sync(kFull, bad)) {
     if (bad) {
 #pragma unroll

@@ -26,7 +26,7 @@ EXPORTS = ["kvc_plan", "kvc_plan_destroy", "kvc_workspace_bytes", "kvc_max_strea
            "kvc_section", "kvc_num_chunks", "kvc_encode", "kvc_decode", "kvc_quantize", "kvc_lossless_encode",
            "kvc_lossless_decode", "kvc_dequantize", "kvc_query", "kvc_status_str", "kvc_launch_count",
            "kvc_timing_enable", "kvc_timing_read", "kvc_debug_lookback", "kvc_lossless_encode_noalloc",
-           "kvc_header_bytes", "kvc_debug_generic_stages"]
+           "kvc_header_bytes", "kvc_debug_generic_stages", "kvc_debug_quotient_check"]
 
 
 class KvcError(RuntimeError):
@@ -111,6 +111,7 @@ def load(build_if_missing: bool = True):
             "kvc_lossless_encode_noalloc": (st, [P, vp, vp, sz, vp, vp, vp]),
             "kvc_header_bytes": (sz, [P]),
             "kvc_debug_generic_stages": (st, [P, C.c_int]),
+            "kvc_debug_quotient_check": (st, [C.c_uint32, C.c_uint32, C.POINTER(C.c_ulonglong), vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -319,6 +320,13 @@ def kvc_timing_read(plan: Plan, max_records: int = 4096):
 
 def kvc_debug_generic_stages(plan: Plan, enable: bool):
     _check(plan.lib.kvc_debug_generic_stages(plan.handle, int(bool(enable))), "kvc_debug_generic_stages")
+
+
+def kvc_debug_quotient_check(seed: int = 0, rounds: int = 1, stream: int = 0):
+    """Returns (quotient mismatches for t >= 1e-30, code mismatches, dividends tested)."""
+    out = (C.c_ulonglong * 3)()
+    _check(load().kvc_debug_quotient_check(seed, rounds, out, stream or None), "kvc_debug_quotient_check")
+    return int(out[0]), int(out[1]), int(out[2])
 
 
 def kvc_debug_lookback(plan: Plan, ticket: int, poll_limit: int = 0):
