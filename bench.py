@@ -429,7 +429,8 @@ def run_e2e(codec, k, v, ok, ov, w, args, device):
     copies the stream in, decodes and copies the KV out.  Three requests are in
     flight, each on its own CUDA stream with its own plan, workspace and buffers
     (a serving process overlaps one request's uploads with others' downloads);
-    every step still moves all of its own bytes."""
+    every step still moves all of its own bytes.  `host_link` is each direction's
+    copy rate over the same buffers and the bound they set on this figure."""
     import torch
 
     from kv_cache_compression_encode_gb300.codec import Codec
@@ -487,9 +488,34 @@ def run_e2e(codec, k, v, ok, ov, w, args, device):
     run(n_steps)
     dt = (time.perf_counter() - t0) / n_steps
     ok_rt = all(torch.equal(a, b.to(a.device)) for L in lanes for a, b in zip(ok + ov, L.rk + L.rv))
+
+    # the host link on its own: each direction's rate over the same pinned buffers (all
+    # lanes copying at once), and the bound they put on this figure with both
+    # directions overlapped (each step moves counts["h2d"] up and counts["d2h"] down)
+    def one_way(up: bool):
+        reps = 2
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            for L in lanes:
+                with torch.cuda.stream(L.s):
+                    for d, h, r in zip(L.dk + L.dv, hk + hv, L.rk + L.rv):
+                        if up:
+                            d.copy_(h, non_blocking=True)
+                        else:
+                            r.copy_(d, non_blocking=True)
+        for L in lanes:
+            L.s.synchronize()
+        return reps * n_lanes * w.raw_bytes / (time.perf_counter() - t0) / 1e9
+
+    one_way(True)
+    h2d_gbs, d2h_gbs = one_way(True), one_way(False)
+    link_ms = max(counts["h2d"] / h2d_gbs, counts["d2h"] / d2h_gbs) / 1e6
     return {"value": round(w.raw_bytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": counts["h2d"],
             "d2h_bytes_per_step": counts["d2h"], "ms_per_step": round(dt * 1e3, 3), "steps": n_steps,
-            "requests_in_flight": n_lanes, "roundtrip_matches_device_path": bool(ok_rt)}
+            "requests_in_flight": n_lanes, "roundtrip_matches_device_path": bool(ok_rt),
+            "host_link": {"h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
+                          "bound_gbs": round(w.raw_bytes / link_ms / 1e6, 2)}}
 
 
 # ---------------------------------------------------------------------------- oracle
