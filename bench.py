@@ -429,24 +429,27 @@ def run_e2e(codec, k, v, ok, ov, w, args, device):
     copies the stream in, decodes and copies the KV out.  Three requests are in
     flight, each on its own CUDA stream with its own plan, workspace and buffers
     (a serving process overlaps one request's uploads with others' downloads);
-    every step still moves all of its own bytes.  `host_link` is each direction's
-    copy rate over the same buffers and the bound they set on this figure."""
+    every step still moves all of its own bytes.  Each request's K (and V) for all
+    layers sits in one contiguous buffer, host and device, whose per-layer views the
+    API takes, so that a direction's KV moves in one copy (a serving KV pool is laid
+    out so; many small copies run the link about 14% slower both ways).
+    `host_link` holds the copy rates over the same buffers (each direction alone,
+    both at once) and the bound they set on this figure."""
     import torch
 
     from kv_cache_compression_encode_gb300.codec import Codec
 
-    hk = [x.cpu().pin_memory() for x in k]
-    hv = [x.cpu().pin_memory() for x in v]
+    hK, hV = torch.stack(k).cpu().pin_memory(), torch.stack(v).cpu().pin_memory()
 
     class Lane:
         def __init__(self, c):
             self.codec = c
             self.s = torch.cuda.Stream(device)
-            self.rk = [torch.empty_like(x, device="cpu").pin_memory() for x in k]
-            self.rv = [torch.empty_like(x, device="cpu").pin_memory() for x in v]
+            self.rK, self.rV = torch.empty_like(hK).pin_memory(), torch.empty_like(hV).pin_memory()
+            self.rk, self.rv = list(self.rK.unbind(0)), list(self.rV.unbind(0))
             self.hs = torch.empty(c.plan.max_stream_bytes, dtype=torch.uint8).pin_memory()
-            self.dk = [torch.empty_like(x) for x in k]
-            self.dv = [torch.empty_like(x) for x in v]
+            self.dK, self.dV = torch.empty_like(hK, device=device), torch.empty_like(hV, device=device)
+            self.dk, self.dv = list(self.dK.unbind(0)), list(self.dV.unbind(0))
             self.sbuf = c.new_stream_buffer()
             self.rbuf = c.new_stream_buffer()
 
@@ -456,8 +459,8 @@ def run_e2e(codec, k, v, ok, ov, w, args, device):
 
     def front(L):  # inputs up, encode
         with torch.cuda.stream(L.s):
-            for d, h in zip(L.dk + L.dv, hk + hv):
-                d.copy_(h, non_blocking=True)
+            L.dK.copy_(hK, non_blocking=True)
+            L.dV.copy_(hV, non_blocking=True)
             L.codec.encode(L.dk, L.dv, out=L.sbuf)
 
     def back(L):  # size scalar to the host, stream down and up again, decode, KV down
@@ -466,8 +469,8 @@ def run_e2e(codec, k, v, ok, ov, w, args, device):
             L.hs[:n].copy_(L.sbuf[:n], non_blocking=True)
             L.rbuf[:n].copy_(L.hs[:n], non_blocking=True)  # the receiving side's upload
             L.codec.decode(L.rbuf, n, L.dk, L.dv)
-            for h, d in zip(L.rk + L.rv, L.dk + L.dv):
-                h.copy_(d, non_blocking=True)
+            L.rK.copy_(L.dK, non_blocking=True)
+            L.rV.copy_(L.dV, non_blocking=True)
         counts["h2d"] = w.raw_bytes + n
         counts["d2h"] = n + w.raw_bytes + 16
 
@@ -489,33 +492,36 @@ def run_e2e(codec, k, v, ok, ov, w, args, device):
     dt = (time.perf_counter() - t0) / n_steps
     ok_rt = all(torch.equal(a, b.to(a.device)) for L in lanes for a, b in zip(ok + ov, L.rk + L.rv))
 
-    # the host link on its own: each direction's rate over the same pinned buffers (all
-    # lanes copying at once), and the bound they put on this figure with both
-    # directions overlapped (each step moves counts["h2d"] up and counts["d2h"] down)
-    def one_way(up: bool):
+    # the host link on its own, over the same pinned buffers with all lanes copying at
+    # once: each direction alone, and both together (uploads on the lanes' streams,
+    # downloads on a second stream per lane); the bound they put on this figure
+    down = [torch.cuda.Stream(device) for _ in lanes]
+    srcK, srcV = torch.stack(k), torch.stack(v)  # downloads read these, which nothing writes meanwhile
+
+    def link(up: bool, dn: bool):
         reps = 2
         torch.cuda.synchronize(device)
         t0 = time.perf_counter()
         for _ in range(reps):
-            for L in lanes:
-                with torch.cuda.stream(L.s):
-                    for d, h, r in zip(L.dk + L.dv, hk + hv, L.rk + L.rv):
-                        if up:
+            for L, sd in zip(lanes, down):
+                for d, h, r, src in ((L.dK, hK, L.rK, srcK), (L.dV, hV, L.rV, srcV)):
+                    if up:
+                        with torch.cuda.stream(L.s):
                             d.copy_(h, non_blocking=True)
-                        else:
-                            r.copy_(d, non_blocking=True)
-        for L in lanes:
-            L.s.synchronize()
-        return reps * n_lanes * w.raw_bytes / (time.perf_counter() - t0) / 1e9
+                    if dn:
+                        with torch.cuda.stream(sd):
+                            r.copy_(src, non_blocking=True)
+        torch.cuda.synchronize(device)
+        return reps * n_lanes * w.raw_bytes * (int(up) + int(dn)) / (time.perf_counter() - t0) / 1e9
 
-    one_way(True)
-    h2d_gbs, d2h_gbs = one_way(True), one_way(False)
-    link_ms = max(counts["h2d"] / h2d_gbs, counts["d2h"] / d2h_gbs) / 1e6
+    link(True, False)
+    h2d_gbs, d2h_gbs, both_gbs = link(True, False), link(False, True), link(True, True)
+    link_ms = max(counts["h2d"] / h2d_gbs, counts["d2h"] / d2h_gbs, (counts["h2d"] + counts["d2h"]) / both_gbs) / 1e6
     return {"value": round(w.raw_bytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": counts["h2d"],
             "d2h_bytes_per_step": counts["d2h"], "ms_per_step": round(dt * 1e3, 3), "steps": n_steps,
             "requests_in_flight": n_lanes, "roundtrip_matches_device_path": bool(ok_rt),
             "host_link": {"h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
-                          "bound_gbs": round(w.raw_bytes / link_ms / 1e6, 2)}}
+                          "both_ways_gbs": round(both_gbs, 1), "bound_gbs": round(w.raw_bytes / link_ms / 1e6, 2)}}
 
 
 # ---------------------------------------------------------------------------- oracle
