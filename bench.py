@@ -426,7 +426,7 @@ def other_configs(args, device):
 def run_e2e(codec, k, v, ok, ov, w, args, device):
     """Same metric through the public API with host buffers: every step copies the
     KV from pinned host memory, encodes, reads the size and the stream back, then
-    copies the stream in, decodes and copies the KV out.  Three requests are in
+    copies the stream in, decodes and copies the KV out.  Three requests (--e2e-requests) are in
     flight, each on its own CUDA stream with its own plan, workspace and buffers
     (a serving process overlaps one request's uploads with others' downloads);
     every step still moves all of its own bytes.  Each request's K (and V) for all
@@ -453,7 +453,7 @@ def run_e2e(codec, k, v, ok, ov, w, args, device):
             self.sbuf = c.new_stream_buffer()
             self.rbuf = c.new_stream_buffer()
 
-    n_lanes = 3
+    n_lanes = args.e2e_requests
     lanes = [Lane(codec)] + [Lane(Codec(codec.profile, codec.shape, device)) for _ in range(n_lanes - 1)]
     counts = {"h2d": 0, "d2h": 0}
 
@@ -619,6 +619,7 @@ def main():
     ap.add_argument("--oracle-seconds", type=float, default=10.0)
     ap.add_argument("--reference-steps", type=int, default=3)
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--e2e-requests", type=int, default=3, help="requests in flight in the end-to-end run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-inputs", action="store_true")
     ap.add_argument("--no-configs", dest="configs", action="store_false")
