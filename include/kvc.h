@@ -276,17 +276,21 @@ kvc_status kvc_debug_lookback(kvc_plan_t *plan, int64_t ticket, uint32_t poll_li
  * launches kvc_lossless_enc / kvc_lossless_dec (generic) or kvc_lossless_enc_fast /
  * kvc_lossless_dec_fast. */
 kvc_status kvc_debug_generic_stages(kvc_plan_t *plan, int enable);
-/* Self-check of the encoders' quotient step (no plan).  The min-max rule codes
- * rint(RN(RN(y - z) / s)) ("Beyond Compression Ratio" §4.1, group-wise asymmetric
- * quantization; "KVServe" §5.1, KIVI-style min-max); the encoders form that
- * quotient as q = RN(t * RN(1/s)) corrected once by the exact residual t - q s
- * (Markstein's correction).  Each round tests every positive finite binary16
- * divisor s against 256 x 256 dividends t drawn from `seed + round` (uniform in
- * [0, 256 s), within 4 ulps of k s and of (k + 1/2) s for k < 256, and any normal
- * value below 2^17) and compares with the correctly rounded division.  Writes
- * counts[0] = quotients that differ for t >= 1e-30, counts[1] = codes that differ
- * (quotients below 4096), counts[2] = dividends tested; host array of 3.
- * Synchronizes `stream`; allocates 24 bytes of device memory for the call.
+/* Self-check of the encoders' two quotient steps (no plan).  The min-max rule
+ * ("Beyond Compression Ratio" §4.1, group-wise asymmetric quantization; "KVServe"
+ * §5.1, KIVI-style min-max) divides twice: the group scale s = fp16_up(RN(w / Q))
+ * with w = max - z and Q = 2^b - 1, and the code rint(RN(RN(y - z) / s)).  The
+ * encoders form both quotients as q = RN(t * RN(1/d)) corrected once by the exact
+ * residual t - q d (Markstein's correction).  Codes: each round tests every
+ * positive finite binary16 divisor s against 256 x 256 dividends t drawn from
+ * `seed + round` (uniform in [0, 256 s), within 4 ulps of k s and of (k + 1/2) s
+ * for k < 256, and any normal value below 2^17) and compares with the correctly
+ * rounded division: counts[0] = quotients that differ for t >= 1e-30, counts[1] =
+ * codes that differ (quotients below 4096), counts[2] = dividends tested.  Scales:
+ * every non-negative binary32 pattern w for b = 2, 3, 4, 8 (one pass, whatever
+ * `rounds`): counts[3] = quotients that differ for finite w >= 1e-30, counts[4] =
+ * binary16 scales that differ, counts[5] = patterns tested.  Host array of 6.
+ * Synchronizes `stream`; allocates 48 bytes of device memory for the call.
  * Returns KVC_ERR_INVALID_ARG for a null `counts`, KVC_ERR_CUDA on a CUDA error. */
 kvc_status kvc_debug_quotient_check(uint32_t seed, uint32_t rounds, unsigned long long *counts, void *stream);
 

@@ -406,11 +406,16 @@ extern "C" kvc_status kvc_debug_quotient_check(uint32_t seed, uint32_t rounds, u
                                                void *stream) {
   if (!counts) return KVC_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return KVC_ERR_CUDA;
   unsigned long long *d = nullptr;
-  if (cudaMalloc(&d, 3 * sizeof(unsigned long long)) != cudaSuccess) return KVC_ERR_CUDA;
-  bool ok = cudaMemsetAsync(d, 0, 3 * sizeof(unsigned long long), st) == cudaSuccess;
+  if (cudaMalloc(&d, 6 * sizeof(unsigned long long)) != cudaSuccess) return KVC_ERR_CUDA;
+  bool ok = cudaMemsetAsync(d, 0, 6 * sizeof(unsigned long long), st) == cudaSuccess;
   for (uint32_t i = 0; ok && i < rounds; i++) ok = kvc::launch_quotient_check(seed + i, d, st) == (int)cudaSuccess;
-  ok = ok && cudaMemcpyAsync(counts, d, 3 * sizeof(unsigned long long), cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  ok = ok && kvc::launch_range_check(d, sms, st) == (int)cudaSuccess;
+  ok = ok && cudaMemcpyAsync(counts, d, 6 * sizeof(unsigned long long), cudaMemcpyDeviceToHost, st) == cudaSuccess;
   ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
   cudaFree(d);
   return ok ? KVC_OK : KVC_ERR_CUDA;

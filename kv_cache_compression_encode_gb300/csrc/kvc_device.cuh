@@ -142,16 +142,33 @@ __device__ __forceinline__ uint32_t saturate_f16(uint32_t h, uint32_t &flags) {
   return h;
 }
 
+// RN(w / (2^BITS - 1)) for a group's range w >= 0, by the quotient correction step
+// of P. Markstein ("Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Develop. 34(1), 1990): with c = RN(1/Q) and q = RN(w c)
+// within one ulp of w / Q, the residual w - q Q is exact in one fma and RN(q + e c)
+// is the correctly rounded quotient, barring underflow.  Where the quotient is
+// below 2^-100 it may be off by an ulp, but every positive value there rounds up to
+// the same binary16 scale (2^-24), so the scale is unchanged.  An infinite or NaN
+// range takes w c, which is what the division gives.
+template <int BITS>
+__device__ __forceinline__ float range_div(float w) {
+  constexpr float Q = (float)((1u << BITS) - 1u);
+  constexpr float c = 1.0f / Q;  // correctly rounded at compile time
+  const float q = __fmul_rn(w, c);
+  const float e = __fmaf_rn(-q, Q, w);
+  const float d = __fmaf_rn(e, c, q);
+  return fabsf(w) <= 3.402823466e38f ? d : __fmul_rn(w, c);
+}
+
 template <int BITS>
 __device__ __forceinline__ uint32_t quant_params(float mn, float mx, float &s, float &z, float &r,
                                                  uint32_t &flags) {
-  const float Qf = (float)((1u << BITS) - 1u);
   mn = __fadd_rn(mn, 0.0f);  // a zero extreme counts as +0
   mx = __fadd_rn(mx, 0.0f);
   const uint32_t zb = saturate_f16(__half_as_ushort(__float2half_rd(mn)), flags);
   z = __half2float(__ushort_as_half((unsigned short)zb));
   const float w = __fsub_rn(mx, z);
-  const float v = __fdiv_rn(w, Qf);
+  const float v = range_div<BITS>(w);
   const uint32_t sb = saturate_f16(__half_as_ushort(__float2half_ru(v)), flags);
   s = __half2float(__ushort_as_half((unsigned short)sb));
   r = s == 0.0f ? 0.0f : __frcp_rn(s);  // 0: every code of the group is 0

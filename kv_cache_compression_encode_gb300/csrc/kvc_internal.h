@@ -120,8 +120,10 @@ struct LosslessParams {
   uint8_t header[kMaxHeaderBytes];  // decode: expected header (header_bytes of it)
 };
 
-// Self-check of the encoders' quotient step (one round, counts in device memory).
+// Self-checks of the encoders' quotient steps (counts in device memory): the codes'
+// quotients (one round of dividends) and the group scales' quotients (every pattern).
 int launch_quotient_check(uint32_t seed, unsigned long long *d_counts, void *stream);
+int launch_range_check(unsigned long long *d_counts, int sm_count, void *stream);
 
 // Launchers (return cudaError_t as int).  `occ_grid` = resident-grid size to use.
 // max_per_sm > 0 caps the resident CTAs per SM of the launch (so that a kernel

@@ -80,8 +80,40 @@ __global__ void __launch_bounds__(256) kvc_quotient_check(uint32_t seed, unsigne
   atomicAdd(counts + 2, nt);
 }
 
+// The group scale's quotient: range_div<BITS>(w) against __fdiv_rn(w, 2^BITS - 1)
+// for every non-negative binary32 bit pattern w (finite, infinite and NaN) and the
+// four widths.  counts[3]: quotients that differ for finite w >= 1e-30; counts[4]:
+// binary16 scales (rounded up) that differ, for any w; counts[5]: patterns tested.
+template <int BITS>
+__device__ __forceinline__ void rc_one(float w, unsigned long long &nq, unsigned long long &ns) {
+  const float a = __fdiv_rn(w, (float)((1u << BITS) - 1u)), b = range_div<BITS>(w);
+  if (w >= 1.0e-30f && fabsf(w) <= 3.402823466e38f && __float_as_uint(a) != __float_as_uint(b)) nq++;
+  if (__half_as_ushort(__float2half_ru(a)) != __half_as_ushort(__float2half_ru(b))) ns++;
+}
+
+__global__ void __launch_bounds__(256) kvc_range_check(unsigned long long *counts) {
+  unsigned long long nq = 0, ns = 0, nt = 0;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < 0x80000000u; u += stride) {
+    const float w = __uint_as_float(u);
+    rc_one<2>(w, nq, ns);
+    rc_one<3>(w, nq, ns);
+    rc_one<4>(w, nq, ns);
+    rc_one<8>(w, nq, ns);
+    nt++;
+  }
+  if (nq) atomicAdd(counts + 3, nq);
+  if (ns) atomicAdd(counts + 4, ns);
+  atomicAdd(counts + 5, nt);
+}
+
 int launch_quotient_check(uint32_t seed, unsigned long long *d_counts, void *stream) {
   kvc_quotient_check<<<0x7bff, 256, 0, (cudaStream_t)stream>>>(seed, d_counts);
+  return (int)cudaGetLastError();
+}
+
+int launch_range_check(unsigned long long *d_counts, int sm_count, void *stream) {
+  kvc_range_check<<<(unsigned)(sm_count > 0 ? sm_count * 8 : 1024), 256, 0, (cudaStream_t)stream>>>(d_counts);
   return (int)cudaGetLastError();
 }
 

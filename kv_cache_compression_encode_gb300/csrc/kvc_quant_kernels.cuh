@@ -946,7 +946,7 @@ __global__ void __launch_bounds__(kThreads) kvc_enc_tile(const QuantParams P, co
 constexpr int kKT = 512;
 constexpr int kTabStride = 36;  // floats per 32-channel part in the parameter tables (spreads the parts over banks)
 // 1 KiB slack for aligning the stage to the swizzle's 1 KiB period
-constexpr size_t kKtileSmem = 1024 + 128 * 256 + (size_t)128 * 128 * 4 + 2 * 4 * kTabStride * 4 + 256 * 4;
+constexpr size_t kKtileSmem = 1024 + 128 * 256 + (size_t)128 * 128 * 4 + 3 * 4 * kTabStride * 4 + 256 * 4;
 
 __device__ __forceinline__ uint32_t stage_off(uint32_t k, uint32_t r) {
   return (k >> 3) * 16384u + 128u * r + 16u * ((k & 7u) ^ (r & 7u));
@@ -1142,7 +1142,9 @@ __global__ void __launch_bounds__(kKT, 2)
   float *Y = reinterpret_cast<float *>(stage + 128 * 256);             // [128][128] fp32, swizzled
   float *tab_mu = Y + 128 * 128;                                       // [4 parts][kTabStride]
   float *tab_inv = tab_mu + 4 * kTabStride;
-  float *st = tab_inv + 4 * kTabStride;  // A: channel c minimum at st[c], maximum at st[128 + c]
+  float *tab_nmi = tab_inv + 4 * kTabStride;                           // -mu * inv
+  float *st = tab_nmi + 4 * kTabStride;  // A: channel c minimum at st[c], maximum at st[128 + c]
+  __shared__ uint32_t s_wide;  // a channel of this tile has e > 100 (see the smoothing in C)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t H = P.g.H, T = P.g.T, n_sb = P.n_sb, G = P.group;
   const uint32_t n_tiles = P.g.L * H * n_sb;
@@ -1198,6 +1200,8 @@ __global__ void __launch_bounds__(kKT, 2)
     // pairs (exact); lanes 8j..8j+7 end with pair j (channels 2j, 2j+1 of the octet).
     // With the token delta they run on the fp32 differences from row 0 instead.
     if (smooth) {
+      // every warp has left the previous tile's C (the barrier after C): the flag is free
+      if (tid == 0) s_wide = 0u;
      if constexpr (DELTA) {
       float an[8];  // the octet's channels of row 0, the block's anchor
       {
@@ -1304,6 +1308,8 @@ __global__ void __launch_bounds__(kKT, 2)
         if (HAD && ((P.sign[warp] >> lane) & 1u)) inv = -inv;  // sign folded into the exact scale
         tab_mu[kTabStride * warp + lane] = mu;
         tab_inv[kTabStride * warp + lane] = inv;
+        tab_nmi[kTabStride * warp + lane] = __fmul_rn(-mu, inv);  // exact: mu is binary16, inv = +-2^-e
+        if (e > 100) s_wide = 1u;
         const size_t cell = ((size_t)lh * n_sb + sb) * kHeadDim + ch;
         reinterpret_cast<uint16_t *>(P.mu)[cell] = (uint16_t)mub;
         P.ex[cell] = (int8_t)e;
@@ -1344,13 +1350,28 @@ __global__ void __launch_bounds__(kKT, 2)
         }
       }
       if (smooth) {
-        const float4 *tm = reinterpret_cast<const float4 *>(tab_mu + kTabStride * cp);
+        // x' = RN(x - mu) 2^-e.  One fma, RN(x inv + (-mu inv)), rounds the exact
+        // (x - mu) inv once: the same value whenever x - mu is exact or the result is
+        // normal.  An inexact x - mu has |x - mu| >= |mu| / 2 >= 2^-25 (binary16 mu,
+        // Sterbenz), so with e <= 100 the result is normal; a tile with a larger e
+        // (a range beyond 2^100) takes the two roundings as written.
         const float4 *ti = reinterpret_cast<const float4 *>(tab_inv + kTabStride * cp);
+        if (!s_wide) {
+          const float4 *tn = reinterpret_cast<const float4 *>(tab_nmi + kTabStride * cp);
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-          const float4 m = tm[k], iv = ti[k];
-          w[2 * k] = mul2(sub2(w[2 * k], make_float2(m.x, m.y)), make_float2(iv.x, iv.y));
-          w[2 * k + 1] = mul2(sub2(w[2 * k + 1], make_float2(m.z, m.w)), make_float2(iv.z, iv.w));
+          for (int k = 0; k < 8; k++) {
+            const float4 n = tn[k], iv = ti[k];
+            w[2 * k] = __ffma2_rn(w[2 * k], make_float2(iv.x, iv.y), make_float2(n.x, n.y));
+            w[2 * k + 1] = __ffma2_rn(w[2 * k + 1], make_float2(iv.z, iv.w), make_float2(n.z, n.w));
+          }
+        } else {
+          const float4 *tm = reinterpret_cast<const float4 *>(tab_mu + kTabStride * cp);
+#pragma unroll
+          for (int k = 0; k < 8; k++) {
+            const float4 m = tm[k], iv = ti[k];
+            w[2 * k] = mul2(sub2(w[2 * k], make_float2(m.x, m.y)), make_float2(iv.x, iv.y));
+            w[2 * k + 1] = mul2(sub2(w[2 * k + 1], make_float2(m.z, m.w)), make_float2(iv.z, iv.w));
+          }
         }
         if (nvalid < 128 && !live) {  // rows past the end stay 0 (only the last tile has any)
 #pragma unroll

@@ -323,10 +323,12 @@ def kvc_debug_generic_stages(plan: Plan, enable: bool):
 
 
 def kvc_debug_quotient_check(seed: int = 0, rounds: int = 1, stream: int = 0):
-    """Returns (quotient mismatches for t >= 1e-30, code mismatches, dividends tested)."""
-    out = (C.c_ulonglong * 3)()
+    """Returns the six counts: code quotients differing for t >= 1e-30, codes
+    differing, dividends tested; scale quotients differing for w >= 1e-30, binary16
+    scales differing, patterns tested."""
+    out = (C.c_ulonglong * 6)()
     _check(load().kvc_debug_quotient_check(seed, rounds, out, stream or None), "kvc_debug_quotient_check")
-    return int(out[0]), int(out[1]), int(out[2])
+    return tuple(int(x) for x in out)
 
 
 def kvc_debug_lookback(plan: Plan, ticket: int, poll_limit: int = 0):

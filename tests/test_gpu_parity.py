@@ -147,7 +147,8 @@ def test_empty_tokens():
 # --------------------------------------------------------------------------- quantization ties
 def test_exact_ties_take_the_even_code():
     """Rows whose values sit exactly on (and one ulp around) the half-steps of their
-    group: the fast reciprocal path must hand these to the exact division."""
+    group: the encoders' corrected quotient must land exactly on each tie and round
+    it to the even code, as the division does."""
     T, H = 64, 1
     base = np.arange(32, dtype=np.float32)
     rows = []
@@ -169,6 +170,25 @@ def test_exact_ties_take_the_even_code():
     codec, Qg, Qo, fg, fo = U.quantize_both(case)
     assert fg == fo == 0
     assert np.array_equal(Qg, Qo)
+
+
+@pytest.mark.parametrize("had", [False, True])
+def test_wide_smoothing_ranges_match_oracle(had):
+    """Key channels whose 128-token block spans more than 2^100 (bf16 reaches 3e38):
+    the key-tile encoder applies the smoothing with one fma per pair only where
+    every exponent of the tile is at most 100 and with the two roundings as
+    written elsewhere; both kinds of tile, side by side, must give the oracle's
+    bytes.  One channel is symmetric around 0 (centre 0, exponent 104), one is
+    large and positive only (the centre saturates: the RANGE flag)."""
+    prof = dict(bits_k=4, bits_v=4, group_k=128, group_v=128, hadamard=had, stages=())
+    case = U.Case(L=1, T=384, H=2, dtype="bf16", profile=prof, seed=5).materialize()
+    sgn = torch.where(torch.arange(128, device="cuda") % 2 == 0, 1.0, -1.0)
+    case.k[0][128:256, 0, 7] = (sgn * 1e31).to(torch.bfloat16)      # tile (h 0, block 1): e = 104
+    case.k[0][128:256, 0, 9] = (sgn * 3.0 + 1.5).to(torch.bfloat16)  # an ordinary channel of the same tile
+    case.k[0][256:384, 1, 40] = 1e36                                 # tile (h 1, block 2): centre saturates
+    codec, Qg, Qo, fg, fo = U.quantize_both(case)
+    assert fg == fo and fg != 0, (fg, fo)  # the saturated centre raises RANGE on both sides
+    assert np.array_equal(Qg, Qo), f"payload differs at {np.flatnonzero(Qg != Qo)[:8]}"
 
 
 # --------------------------------------------------------------------------- status words
