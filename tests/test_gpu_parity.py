@@ -117,6 +117,16 @@ def test_ragged_token_counts(T):
     _run_full(U.Case(L=2, T=T, H=1, dtype="bf16", dist="llama", seed=T, profile=prof))
 
 
+@pytest.mark.parametrize("L", [128, 129, 256])
+def test_layer_counts_up_to_the_limit(L):
+    """Up to 128 layers the key tiles arrive by TMA (one tensor map per layer in the
+    launch's parameters); past that the same kernel loads them with cp.async; 256 is
+    the most a plan takes (KVC_MAX_LAYERS)."""
+    prof = dict(smooth_keys=True, hadamard=True, bits_k=4, bits_v=4, group_k=128, group_v=128, stages=LC,
+                chunk_bytes=4096)
+    _run_full(U.Case(L=L, T=130, H=1, dtype="bf16", dist="llama", seed=L, profile=prof))
+
+
 @pytest.mark.parametrize("had", [False, True])
 def test_paged_gather_and_scatter(had):
     prof = dict(smooth_keys=True, hadamard=had, bits_k=4, bits_v=4, group_k=128, group_v=128, stages=LC,
