@@ -131,6 +131,9 @@ def workload_and_profile(name: str):
 
     if name in V2_PROFILES:
         return WORKLOADS["llama8b"], V2_PROFILES[name]
+    if name.endswith(FUSED_SUFFIX):  # the same workload, encoded with kvc_fuse_value_chunks
+        base = name[: -len(FUSED_SUFFIX)]
+        return WORKLOADS[base], PROFILES[base]
     return WORKLOADS[name], PROFILES[name]
 
 
@@ -179,7 +182,21 @@ def kernel_bytes(plan, w, name: str, stream_bytes: int) -> int:
     v_out = sec[2] + sec[3] + sec[7]
     Q = plan.payload_bytes
     table = 4 * plan.n_chunks
+    # the split encode (value-code chunks written by the value encoder): the lossless
+    # launches before and after them read their chunks and write their stored form
+    # (the stream's ratio to the payload assumed for each part)
+    cb = plan.profile.chunk_bytes if hasattr(plan, "profile") else 0
+    head = tail = 0
+    if cb:
+        off2, size2 = plan.section(2)
+        c0, nfull = off2 // cb, size2 // cb
+        head = min(c0 * cb, Q)
+        tail = max(Q - (c0 + nfull) * cb, 0)
+    ratio = stream_bytes / Q if Q else 0.0
     return {
+        "kvc_enc_rows_lc": raw_tensor + v_out,
+        "kvc_lossless_enc_fast_head": int(head * (1 + ratio)),
+        "kvc_lossless_enc_fast_tail": int(tail * (1 + ratio)),
         "kvc_enc_tile": raw_tensor + k_out,
         "kvc_enc_ktile": raw_tensor + k_out,
         "kvc_enc_rows": raw_tensor + v_out,
@@ -369,7 +386,8 @@ def run_kvc(args):
         dist.destroy_process_group()
 
 
-OTHER_CONFIGS = ("llama70b", "llama8b_32k", "llama8b_mixhq", "llama8b_delta")
+FUSED_SUFFIX = "_fused_values"
+OTHER_CONFIGS = ("llama70b", "llama8b_32k", "llama8b_mixhq", "llama8b_delta", "llama8b" + FUSED_SUFFIX)
 
 
 def other_configs(args, device):
@@ -390,6 +408,11 @@ def other_configs(args, device):
         sbuf = codec.new_stream_buffer()
         ok = [torch.empty_like(x) for x in k]
         ov = [torch.empty_like(x) for x in v]
+        fused = name.endswith(FUSED_SUFFIX)
+        if fused:  # the stream must not depend on the execution choice
+            ref = codec.encode(k, v).clone()
+            _, nref, _ = codec.query()
+            kvc.kvc_fuse_value_chunks(codec.plan, True)
         codec.encode(k, v, out=sbuf)
         st, nbytes, _ = codec.query()
         codec.decode(sbuf, nbytes, ok, ov)
@@ -416,6 +439,9 @@ def other_configs(args, device):
                      "status": kvc.status_str(st) if st != kvc.KVC_OK else kvc.status_str(st2)}
         if name == "llama70b":
             out[name]["headline"] = "decode"
+        if fused:
+            out[name]["execution"] = "value-code chunks written by the value encoder (kvc_fuse_value_chunks)"
+            out[name]["stream_matches_unfused"] = bool(nref == nbytes and torch.equal(ref[:nref], sbuf[:nbytes]))
         if prof.get("bits_map_k") is not None or prof.get("token_delta"):
             out[name]["profile"] = json_profile(prof)
         del k, v, ok, ov, sbuf, codec

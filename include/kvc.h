@@ -262,6 +262,22 @@ typedef struct kvc_timing {
 } kvc_timing;
 int kvc_timing_read(kvc_plan_t *plan, kvc_timing *out, int max);
 
+/* Execution choice for kvc_encode (the stream is the same byte for byte either way):
+ * with enable != 0 the value encoder itself writes the whole lossless chunks of the
+ * value-code section into the stream -- it quantizes a chunk's rows into shared
+ * memory, runs the chunk's stages there and takes the chunk's place through the
+ * look-back -- between a lossless launch over the chunks before that section and
+ * one over the rest ("Beyond Compression Ratio" §3 design goal G1, one kernel for
+ * closely coupled operations; §4.1-4.2).  It applies when the values are grouped
+ * over channels with a uniform width of 2, 4 or 8 bits and no token delta, the
+ * stage list is TUPL_8 BIT_8 [DELTA_1] RZE_1/2 with 4, 8, 12 or 16 KiB chunks that
+ * hold a multiple of 128 value rows, and the value-code section starts on a chunk
+ * boundary; otherwise kvc_encode runs as usual.  Off by default: on a GB300 the
+ * fused value encoder (llama8b, 16 KiB chunks) takes longer than the value encoder
+ * and the lossless work it saves together.  Returns KVC_ERR_INVALID_ARG for a null
+ * plan. */
+kvc_status kvc_fuse_value_chunks(kvc_plan_t *plan, int enable);
+
 /* ---- test hooks -------------------------------------------------------------- */
 /* Fault injection on the host side of the look-back scan: the chunk with ticket
  * `ticket` (>= 0) does not publish its size, so its successor's bounded wait runs

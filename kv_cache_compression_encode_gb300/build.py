@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkvc.so")
-SOURCES = ["kvc_api.cu", "kvc_quant.cu", "kvc_quant_delta.cu", "kvc_quant_mixed.cu", "kvc_lossless.cu"]
+SOURCES = ["kvc_api.cu", "kvc_quant.cu", "kvc_quant_delta.cu", "kvc_quant_mixed.cu", "kvc_lossless.cu", "kvc_fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-Xcompiler", "-fPIC,-O2",
          "-I", os.path.join(ROOT, "include")]

@@ -62,6 +62,8 @@ struct kvc_plan_s {
   int64_t skip_ticket;
   uint32_t poll_limit;
   bool generic_stages;
+  // kvc_fuse_value_chunks: the value encoder writes its whole code chunks itself
+  bool fuse_values;
 };
 
 static constexpr uint32_t kDefaultPollLimit = 1u << 22;
@@ -396,6 +398,12 @@ extern "C" int kvc_timing_read(kvc_plan_t *plan, kvc_timing *out, int max) {
   return n;
 }
 
+extern "C" kvc_status kvc_fuse_value_chunks(kvc_plan_t *plan, int enable) {
+  if (!plan) return KVC_ERR_INVALID_ARG;
+  plan->fuse_values = enable != 0;
+  return KVC_OK;
+}
+
 extern "C" kvc_status kvc_debug_generic_stages(kvc_plan_t *plan, int enable) {
   if (!plan) return KVC_ERR_INVALID_ARG;
   plan->generic_stages = enable != 0;
@@ -529,6 +537,37 @@ static const TmaMaps *tensor_maps(kvc_plan_s *P, int t, void *const *layers) {
 // not the encoders: with both grids the 70B encode got 3% slower, and with one
 // CTA of each per SM the shorter kernel's SMs idle once it is done (70B and
 // 8B@32K encodes 23-27% slower), so the encoders run one after the other.
+// The launch parameters of one tensor (0 = K, 1 = V) over payload Q; returns the
+// key tiles' tensor maps when the encoder can load them by TMA.
+static const TmaMaps *fill_quant(kvc_plan_s *P, const kvc_kv *kv, uint8_t *Q, void *ws, int tensor, bool enc,
+                                 bool check_corrupt, QuantParams &q) {
+  memset(&q, 0, sizeof q);
+  fill_geom(P, kv, q.g);
+  void *const *src = tensor ? kv->v_layers : kv->k_layers;
+  for (uint32_t l = 0; l < P->shape.layers; l++) q.layers[l] = src[l];
+  q.bits = tensor ? P->prof.bits_v : P->prof.bits_k;
+  q.group = tensor ? P->prof.group_v : P->prof.group_k;
+  q.axis = tensor ? P->prof.axis_v : P->prof.axis_k;
+  q.smooth = tensor == 0 && P->prof.smooth_keys;
+  q.n_tg = (uint32_t)(tensor ? P->n_tg_v : P->n_tg_k);
+  q.n_sb = (uint32_t)P->n_sb;
+  q.hadamard = P->prof.hadamard;
+  memcpy(q.sign, P->sign, sizeof q.sign);
+  q.codes = Q + P->off[tensor ? 2 : 0];
+  q.meta = Q + P->off[tensor ? 3 : 1];
+  q.mu = Q + P->off[4];
+  q.ex = reinterpret_cast<int8_t *>(Q + P->off[5]);
+  q.status = ctrl_of(ws) + kCtrlFlags;
+  q.check_corrupt = check_corrupt;
+  q.delta = P->prof.token_delta;
+  q.anchors = Q + P->off[tensor ? 7 : 6];
+  q.mixed = P->mixed;
+  const TmaMaps *maps = nullptr;
+  if (enc && q.axis == KVC_AXIS_OVER_TOKENS && !kv->block_table) maps = tensor_maps(P, tensor, src);
+  q.tma = maps != nullptr;
+  return maps;
+}
+
 static kvc_status run_quant(kvc_plan_s *P, const kvc_kv *kv, uint8_t *Q, void *ws, bool enc, bool check_corrupt,
                             cudaStream_t st) {
   if (P->shape.layers == 0 || P->shape.tokens == 0) return KVC_OK;
@@ -543,31 +582,8 @@ static kvc_status run_quant(kvc_plan_s *P, const kvc_kv *kv, uint8_t *Q, void *w
   for (int tensor = 0; tensor < 2 && status == KVC_OK; tensor++) {
     cudaStream_t s = fork && tensor == 1 ? P->side : st;
     QuantParams q;
-    memset(&q, 0, sizeof q);
-    fill_geom(P, kv, q.g);
-    void *const *src = tensor ? kv->v_layers : kv->k_layers;
-    for (uint32_t l = 0; l < P->shape.layers; l++) q.layers[l] = src[l];
-    q.bits = tensor ? P->prof.bits_v : P->prof.bits_k;
-    q.group = tensor ? P->prof.group_v : P->prof.group_k;
-    q.axis = tensor ? P->prof.axis_v : P->prof.axis_k;
-    q.smooth = tensor == 0 && P->prof.smooth_keys;
-    q.n_tg = (uint32_t)(tensor ? P->n_tg_v : P->n_tg_k);
-    q.n_sb = (uint32_t)P->n_sb;
-    q.hadamard = P->prof.hadamard;
-    memcpy(q.sign, P->sign, sizeof q.sign);
-    q.codes = Q + P->off[tensor ? 2 : 0];
-    q.meta = Q + P->off[tensor ? 3 : 1];
-    q.mu = Q + P->off[4];
-    q.ex = reinterpret_cast<int8_t *>(Q + P->off[5]);
-    q.status = ctrl_of(ws) + kCtrlFlags;
-    q.check_corrupt = check_corrupt;
-    q.delta = P->prof.token_delta;
-    q.anchors = Q + P->off[tensor ? 7 : 6];
-    q.mixed = P->mixed;
+    const TmaMaps *maps = fill_quant(P, kv, Q, ws, tensor, enc, check_corrupt, q);
     const WidthTable *wt = P->mixed ? P->wt[tensor] : nullptr;
-    const TmaMaps *maps = nullptr;
-    if (enc && q.axis == KVC_AXIS_OVER_TOKENS && !kv->block_table) maps = tensor_maps(P, tensor, src);
-    q.tma = maps != nullptr;
     Bracket br(P, s);
     const char *name = "";
     const int rc = enc ? launch_quantize(q, maps, wt, P->sm_count, cap, s, &P->launches, &name)
@@ -635,6 +651,9 @@ static void fill_lossless(kvc_plan_s *P, LosslessParams &lp, void *ws) {
   lp.poll_limit = P->poll_limit;
   lp.generic_only = P->generic_stages ? 1u : 0u;
   lp.header_bytes = P->header_bytes;
+  lp.first_chunk = 0;
+  lp.last_chunk = lp.n_chunks;
+  lp.ticket_word = kCtrlTicket;
   memcpy(lp.header, P->header, P->header_bytes);
 }
 
@@ -689,6 +708,51 @@ extern "C" kvc_status kvc_lossless_encode(kvc_plan_t *plan, const void *d_payloa
                               d_stream_bytes, st);
 }
 
+// Encode with the value-code chunks written by the value encoder itself (see
+// kvc_fused.cu): the key encoder; the lossless stages over the chunks before the
+// value codes; the value encoder with the section's whole chunks; the lossless
+// stages over the rest.  Every chunk takes its place through the one look-back, in
+// chunk order across the three launches, so the stream is the one the unfused
+// path writes.
+static kvc_status encode_split(kvc_plan_s *P, const kvc_kv *in, uint8_t *Q, void *ws, const QuantParams &qv,
+                               LosslessParams lp, uint32_t c0, uint32_t nfull, cudaStream_t st) {
+  {
+    QuantParams qk;
+    const TmaMaps *maps = fill_quant(P, in, Q, ws, 0, true, false, qk);
+    Bracket br(P, st);
+    const char *name = "";
+    const int rc = launch_quantize(qk, maps, nullptr, P->sm_count, 0, st, &P->launches, &name);
+    br.done(name);
+    if (rc) return KVC_ERR_CUDA;
+  }
+  lp.first_chunk = 0;
+  lp.last_chunk = c0;
+  lp.ticket_word = kCtrlTicket;
+  if (c0) {
+    Bracket br(P, st);
+    const int rc = launch_lossless_encode(lp, P->sm_count, st);
+    br.done("kvc_lossless_enc_fast_head");
+    P->launches++;
+    if (rc) return KVC_ERR_CUDA;
+  }
+  lp.ticket_word = kCtrlTicket + 1;
+  {
+    Bracket br(P, st);
+    const int rc = launch_v_lossless(qv, lp, c0, nfull, P->sm_count, st);
+    br.done("kvc_enc_rows_lc");
+    P->launches++;
+    if (rc) return KVC_ERR_CUDA;
+  }
+  lp.first_chunk = c0 + nfull;
+  lp.last_chunk = lp.n_chunks;
+  lp.ticket_word = kCtrlTicket + 2;
+  Bracket br(P, st);
+  const int rc = launch_lossless_encode(lp, P->sm_count, st);
+  br.done("kvc_lossless_enc_fast_tail");
+  P->launches++;
+  return cuda_status(rc);
+}
+
 extern "C" kvc_status kvc_encode(kvc_plan_t *plan, const kvc_kv *in, void *d_stream, size_t stream_cap,
                                  void *d_workspace, size_t workspace_bytes, uint64_t *d_stream_bytes,
                                  kvc_stream_t stream) {
@@ -702,6 +766,19 @@ extern "C" kvc_status kvc_encode(kvc_plan_t *plan, const kvc_kv *in, void *d_str
   // without lossless stages the payload is written in place after the header
   uint8_t *Q = plan->prof.n_stages ? ws_payload(plan, d_workspace) : out + plan->header_bytes;
   if ((s = run_prologue(plan, d_workspace, true, true, out, d_stream_bytes, Q, st)) != KVC_OK) return s;
+  if (plan->fuse_values && plan->prof.n_stages && plan->shape.layers && plan->shape.tokens && !plan->mixed) {
+    QuantParams qv;
+    fill_quant(plan, in, Q, d_workspace, 1, true, false, qv);
+    LosslessParams lp;
+    fill_lossless(plan, lp, d_workspace);
+    lp.payload = Q;
+    lp.stream = out;
+    lp.stream_cap = stream_cap;
+    lp.d_stream_bytes = d_stream_bytes;
+    uint32_t c0 = 0, nfull = 0;
+    if (v_lossless_fusable(qv, lp, plan->off[2], plan->size[2], &c0, &nfull))
+      return encode_split(plan, in, Q, d_workspace, qv, lp, c0, nfull, st);
+  }
   if ((s = run_quant(plan, in, Q, d_workspace, true, false, st)) != KVC_OK) return s;
   if (plan->prof.n_stages == 0) return KVC_OK;
   return lossless_encode_impl(plan, Q, d_stream, stream_cap, d_workspace, d_stream_bytes, st);

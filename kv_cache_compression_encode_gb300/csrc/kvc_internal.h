@@ -3,7 +3,9 @@
 // Workspace control block (first 256 bytes of the caller's workspace):
 //   u32 [0]  status flags (KVC_FLAG_*), set with atomicOr by any kernel
 //   u64 @8   stream size written by the last encode
-//   u32 [4]  chunk ticket counter of the lossless encoder
+//   u32 [4]  chunk ticket counter of the lossless encoder ([5], [6]: the value
+//            encoder that writes code chunks into the stream, and the encoder
+//            launch after it)
 // followed at byte 256 by one u64 per lossless chunk (encode: look-back words;
 // decode: chunk byte offsets), then (256-aligned) the quantized payload when
 // lossless stages are on.
@@ -20,7 +22,7 @@ constexpr int kSmoothBlock = 128;   // tokens per key-smoothing block
 constexpr uint32_t kCtrlBytes = 256;
 constexpr int kCtrlFlags = 0;       // u32 index
 constexpr int kCtrlStreamBytes = 1; // u64 index
-constexpr int kCtrlTicket = 4;      // u32 index
+constexpr int kCtrlTicket = 4;      // u32 index (a split encode also uses the next two words)
 constexpr int kSections = 8;        // payload sections (kvc_section)
 // largest stream header: 64 bytes + a 2-bit width map of KVC_MAX_MAP_ENTRIES
 // (layer, head) entries for each of K and V
@@ -117,6 +119,9 @@ struct LosslessParams {
   uint32_t fused_offsets;  // decode: the decoder checks the table and computes the chunk offsets itself
   uint32_t header_bytes;   // the chunk table starts here
   uint32_t generic_only;   // measurement hook: the generic stage kernels even where a fast one exists
+  // encode: this launch takes chunks first_chunk .. last_chunk - 1, in the order of
+  // the ticket counter ctrl[ticket_word] (the whole stream: 0, n_chunks, kCtrlTicket)
+  uint32_t first_chunk, last_chunk, ticket_word, pad2_;
   uint8_t header[kMaxHeaderBytes];  // decode: expected header (header_bytes of it)
 };
 
@@ -134,6 +139,16 @@ int launch_dequantize(const QuantParams &p, const WidthTable *widths, int sm_cou
                       uint64_t *launches, const char **name);
 int launch_prologue(const PrologueParams &p, void *stream);
 int launch_lossless_encode(const LosslessParams &p, int sm_count, void *stream);
+// The value encoder that writes the whole chunks of the value-code section into
+// the stream itself (kvc_fused.cu): whether a profile takes it (the section, at
+// byte codes_off of the payload, starts on a chunk boundary, its chunks hold whole
+// rows, the stage list has the fast path with BIT_8), the chunk index of the
+// section's start and its number of whole chunks; and the launch, which takes its
+// chunks by the ticket counter ctrl[lp.ticket_word].
+bool v_lossless_fusable(const QuantParams &v, const LosslessParams &lp, uint64_t codes_off, uint64_t codes_bytes,
+                        uint32_t *c0, uint32_t *nfull);
+int launch_v_lossless(const QuantParams &v, const LosslessParams &lp, uint32_t c0, uint32_t nfull, int sm_count,
+                      void *stream);
 int launch_decode_prepare(const LosslessParams &p, void *stream);
 int launch_lossless_decode(const LosslessParams &p, int sm_count, void *stream);
 // Whether launch_lossless_decode can take the prepare step into the decoder for

@@ -26,7 +26,7 @@ EXPORTS = ["kvc_plan", "kvc_plan_destroy", "kvc_workspace_bytes", "kvc_max_strea
            "kvc_section", "kvc_num_chunks", "kvc_encode", "kvc_decode", "kvc_quantize", "kvc_lossless_encode",
            "kvc_lossless_decode", "kvc_dequantize", "kvc_query", "kvc_status_str", "kvc_launch_count",
            "kvc_timing_enable", "kvc_timing_read", "kvc_debug_lookback", "kvc_lossless_encode_noalloc",
-           "kvc_header_bytes", "kvc_debug_generic_stages", "kvc_debug_quotient_check"]
+           "kvc_header_bytes", "kvc_debug_generic_stages", "kvc_debug_quotient_check", "kvc_fuse_value_chunks"]
 
 
 class KvcError(RuntimeError):
@@ -111,6 +111,7 @@ def load(build_if_missing: bool = True):
             "kvc_lossless_encode_noalloc": (st, [P, vp, vp, sz, vp, vp, vp]),
             "kvc_header_bytes": (sz, [P]),
             "kvc_debug_generic_stages": (st, [P, C.c_int]),
+            "kvc_fuse_value_chunks": (st, [P, C.c_int]),
             "kvc_debug_quotient_check": (st, [C.c_uint32, C.c_uint32, C.POINTER(C.c_ulonglong), vp]),
         }
         for name, (res, args) in sigs.items():
@@ -316,6 +317,11 @@ def kvc_timing_read(plan: Plan, max_records: int = 4096):
     arr = (Timing * max_records)()
     n = plan.lib.kvc_timing_read(plan.handle, arr, max_records)
     return [(arr[i].kernel.decode(), arr[i].ms) for i in range(n)]
+
+
+def kvc_fuse_value_chunks(plan: Plan, enable: bool):
+    """kvc_encode with the value encoder writing its whole code chunks into the stream."""
+    _check(plan.lib.kvc_fuse_value_chunks(plan.handle, int(bool(enable))), "kvc_fuse_value_chunks")
 
 
 def kvc_debug_generic_stages(plan: Plan, enable: bool):
