@@ -122,3 +122,29 @@ def test_profiles_outside_the_split_path(prof):
     case = U.Case(L=1, T=512, H=8, dtype="bf16", dist="llama", seed=9, profile=prof)
     names = _run(case)
     assert "kvc_enc_rows_lc" not in names
+
+
+@pytest.mark.parametrize("ticket", [3, 37])
+def test_split_encode_lookback_wait_is_bounded(ticket):
+    """A chunk that never publishes (before the value codes, or one of the value
+    encoder's own): the look-backs that meet it run out, the status says TIMEOUT,
+    and the next encode on the same plan is clean and matches the oracle."""
+    prof = dict(smooth_keys=True, hadamard=True, bits_k=4, bits_v=4, group_k=128, group_v=128, stages=FULL,
+                chunk_bytes=16384)
+    case = U.Case(L=2, T=512, H=8, dtype="bf16", dist="llama", seed=8, profile=prof).materialize()
+    assert _fusable(case)
+    lay = O.layout(U.oracle_profile(prof), case.oracle_shape())
+    c0, nfull = lay.off[2] // 16384, lay.size[2] // 16384
+    assert ticket < c0 or c0 <= ticket < c0 + nfull
+    codec = U.Codec(U.kvc_profile(prof), case.kvc_shape())
+    kvc.kvc_fuse_value_chunks(codec.plan, True)
+    kvc.kvc_debug_lookback(codec.plan, ticket, 2000)
+    codec.encode(case.k, case.v)
+    st, _, flags = codec.query()
+    assert st == kvc.KVC_ERR_TIMEOUT and flags & kvc.FLAG_TIMEOUT
+    kvc.kvc_debug_lookback(codec.plan, -1, 0)
+    sg = codec.encode(case.k, case.v)
+    st, nbytes, flags = codec.query()
+    assert st == kvc.KVC_OK and flags == 0
+    so, _ = O.encode(U.oracle_profile(prof), case.oracle_shape(), case.host_bits(case.k), case.host_bits(case.v))
+    assert np.array_equal(U.to_np(sg, nbytes), so)
