@@ -460,7 +460,8 @@ def run_e2e(codec, k, v, ok, ov, w, args, device):
     API takes, so that a direction's KV moves in one copy (a serving KV pool is laid
     out so; many small copies run the link about 14% slower both ways).
     `host_link` holds the copy rates over the same buffers (each direction alone,
-    both at once) and the bound they set on this figure."""
+    both at once) and the bound they set on this figure.  Three timed windows of
+    the same length; the median is the figure (all three are listed)."""
     import torch
 
     from kv_cache_compression_encode_gb300.codec import Codec
@@ -512,15 +513,21 @@ def run_e2e(codec, k, v, ok, ov, w, args, device):
 
     run(4)
     n_steps = max(4, min(20, args.steps // 100))
-    torch.cuda.synchronize(device)
-    t0 = time.perf_counter()
-    run(n_steps)
-    dt = (time.perf_counter() - t0) / n_steps
+    # the host side of the link is shared with other jobs on the machine, which
+    # now and then halve its rate for a while: three windows, the median reported
+    windows = []
+    for _ in range(3):
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        run(n_steps)
+        windows.append((time.perf_counter() - t0) / n_steps)
+    dt = sorted(windows)[1]
     ok_rt = all(torch.equal(a, b.to(a.device)) for L in lanes for a, b in zip(ok + ov, L.rk + L.rv))
 
     # the host link on its own, over the same pinned buffers with all lanes copying at
     # once: each direction alone, and both together (uploads on the lanes' streams,
-    # downloads on a second stream per lane); the bound they put on this figure
+    # downloads on a second stream per lane), each the best of three; the bound they
+    # put on this figure
     down = [torch.cuda.Stream(device) for _ in lanes]
     srcK, srcV = torch.stack(k), torch.stack(v)  # downloads read these, which nothing writes meanwhile
 
@@ -541,11 +548,16 @@ def run_e2e(codec, k, v, ok, ov, w, args, device):
         return reps * n_lanes * w.raw_bytes * (int(up) + int(dn)) / (time.perf_counter() - t0) / 1e9
 
     link(True, False)
-    h2d_gbs, d2h_gbs, both_gbs = link(True, False), link(False, True), link(True, True)
+
+    def best3(up, dn):  # the link's rate when nothing else on the host is using it
+        return max(link(up, dn) for _ in range(3))
+
+    h2d_gbs, d2h_gbs, both_gbs = best3(True, False), best3(False, True), best3(True, True)
     link_ms = max(counts["h2d"] / h2d_gbs, counts["d2h"] / d2h_gbs, (counts["h2d"] + counts["d2h"]) / both_gbs) / 1e6
     return {"value": round(w.raw_bytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": counts["h2d"],
             "d2h_bytes_per_step": counts["d2h"], "ms_per_step": round(dt * 1e3, 3), "steps": n_steps,
             "requests_in_flight": n_lanes, "roundtrip_matches_device_path": bool(ok_rt),
+            "windows_gbs": [round(w.raw_bytes / x / 1e9, 2) for x in windows],
             "host_link": {"h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
                           "both_ways_gbs": round(both_gbs, 1), "bound_gbs": round(w.raw_bytes / link_ms / 1e6, 2)}}
 
