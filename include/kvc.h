@@ -152,8 +152,9 @@ void kvc_plan_destroy(kvc_plan_t *plan);
 
 /* Bytes of the caller-provided device workspace encode/decode need ("persistent
  * runtime scratch", "Beyond Compression Ratio" §4.2): a 256-byte control block
- * (status word, stream size, chunk ticket), per-chunk look-back / offset words and,
- * when lossless stages are on, the quantized payload. */
+ * (status word, stream size, chunk tickets), per-chunk look-back / offset words
+ * (and one word per 4096 chunks for the decode's partial sums) and, when lossless
+ * stages are on, the quantized payload. */
 size_t kvc_workspace_bytes(const kvc_plan_t *plan);
 /* Worst-case stream size (header + chunk table + every chunk stored raw): the
  * capacity of the caller's preallocated output buffer ("Beyond Compression

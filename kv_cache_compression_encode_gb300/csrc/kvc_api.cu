@@ -68,6 +68,14 @@ struct kvc_plan_s {
 
 static constexpr uint32_t kDefaultPollLimit = 1u << 22;
 
+// Bytes of the workspace's per-chunk words: one u64 per chunk (look-back words,
+// then decode offsets) and one per kDecodeSumSeg chunks (the decode prepare's
+// partial sums), 256-aligned.
+static uint64_t state_bytes(uint64_t n_chunks) {
+  const uint64_t n_sums = (n_chunks + kDecodeSumSeg - 1) / kDecodeSumSeg;
+  return (8 * (n_chunks + n_sums) + 255) / 256 * 256;
+}
+
 static uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
 static uint64_t align_up(uint64_t a, uint64_t b) { return (a + b - 1) / b * b; }
 
@@ -266,7 +274,7 @@ extern "C" kvc_status kvc_plan(const kvc_profile *profile_in, const kvc_shape *s
     P->data_start = P->header_bytes;
   }
   P->max_stream_bytes = P->data_start + o;
-  P->workspace_bytes = kCtrlBytes + align_up(8 * P->n_chunks, 256) + (profile->n_stages ? o : 0);
+  P->workspace_bytes = kCtrlBytes + state_bytes(P->n_chunks) + (profile->n_stages ? o : 0);
   P->n_tg_k = ceil_div(s.tokens, profile->group_k);
   P->n_tg_v = ceil_div(s.tokens, profile->group_v);
   P->n_sb = ceil_div(s.tokens, kSmoothBlock);
@@ -461,7 +469,7 @@ static kvc_status check_ws(const kvc_plan_s *P, const void *ws, size_t bytes) {
 static uint32_t *ctrl_of(void *ws) { return static_cast<uint32_t *>(ws); }
 static uint64_t *state_of(void *ws) { return reinterpret_cast<uint64_t *>(static_cast<uint8_t *>(ws) + kCtrlBytes); }
 static uint8_t *ws_payload(const kvc_plan_s *P, void *ws) {
-  return static_cast<uint8_t *>(ws) + kCtrlBytes + align_up(8 * P->n_chunks, 256);
+  return static_cast<uint8_t *>(ws) + kCtrlBytes + state_bytes(P->n_chunks);
 }
 
 static void fill_geom(const kvc_plan_s *P, const kvc_kv *kv, KvGeom &g) {
@@ -798,7 +806,7 @@ static kvc_status lossless_decode_impl(kvc_plan_s *P, const void *d_stream, size
     Bracket br(P, st);
     const int rc = launch_decode_prepare(lp, st);
     br.done("kvc_decode_prepare");
-    P->launches++;
+    P->launches += lp.n_chunks ? 2 : 1;  // the sums (header checks) and the offsets
     if (rc) return KVC_ERR_CUDA;
   }
   if (P->prof.n_stages == 0) {

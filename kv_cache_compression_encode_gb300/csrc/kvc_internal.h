@@ -7,8 +7,9 @@
 //            encoder that writes code chunks into the stream, and the encoder
 //            launch after it)
 // followed at byte 256 by one u64 per lossless chunk (encode: look-back words;
-// decode: chunk byte offsets), then (256-aligned) the quantized payload when
-// lossless stages are on.
+// decode: chunk byte offsets) and one u64 per kDecodeSumSeg chunks (the decode
+// prepare's partial sums), then (256-aligned) the quantized payload when lossless
+// stages are on.
 #pragma once
 #include <cuda.h>
 #include <stdint.h>
@@ -24,6 +25,7 @@ constexpr int kCtrlFlags = 0;       // u32 index
 constexpr int kCtrlStreamBytes = 1; // u64 index
 constexpr int kCtrlTicket = 4;      // u32 index (a split encode also uses the next two words)
 constexpr int kSections = 8;        // payload sections (kvc_section)
+constexpr uint32_t kDecodeSumSeg = 4096;  // table entries per partial sum of the decode prepare
 // largest stream header: 64 bytes + a 2-bit width map of KVC_MAX_MAP_ENTRIES
 // (layer, head) entries for each of K and V
 constexpr int kMaxHeaderBytes = KVC_HEADER_BYTES + 2 * KVC_MAX_MAP_ENTRIES * 2 / 8;

@@ -746,103 +746,139 @@ __device__ bool fast_decode_chunk(const uint8_t *in, uint32_t size, uint32_t n, 
 // chunk offsets.  Any inconsistency sets KVC_FLAG_CORRUPT.
 // ---------------------------------------------------------------------------
 constexpr int PT = 1024;
+constexpr uint32_t kPrepSeg = 4 * PT;  // table entries per CTA of the prepare kernels: one 16-byte load a thread
+static_assert(kPrepSeg == kDecodeSumSeg, "one partial sum per prepare CTA");
 
-__global__ void __launch_bounds__(PT) kvc_decode_prepare(const LosslessParams P) {
+// Block-wide exclusive scan (PT threads) of 64-bit values; tmp holds PT/32 + 1
+// words and ends with the block total in tmp[PT/32].
+__device__ __forceinline__ unsigned long long prep_scan(unsigned long long v, unsigned long long *tmp) {
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= (uint32_t)o) x += y;
+  }
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long w = tmp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= (uint32_t)o) w += y;
+    }
+    tmp[lane] = w;
+    if (lane == 31) tmp[PT / 32] = w;
+  }
+  __syncthreads();
+  return x - v + (warp ? tmp[warp - 1] : 0ull);
+}
+
+// Decode, step 1 (tables too large for the decoder to scan in every CTA), first
+// kernel: CTA b checks table entries [b kPrepSeg, (b + 1) kPrepSeg) against their
+// chunks' lengths (a stored chunk holds exactly its length, a compressed one less)
+// and writes the sum of their aligned sizes to sums[b]; CTA 0 also checks the
+// header and that the stream reaches the chunk data (without stages: the whole
+// payload after the header).  A failed check sets CORRUPT
+// (the caller has cleared the status word).  The sums follow the chunks' words in
+// the workspace (state[n_chunks + b]).
+__global__ void __launch_bounds__(PT) kvc_decode_sums(const LosslessParams P) {
   __shared__ unsigned long long tmp[PT / 32 + 1];
   __shared__ int s_bad;
-  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    s_bad = 0;
-    P.ctrl[kCtrlFlags] = 0u;
-  }
+  const uint32_t tid = threadIdx.x;
+  if (tid == 0) s_bad = 0;
   __syncthreads();
   const uint64_t stream_bytes = P.stream_cap;
-  if (stream_bytes < P.header_bytes) {
-    if (tid == 0) s_bad = 1;
-  } else if (tid < P.header_bytes / 4) {
-    if (reinterpret_cast<const uint32_t *>(P.stream)[tid] != reinterpret_cast<const uint32_t *>(P.header)[tid])
-      atomicOr(&s_bad, 1);
-  }
-  __syncthreads();
-  if (!s_bad) {
-    if (P.n_stages == 0) {
-      if (tid == 0 && stream_bytes < P.header_bytes + P.payload_bytes) s_bad = 1;
-    } else if (stream_bytes < P.data_start) {
+  if (blockIdx.x == 0) {
+    if (stream_bytes < P.header_bytes) {
       if (tid == 0) s_bad = 1;
     } else {
-      // thread tid takes entries [S tid, S tid + S), S a multiple of 4: 16-byte
-      // loads of the table (the table is 16-byte aligned and padded to data_start)
-      const uint32_t nc = P.n_chunks;
-      const uint32_t S = ((nc + PT - 1) / PT + 3) & ~3u;
-      const uint32_t i0 = min(nc, tid * S), i1 = min(nc, i0 + S);
-      const uint32_t *table = reinterpret_cast<const uint32_t *>(P.stream + P.header_bytes);
-      unsigned long long sum = 0;
-      int bad = 0;
-      for (uint32_t i = i0; i < i1; i += 4) {
-        const uint4 q = *reinterpret_cast<const uint4 *>(table + i);
-        const uint32_t e4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          if (i + k < i1) {
-            const uint32_t e = e4[k], sz = e & 0x7fffffffu;
-            const uint64_t off = (uint64_t)(i + k) * P.chunk_bytes;
-            const uint32_t n = (uint32_t)min((uint64_t)P.chunk_bytes, P.payload_bytes - off);
-            if (e >> 31) bad |= sz != n;
-            else bad |= sz >= n;
-            sum += align16u(sz);
-          }
-        }
-      }
-      if (bad) atomicOr(&s_bad, 1);
-      // exclusive scan of the aligned sizes (64-bit)
-      unsigned long long x = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= (uint32_t)o) x += y;
-      }
-      if (lane == 31) tmp[warp] = x;
-      __syncthreads();
-      if (warp == 0) {
-        unsigned long long w = tmp[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned long long y = __shfl_up_sync(0xffffffffu, w, o);
-          if (lane >= (uint32_t)o) w += y;
-        }
-        tmp[lane] = w;
-        if (lane == 31) tmp[PT / 32] = w;
-      }
-      __syncthreads();
-      unsigned long long pos = P.data_start + x - sum + (warp ? tmp[warp - 1] : 0ull);
-      for (uint32_t i = i0; i < i1; i += 4) {
-        const uint4 q = *reinterpret_cast<const uint4 *>(table + i);
-        const uint32_t e4[4] = {q.x, q.y, q.z, q.w};
-        unsigned long long o4[4];
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          o4[k] = pos;
-          if (i + k < i1) pos += align16u(e4[k] & 0x7fffffffu);
-        }
-        if (i + 4 <= i1) {  // offsets of four chunks: two 16-byte stores
-          reinterpret_cast<ulonglong2 *>(P.state + i)[0] = make_ulonglong2(o4[0], o4[1]);
-          reinterpret_cast<ulonglong2 *>(P.state + i)[1] = make_ulonglong2(o4[2], o4[3]);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; k++)
-            if (i + k < i1) P.state[i + k] = o4[k];
-        }
-      }
-      if (tid == 0 && P.data_start + tmp[PT / 32] > stream_bytes) s_bad = 1;
+      if (tid < P.header_bytes / 4 &&
+          reinterpret_cast<const uint32_t *>(P.stream)[tid] != reinterpret_cast<const uint32_t *>(P.header)[tid])
+        atomicOr(&s_bad, 1);
+      // without stages the payload follows the header as it is
+      if (tid == 0 && (P.n_stages == 0 ? stream_bytes < P.header_bytes + P.payload_bytes : stream_bytes < P.data_start))
+        s_bad = 1;
     }
   }
-  __syncthreads();
-  if (tid == 0 && s_bad) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CORRUPT);
+  const uint32_t nc = P.n_chunks, i = blockIdx.x * kPrepSeg + 4 * tid;
+  unsigned long long sum = 0;
+  int bad = 0;
+  if (i < nc && stream_bytes >= P.data_start) {
+    // the table is 16-byte aligned and padded to data_start
+    const uint4 q = *reinterpret_cast<const uint4 *>(P.stream + P.header_bytes + 4 * (size_t)i);
+    const uint32_t e4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      if (i + k < nc) {
+        const uint32_t e = e4[k], sz = e & 0x7fffffffu;
+        const uint64_t off = (uint64_t)(i + k) * P.chunk_bytes;
+        const uint32_t n = (uint32_t)min((uint64_t)P.chunk_bytes, P.payload_bytes - off);
+        if (e >> 31) bad |= sz != n;
+        else bad |= sz >= n;
+        sum += align16u(sz);
+      }
+    }
+  }
+  if (bad) atomicOr(&s_bad, 1);
+  prep_scan(sum, tmp);
+  if (tid == 0) {
+    if (nc) P.state[nc + blockIdx.x] = tmp[PT / 32];
+    if (s_bad) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CORRUPT);
+  }
+}
+
+// Second kernel: CTA b adds the sums of the CTAs before it to data_start, scans
+// its entries' aligned sizes and writes every chunk's byte offset in the stream
+// to state[]; the last CTA checks that the chunks end inside the stream.
+__global__ void __launch_bounds__(PT) kvc_decode_offsets(const LosslessParams P) {
+  __shared__ unsigned long long tmp[PT / 32 + 1];
+  __shared__ unsigned long long s_base;
+  const uint32_t tid = threadIdx.x, lane = tid & 31;
+  const uint64_t *sums = P.state + P.n_chunks;
+  if (tid < 32) {  // sum of sums[0 .. blockIdx.x - 1] by the first warp
+    unsigned long long x = 0;
+    for (uint32_t j = lane; j < blockIdx.x; j += 32) x += sums[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) s_base = P.data_start + x;
+  }
+  const uint32_t nc = P.n_chunks, i = blockIdx.x * kPrepSeg + 4 * tid;
+  uint32_t e4[4] = {0u, 0u, 0u, 0u};
+  unsigned long long sum = 0;
+  if (i < nc && P.stream_cap >= P.data_start) {
+    const uint4 q = *reinterpret_cast<const uint4 *>(P.stream + P.header_bytes + 4 * (size_t)i);
+    e4[0] = q.x; e4[1] = q.y; e4[2] = q.z; e4[3] = q.w;
+#pragma unroll
+    for (int k = 0; k < 4; k++)
+      if (i + k < nc) sum += align16u(e4[k] & 0x7fffffffu);
+  }
+  unsigned long long pos = prep_scan(sum, tmp);  // also publishes s_base (barriers inside)
+  pos += s_base;
+  if (i < nc) {
+    unsigned long long o4[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      o4[k] = pos;
+      if (i + k < nc) pos += align16u(e4[k] & 0x7fffffffu);
+    }
+    if (i + 4 <= nc) {  // offsets of four chunks: two 16-byte stores
+      reinterpret_cast<ulonglong2 *>(P.state + i)[0] = make_ulonglong2(o4[0], o4[1]);
+      reinterpret_cast<ulonglong2 *>(P.state + i)[1] = make_ulonglong2(o4[2], o4[3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; k++)
+        if (i + k < nc) P.state[i + k] = o4[k];
+    }
+  }
+  if (blockIdx.x == gridDim.x - 1 && tid == 0 && s_base + tmp[PT / 32] > P.stream_cap)
+    atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CORRUPT);
 }
 
 // ---------------------------------------------------------------------------
 // Decode, step 1 inside the decoder (tables of up to kFusedMaxChunks chunks):
-// every CTA checks the header and the whole table exactly as kvc_decode_prepare
+// every CTA checks the header and the whole table exactly as kvc_decode_sums
 // does and takes the offsets of its own chunks (c = blockIdx.x + k gridDim.x) from
 // one block scan; all CTAs reach the same verdict, CTA 0 reports a corrupt stream.
 // ---------------------------------------------------------------------------
@@ -1053,7 +1089,11 @@ bool lossless_decode_is_fast(const LosslessParams &p) {
 }
 
 int launch_decode_prepare(const LosslessParams &p, void *stream) {
-  kvc_decode_prepare<<<1, PT, 0, (cudaStream_t)stream>>>(p);
+  if (cudaMemsetAsync(p.ctrl + kCtrlFlags, 0, sizeof(uint32_t), (cudaStream_t)stream) != cudaSuccess)
+    return (int)cudaGetLastError();
+  const uint32_t blocks = p.n_chunks ? (p.n_chunks + kPrepSeg - 1) / kPrepSeg : 1;
+  kvc_decode_sums<<<blocks, PT, 0, (cudaStream_t)stream>>>(p);  // with no chunks: the header checks only
+  if (p.n_chunks) kvc_decode_offsets<<<blocks, PT, 0, (cudaStream_t)stream>>>(p);
   return (int)cudaGetLastError();
 }
 
