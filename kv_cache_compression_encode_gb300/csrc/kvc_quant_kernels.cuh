@@ -226,6 +226,16 @@ __device__ __forceinline__ void enc_row(const QuantParams &P, const uint32_t (*s
         else abase = static_cast<const uint8_t *>(P.layers[l]) + ao + (size_t)(h * kHeadDim + 64 * half) * 2;
       }
     }
+    uint4 av[DELTA ? 8 : 1];  // token delta: the anchor half row, loaded beside the row itself
+    if constexpr (DELTA) {
+#pragma unroll
+      for (int j = 0; j < 8; j++) av[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (abase) {
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+          ld_global32_nc(reinterpret_cast<const uint4 *>(abase) + 2 * j, av[2 * j], av[2 * j + 1]);
+      }
+    }
     if constexpr (DELTA) {
       if (valid && (t & (kSmoothBlock - 1)) == 0) {  // the anchor row keeps its element bits
         uint4 *cell = reinterpret_cast<uint4 *>(
@@ -239,10 +249,7 @@ __device__ __forceinline__ void enc_row(const QuantParams &P, const uint32_t (*s
       uint32_t r4[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
       uint32_t a4[4] = {0u, 0u, 0u, 0u};
       if constexpr (DELTA) {
-        if (abase) {
-          const uint4 a = __ldg(reinterpret_cast<const uint4 *>(abase) + j);
-          a4[0] = a.x; a4[1] = a.y; a4[2] = a.z; a4[3] = a.w;
-        }
+        a4[0] = av[j].x; a4[1] = av[j].y; a4[2] = av[j].z; a4[3] = av[j].w;
       }
 #pragma unroll
       for (int e = 0; e < 4; e++) {
