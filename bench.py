@@ -173,9 +173,43 @@ PAIRED = {"kvc_enc_ktile": "kvc_quantize_kv", "kvc_enc_tile": "kvc_quantize_kv",
 PAIRS = {"kvc_quantize_kv", "kvc_dequantize_kv"}
 
 
-def kernel_bytes(plan, w, name: str, stream_bytes: int) -> int:
+def in_place_ranges(plan, tokens: int):
+    """The chunk ranges of the code sections whose stored chunks kvc_decode's
+    dequantizers read straight from the stream (the library's rule for
+    kvc_decode_codes_in_place, restated for the byte counts)."""
+    p = plan.profile
+    cb = p.chunk_bytes
+    if not p.n_stages or p.bits_map_k or p.bits_map_v or cb & (cb - 1):
+        return []
+    out = []
+    for t in (0, 1):
+        bits, G = (p.bits_v, p.group_v) if t else (p.bits_k, p.group_k)
+        off, size = plan.section(2 * t)
+        ok = bits in (2, 4, 8) and off % cb == 0 and (off + size) // cb > off // cb
+        if (p.axis_v if t else p.axis_k) == 0:  # groups over tokens: the key-tile decoder
+            ok = ok and (-(-tokens // G) * G) % 128 == 0 and cb % (2048 * bits) == 0
+        else:  # the value-row decoder
+            ok = ok and not (t == 0 and p.smooth_keys) and cb % (256 * bits) == 0
+        if ok:
+            out.append((off // cb, (off + size) // cb))
+    return out
+
+
+def raw_in_place_bytes(plan, tokens: int, stream_buf) -> int:
+    """Bytes of the stored (raw) chunks that kvc_decode leaves in the stream: the
+    lossless decoder neither reads nor writes them."""
+    ranges = in_place_ranges(plan, tokens)
+    if not ranges:
+        return 0
+    h = plan.header_bytes
+    table = stream_buf[h:h + 4 * plan.n_chunks].cpu().numpy().view(np.uint32)
+    return sum(int((table[lo:hi] >> 31).sum()) for lo, hi in ranges) * plan.profile.chunk_bytes
+
+
+def kernel_bytes(plan, w, name: str, stream_bytes: int, in_place: int = 0) -> int:
     """Algorithmic bytes one launch of `name` must move (read + write); a pair moves
-    both tensors' bytes."""
+    both tensors' bytes.  `in_place`: bytes of the stored chunks the dequantizers
+    read from the stream, which the lossless decoder skips."""
     raw_tensor = w.layers * w.tokens * w.kv_heads * w.head_dim * 2
     sec = [plan.section(i)[1] for i in range(8)]
     k_out = sec[0] + sec[1] + sec[4] + sec[5] + sec[6]
@@ -207,6 +241,8 @@ def kernel_bytes(plan, w, name: str, stream_bytes: int) -> int:
         "kvc_lossless_enc_fast": Q + stream_bytes,
         "kvc_lossless_dec": stream_bytes + Q,
         "kvc_lossless_dec_fast": stream_bytes + Q,
+        "kvc_lossless_dec_inplace": stream_bytes + Q - 2 * in_place,
+        "kvc_lossless_dec_fast_inplace": stream_bytes + Q - 2 * in_place,
         "kvc_decode_prepare": table + 8 * plan.n_chunks,
         "kvc_prologue": 64 + 8 * plan.n_chunks,
         "kvc_quantize_kv": 2 * raw_tensor + k_out + v_out,
@@ -278,6 +314,7 @@ def run_kvc(args):
     st, _, flags = codec.query()
     if st != kvc.KVC_OK:
         raise RuntimeError(f"decode failed: {kvc.status_str(st)} flags={flags}")
+    in_place = raw_in_place_bytes(codec.plan, w.tokens, stream_buf)
 
     for _ in range(args.warmup):
         step()
@@ -296,6 +333,10 @@ def run_kvc(args):
     n_side = max(3, min(50, args.steps // 10))
     enc_ms = time_loop(lambda: codec.encode(k, v, out=stream_buf), n_side)
     dec_ms = time_loop(lambda: codec.decode(stream_buf, nbytes, ok, ov), n_side)
+    # the same decode with every code chunk restored into the payload first
+    kvc.kvc_decode_codes_in_place(codec.plan, False)
+    dec_payload_ms = time_loop(lambda: codec.decode(stream_buf, nbytes, ok, ov), n_side)
+    kvc.kvc_decode_codes_in_place(codec.plan, True)
 
     # ---- timed region: K steps as a user runs them (no per-launch events)
     launches0 = codec.plan.launches
@@ -354,7 +395,7 @@ def run_kvc(args):
         kernels = {}
         for name, (ms_sum, n) in sorted(per.items(), key=lambda kv: -kv[1][0]):
             avg = ms_sum / n
-            b = kernel_bytes(codec.plan, w, name, nbytes)
+            b = kernel_bytes(codec.plan, w, name, nbytes, in_place)
             rec = {"launches": n, "avg_ms": round(avg, 5), "alg_bytes": b,
                    "gbs": round(b / (avg * 1e-3) / 1e9, 1) if avg > 0 else None}
             if name in units:
@@ -365,7 +406,7 @@ def run_kvc(args):
         top = max(units.items(), key=lambda kv: kv[1][0])[0]
         peak, peak_src = peaks()
         top_avg = per[top][0] / per[top][1]
-        achieved = kernel_bytes(codec.plan, w, top, nbytes) / (top_avg * 1e-3) / 1e9
+        achieved = kernel_bytes(codec.plan, w, top, nbytes, in_place) / (top_avg * 1e-3) / 1e9
         e2e = run_e2e(codec, k, v, ok, ov, w, args, device) if args.e2e else None
         # free this workload before the other configurations are set up
         del k, v, ok, ov, stream_buf
@@ -384,6 +425,8 @@ def run_kvc(args):
                        "step": "kvc_encode + kvc_decode", "l2": "inputs larger than L2 (no flush needed)",
                        "parallelism": f"replicas x{world}"},
             "encode_gbs": round(raw / (enc_ms * 1e-3) / 1e9, 2), "decode_gbs": round(raw / (dec_ms * 1e-3) / 1e9, 2),
+            "decode_payload_path_gbs": round(raw / (dec_payload_ms * 1e-3) / 1e9, 2),
+            "decode_in_place_bytes": in_place,
             "benefit": benefit_report(raw / (enc_ms * 1e-3) / 1e9, raw / (dec_ms * 1e-3) / 1e9, raw / nbytes),
             "roofline": {"bound": "hbm", "kernel": top, "achieved": round(achieved, 1), "peak": peak,
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
@@ -447,10 +490,14 @@ def other_configs(args, device):
         n = max(5, min(50, args.steps // 40))
         enc_ms = loop(lambda: codec.encode(k, v, out=sbuf), n)
         dec_ms = loop(lambda: codec.decode(sbuf, nbytes, ok, ov), n)
+        kvc.kvc_decode_codes_in_place(codec.plan, False)
+        dec_payload_ms = loop(lambda: codec.decode(sbuf, nbytes, ok, ov), n)
+        kvc.kvc_decode_codes_in_place(codec.plan, True)
         out[name] = {"workload": w.name, "raw_bytes": w.raw_bytes, "stream_bytes": nbytes,
                      "compression_ratio": round(w.raw_bytes / nbytes, 4), "encode_ms": round(enc_ms, 4),
                      "decode_ms": round(dec_ms, 4), "encode_gbs": round(w.raw_bytes / (enc_ms * 1e-3) / 1e9, 1),
-                     "decode_gbs": round(w.raw_bytes / (dec_ms * 1e-3) / 1e9, 1), "steps": n,
+                     "decode_gbs": round(w.raw_bytes / (dec_ms * 1e-3) / 1e9, 1),
+                     "decode_payload_path_gbs": round(w.raw_bytes / (dec_payload_ms * 1e-3) / 1e9, 1), "steps": n,
                      "status": kvc.status_str(st) if st != kvc.KVC_OK else kvc.status_str(st2)}
         if name == "llama70b":
             out[name]["headline"] = "decode"

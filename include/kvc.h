@@ -279,6 +279,19 @@ int kvc_timing_read(kvc_plan_t *plan, kvc_timing *out, int max);
  * plan. */
 kvc_status kvc_fuse_value_chunks(kvc_plan_t *plan, int enable);
 
+/* Execution choice for kvc_decode (the reconstruction is the same either way): with
+ * enable != 0 (the default) the dequantizers read the codes of stored (raw) chunks
+ * straight from the stream, so those chunks never pass through the workspace
+ * payload; the lossless decoder restores only the other chunks ("Beyond Compression
+ * Ratio" §3 design goal G1 and §4.2: the decoder's output feeds reconstruction on
+ * the device).  It applies per tensor to the whole chunks of its code section when
+ * the width is a uniform 2, 4 or 8 bits, chunk_bytes is a power of two, the section
+ * starts on a chunk boundary, and either the groups run over tokens with
+ * ceil(T / group) * group a multiple of 128 and 2048 * bits dividing chunk_bytes,
+ * or they run over channels without key smoothing.  kvc_lossless_decode always
+ * writes the whole payload.  Returns KVC_ERR_INVALID_ARG for a null plan. */
+kvc_status kvc_decode_codes_in_place(kvc_plan_t *plan, int enable);
+
 /* ---- test hooks -------------------------------------------------------------- */
 /* Fault injection on the host side of the look-back scan: the chunk with ticket
  * `ticket` (>= 0) does not publish its size, so its successor's bounded wait runs

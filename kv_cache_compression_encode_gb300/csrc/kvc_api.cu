@@ -64,6 +64,9 @@ struct kvc_plan_s {
   bool generic_stages;
   // kvc_fuse_value_chunks: the value encoder writes its whole code chunks itself
   bool fuse_values;
+  // kvc_decode_codes_in_place: kvc_decode's dequantizers read stored code chunks
+  // from the stream
+  bool codes_in_place;
 };
 
 static constexpr uint32_t kDefaultPollLimit = 1u << 22;
@@ -290,6 +293,7 @@ extern "C" kvc_status kvc_plan(const kvc_profile *profile_in, const kvc_shape *s
   if (P->sm_count <= 0) P->sm_count = 1;
   P->skip_ticket = -1;
   P->poll_limit = kDefaultPollLimit;
+  P->codes_in_place = true;
   // the side stream and its events are made here, once, so that encode and decode
   // create nothing; without them the two tensors' kernels run one after the other
   P->side = nullptr;
@@ -409,6 +413,12 @@ extern "C" int kvc_timing_read(kvc_plan_t *plan, kvc_timing *out, int max) {
 extern "C" kvc_status kvc_fuse_value_chunks(kvc_plan_t *plan, int enable) {
   if (!plan) return KVC_ERR_INVALID_ARG;
   plan->fuse_values = enable != 0;
+  return KVC_OK;
+}
+
+extern "C" kvc_status kvc_decode_codes_in_place(kvc_plan_t *plan, int enable) {
+  if (!plan) return KVC_ERR_INVALID_ARG;
+  plan->codes_in_place = enable != 0;
   return KVC_OK;
 }
 
@@ -536,6 +546,35 @@ static const TmaMaps *tensor_maps(kvc_plan_s *P, int t, void *const *layers) {
   return P->tm[t];
 }
 
+// The chunks [lo, hi) whose codes of tensor t (0 = K, 1 = V) kvc_decode's
+// dequantizer reads in place: the whole chunks of the tensor's code section, where
+// its decoder reads a unit's codes through one lookup -- the key-tile decoder
+// (groups over tokens, every (layer, head) holding whole 128-token tiles, a tile of
+// 2048 BITS bytes dividing the chunk) or the value-row decoder (groups over channels
+// without smoothing, 16 rows of 16 BITS bytes dividing the chunk) -- with a uniform
+// width of 2, 4 or 8 bits, chunks of a power of two bytes and the section starting
+// on a chunk boundary.
+static bool in_place_range(const kvc_plan_s *P, int t, uint32_t *lo, uint32_t *hi) {
+  *lo = *hi = 0;
+  if (!P->codes_in_place || P->prof.n_stages == 0 || P->mixed || P->n_chunks == 0) return false;
+  const uint32_t bits = t ? P->prof.bits_v : P->prof.bits_k, G = t ? P->prof.group_v : P->prof.group_k;
+  const uint32_t axis = t ? P->prof.axis_v : P->prof.axis_k;
+  const bool smooth = t == 0 && P->prof.smooth_keys;
+  const uint64_t cb = P->prof.chunk_bytes, off = P->off[t ? 2 : 0], size = P->size[t ? 2 : 0];
+  if ((bits != 2 && bits != 4 && bits != 8) || cb == 0 || (cb & (cb - 1)) || off % cb) return false;
+  if (axis == KVC_AXIS_OVER_TOKENS) {
+    const uint64_t n_tg = t ? P->n_tg_v : P->n_tg_k;
+    if ((n_tg * G) % kSmoothBlock || cb % (2048ull * bits)) return false;
+  } else if (smooth || cb % (256ull * bits)) {
+    return false;
+  }
+  const uint64_t l = off / cb, h = (off + size) / cb;
+  if (h <= l || h > P->n_chunks) return false;
+  *lo = (uint32_t)l;
+  *hi = (uint32_t)h;
+  return true;
+}
+
 // One quantize / dequantize launch per tensor.  Decoding runs K on the caller's
 // stream and V beside it on the plan's side stream (forked after the work already
 // queued on the caller's stream, joined back before anything queued after): the
@@ -548,7 +587,7 @@ static const TmaMaps *tensor_maps(kvc_plan_s *P, int t, void *const *layers) {
 // The launch parameters of one tensor (0 = K, 1 = V) over payload Q; returns the
 // key tiles' tensor maps when the encoder can load them by TMA.
 static const TmaMaps *fill_quant(kvc_plan_s *P, const kvc_kv *kv, uint8_t *Q, void *ws, int tensor, bool enc,
-                                 bool check_corrupt, QuantParams &q) {
+                                 bool check_corrupt, bool in_place, QuantParams &q) {
   memset(&q, 0, sizeof q);
   fill_geom(P, kv, q.g);
   void *const *src = tensor ? kv->v_layers : kv->k_layers;
@@ -570,6 +609,14 @@ static const TmaMaps *fill_quant(kvc_plan_s *P, const kvc_kv *kv, uint8_t *Q, vo
   q.delta = P->prof.token_delta;
   q.anchors = Q + P->off[tensor ? 7 : 6];
   q.mixed = P->mixed;
+  uint32_t lo, hi;
+  if (in_place && !enc && in_place_range(P, tensor, &lo, &hi)) {
+    q.src_of = state_of(ws);
+    q.codes_off = P->off[tensor ? 2 : 0];
+    q.chunk_shift = (uint32_t)__builtin_ctz(P->prof.chunk_bytes);
+    q.in_lo = lo;
+    q.in_hi = hi;
+  }
   const TmaMaps *maps = nullptr;
   if (enc && q.axis == KVC_AXIS_OVER_TOKENS && !kv->block_table) maps = tensor_maps(P, tensor, src);
   q.tma = maps != nullptr;
@@ -577,7 +624,7 @@ static const TmaMaps *fill_quant(kvc_plan_s *P, const kvc_kv *kv, uint8_t *Q, vo
 }
 
 static kvc_status run_quant(kvc_plan_s *P, const kvc_kv *kv, uint8_t *Q, void *ws, bool enc, bool check_corrupt,
-                            cudaStream_t st) {
+                            cudaStream_t st, bool in_place = false) {
   if (P->shape.layers == 0 || P->shape.tokens == 0) return KVC_OK;
   const bool fork = P->side != nullptr && !enc;
   const int cap = 0;
@@ -590,7 +637,7 @@ static kvc_status run_quant(kvc_plan_s *P, const kvc_kv *kv, uint8_t *Q, void *w
   for (int tensor = 0; tensor < 2 && status == KVC_OK; tensor++) {
     cudaStream_t s = fork && tensor == 1 ? P->side : st;
     QuantParams q;
-    const TmaMaps *maps = fill_quant(P, kv, Q, ws, tensor, enc, check_corrupt, q);
+    const TmaMaps *maps = fill_quant(P, kv, Q, ws, tensor, enc, check_corrupt, in_place, q);
     const WidthTable *wt = P->mixed ? P->wt[tensor] : nullptr;
     Bracket br(P, s);
     const char *name = "";
@@ -726,7 +773,7 @@ static kvc_status encode_split(kvc_plan_s *P, const kvc_kv *in, uint8_t *Q, void
                                LosslessParams lp, uint32_t c0, uint32_t nfull, cudaStream_t st) {
   {
     QuantParams qk;
-    const TmaMaps *maps = fill_quant(P, in, Q, ws, 0, true, false, qk);
+    const TmaMaps *maps = fill_quant(P, in, Q, ws, 0, true, false, false, qk);
     Bracket br(P, st);
     const char *name = "";
     const int rc = launch_quantize(qk, maps, nullptr, P->sm_count, 0, st, &P->launches, &name);
@@ -776,7 +823,7 @@ extern "C" kvc_status kvc_encode(kvc_plan_t *plan, const kvc_kv *in, void *d_str
   if ((s = run_prologue(plan, d_workspace, true, true, out, d_stream_bytes, Q, st)) != KVC_OK) return s;
   if (plan->fuse_values && plan->prof.n_stages && plan->shape.layers && plan->shape.tokens && !plan->mixed) {
     QuantParams qv;
-    fill_quant(plan, in, Q, d_workspace, 1, true, false, qv);
+    fill_quant(plan, in, Q, d_workspace, 1, true, false, false, qv);
     LosslessParams lp;
     fill_lossless(plan, lp, d_workspace);
     lp.payload = Q;
@@ -793,9 +840,11 @@ extern "C" kvc_status kvc_encode(kvc_plan_t *plan, const kvc_kv *in, void *d_str
 }
 
 static kvc_status lossless_decode_impl(kvc_plan_s *P, const void *d_stream, size_t stream_bytes, uint8_t *Q, void *ws,
-                                       bool copy_plain, cudaStream_t st) {
+                                       bool copy_plain, cudaStream_t st, bool in_place = false) {
   LosslessParams lp;
   fill_lossless(P, lp, ws);
+  bool some = false;
+  for (int t = 0; t < 2 && in_place; t++) some |= in_place_range(P, t, &lp.inplace_lo[t], &lp.inplace_hi[t]);
   lp.stream = static_cast<uint8_t *>(const_cast<void *>(d_stream));
   lp.stream_cap = stream_bytes;
   lp.out_payload = Q;
@@ -819,7 +868,8 @@ static kvc_status lossless_decode_impl(kvc_plan_s *P, const void *d_stream, size
   }
   Bracket br(P, st);
   const int rc = launch_lossless_decode(lp, P->sm_count, st);
-  br.done(lossless_decode_is_fast(lp) ? "kvc_lossless_dec_fast" : "kvc_lossless_dec");
+  br.done(lossless_decode_is_fast(lp) ? (some ? "kvc_lossless_dec_fast_inplace" : "kvc_lossless_dec_fast")
+                                      : (some ? "kvc_lossless_dec_inplace" : "kvc_lossless_dec"));
   if (P->n_chunks) P->launches++;
   return cuda_status(rc);
 }
@@ -855,8 +905,8 @@ extern "C" kvc_status kvc_decode(kvc_plan_t *plan, const void *d_stream, size_t 
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t *Q = plan->prof.n_stages ? ws_payload(plan, d_workspace)
                                    : static_cast<uint8_t *>(const_cast<void *>(d_stream)) + plan->header_bytes;
-  if ((s = lossless_decode_impl(plan, d_stream, stream_bytes, Q, d_workspace, false, st)) != KVC_OK) return s;
-  return run_quant(plan, out, Q, d_workspace, false, true, st);
+  if ((s = lossless_decode_impl(plan, d_stream, stream_bytes, Q, d_workspace, false, st, true)) != KVC_OK) return s;
+  return run_quant(plan, out, Q, d_workspace, false, true, st, true);
 }
 
 extern "C" kvc_status kvc_query(const void *d_workspace, kvc_stream_t stream, uint64_t *host_stream_bytes,

@@ -7,7 +7,8 @@
 //            encoder that writes code chunks into the stream, and the encoder
 //            launch after it)
 // followed at byte 256 by one u64 per lossless chunk (encode: look-back words;
-// decode: chunk byte offsets) and one u64 per kDecodeSumSeg chunks (the decode
+// decode: chunk byte offsets, then for chunks whose codes are read in place the
+// address of their bytes) and one u64 per kDecodeSumSeg chunks (the decode
 // prepare's partial sums), then (256-aligned) the quantized payload when lossless
 // stages are on.
 #pragma once
@@ -60,6 +61,16 @@ struct QuantParams {
   uint32_t delta;                // token delta: subtract (add back) each 128-token block's first row
   uint32_t mixed;                // per-(layer, head) widths: the launch also takes a WidthTable
   uint8_t *anchors;              // token delta: anchor element bits [layer][head][block][channel]
+  // decode with codes read in place (in_lo < in_hi): the code bytes at payload
+  // offset o = codes_off + (their offset from `codes`) lie in chunk c = o >> chunk_shift;
+  // for in_lo <= c < in_hi they are read at src_of[c] + (o mod 2^chunk_shift), the
+  // address the lossless decoder left there (the stored chunk in the stream when it
+  // is stored raw, else the chunk decoded into the payload).  A decoder reads one
+  // unit (a key tile, 16 value rows) from one such lookup, so the host enables it
+  // only where no unit crosses a chunk boundary.
+  const uint64_t *src_of;
+  uint64_t codes_off;
+  uint32_t chunk_shift, in_lo, in_hi, pad3_;
 };
 
 // Per-(layer, head) widths of one tensor: wsum[i] = sum of the widths of entries
@@ -124,6 +135,10 @@ struct LosslessParams {
   // encode: this launch takes chunks first_chunk .. last_chunk - 1, in the order of
   // the ticket counter ctrl[ticket_word] (the whole stream: 0, n_chunks, kCtrlTicket)
   uint32_t first_chunk, last_chunk, ticket_word, pad2_;
+  // decode: chunks c with inplace_lo[i] <= c < inplace_hi[i] hold codes that the
+  // dequantizers read in place; the decoder leaves a raw one in the stream (no copy)
+  // and sets state[c] to the address of the chunk's bytes (stream or payload)
+  uint32_t inplace_lo[2], inplace_hi[2];
   uint8_t header[kMaxHeaderBytes];  // decode: expected header (header_bytes of it)
 };
 

@@ -944,8 +944,14 @@ __device__ bool decode_offsets(const LosslessParams &P, unsigned long long *tmp,
   return true;
 }
 
+__device__ __forceinline__ bool in_place_chunk(const LosslessParams &P, uint32_t c) {
+  return (c >= P.inplace_lo[0] && c < P.inplace_hi[0]) || (c >= P.inplace_lo[1] && c < P.inplace_hi[1]);
+}
+
 // ---------------------------------------------------------------------------
-// Decode, step 2: one chunk per CTA iteration back into the payload.
+// Decode, step 2: one chunk per CTA iteration back into the payload.  A chunk
+// whose codes the dequantizers read in place (inplace_lo/hi) gets the address of
+// its bytes in state[c]; stored raw, it is left in the stream.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(LT, 3) kvc_lossless_dec(const LosslessParams P, const FastSpec F) {
   extern __shared__ uint4 smem_u4[];
@@ -969,58 +975,95 @@ __global__ void __launch_bounds__(LT, 3) kvc_lossless_dec(const LosslessParams P
   const uint32_t last = P.n_stages - 1;
   const bool has_rze = P.kind[last] == KVC_ST_RZE;
 
-  for (uint32_t c = blockIdx.x, kc = 0; c < P.n_chunks; c += gridDim.x, kc++) {
-    const uint32_t e = table[c], size = e & 0x7fffffffu;
-    const uint64_t off = (uint64_t)c * P.chunk_bytes;
-    const uint32_t n = (uint32_t)min((uint64_t)P.chunk_bytes, P.payload_bytes - off);
-    const uint4 *src = reinterpret_cast<const uint4 *>(P.stream + (P.fused_offsets ? s_off[kc] : P.state[c]));
-    uint4 *dst = reinterpret_cast<uint4 *>(P.out_payload + off);
-    if (e >> 31) {
-      for (uint32_t i = threadIdx.x; i < n / 16; i += LT) dst[i] = __ldg(src + i);
-      continue;
-    }
-    if (!has_rze) {  // a non-raw chunk needs an RZE stage (the prepare step allows size < n only)
-      if (threadIdx.x == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CORRUPT);
-      continue;
-    }
-    for (uint32_t i = threadIdx.x; i < align16u(size) / 16; i += LT) reinterpret_cast<uint4 *>(bufA)[i] = __ldg(src + i);
-    __syncthreads();
-    if (F.rze_w != 0 && fast_len(n)) {
-      uint8_t *d8 = P.out_payload + off;
-      bool ok;
-      if (F.rze_w == 2) {
-        if (F.delta1) ok = F.bit8 ? fast_decode_chunk<2, true, true>(bufA, size, n, bufB, d8, tmp)
-                                  : fast_decode_chunk<2, true, false>(bufA, size, n, bufB, d8, tmp);
-        else ok = F.bit8 ? fast_decode_chunk<2, false, true>(bufA, size, n, bufB, d8, tmp)
-                         : fast_decode_chunk<2, false, false>(bufA, size, n, bufB, d8, tmp);
-      } else {
-        if (F.delta1) ok = F.bit8 ? fast_decode_chunk<1, true, true>(bufA, size, n, bufB, d8, tmp)
-                                  : fast_decode_chunk<1, true, false>(bufA, size, n, bufB, d8, tmp);
-        else ok = F.bit8 ? fast_decode_chunk<1, false, true>(bufA, size, n, bufB, d8, tmp)
-                         : fast_decode_chunk<1, false, false>(bufA, size, n, bufB, d8, tmp);
+  // this CTA's chunks c = blockIdx.x + k gridDim.x, k < n_own, in batches of LT
+  const uint32_t b = blockIdx.x, grid = gridDim.x;
+  const uint32_t n_own = b < P.n_chunks ? (P.n_chunks - 1 - b) / grid + 1 : 0;
+  const bool any_inpl = P.inplace_hi[0] > P.inplace_lo[0] || P.inplace_hi[1] > P.inplace_lo[1];
+  __shared__ uint32_t s_skip[LT / 32];
+  for (uint32_t kb = 0; kb < n_own; kb += LT) {
+    if (any_inpl) {
+      // one chunk of the batch per thread: a raw chunk whose codes are read in place
+      // only gets its stream address in state[c] and is skipped below
+      const uint32_t k = kb + threadIdx.x;
+      bool skip = false;
+      if (k < n_own) {
+        const uint32_t c = b + k * grid;
+        if (in_place_chunk(P, c)) {
+          const uint32_t e = table[c];
+          if (e >> 31) {
+            const uint64_t soff = P.fused_offsets ? s_off[k] : P.state[c];
+            P.state[c] = (uint64_t)(uintptr_t)(P.stream + soff);
+            skip = true;
+          }
+        }
       }
+      const uint32_t m = __ballot_sync(0xffffffffu, skip);
+      if ((threadIdx.x & 31) == 0) s_skip[threadIdx.x >> 5] = m;
+      __syncthreads();
+    }
+    const uint32_t kend = min(n_own, kb + (uint32_t)LT);
+    for (uint32_t kc = kb; kc < kend; kc++) {
+      if (any_inpl && ((s_skip[(kc - kb) >> 5] >> ((kc - kb) & 31)) & 1u)) continue;
+      const uint32_t c = b + kc * grid;
+      const uint32_t e = table[c], size = e & 0x7fffffffu;
+      const uint64_t off = (uint64_t)c * P.chunk_bytes;
+      const uint32_t n = (uint32_t)min((uint64_t)P.chunk_bytes, P.payload_bytes - off);
+      const uint64_t soff = P.fused_offsets ? s_off[kc] : P.state[c];
+      const uint4 *src = reinterpret_cast<const uint4 *>(P.stream + soff);
+      uint4 *dst = reinterpret_cast<uint4 *>(P.out_payload + off);
+      if (in_place_chunk(P, c)) {  // a compressed chunk read in place: restored into the payload
+        if (!P.fused_offsets) __syncthreads();  // every thread has read state[c]
+        if (threadIdx.x == 0) P.state[c] = (uint64_t)(uintptr_t)(P.out_payload + off);
+      }
+      if (e >> 31) {
+        for (uint32_t i = threadIdx.x; i < n / 16; i += LT) dst[i] = __ldg(src + i);
+        continue;
+      }
+      if (!has_rze) {  // a non-raw chunk needs an RZE stage (the prepare step allows size < n only)
+        if (threadIdx.x == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CORRUPT);
+        continue;
+      }
+      for (uint32_t i = threadIdx.x; i < align16u(size) / 16; i += LT)
+        reinterpret_cast<uint4 *>(bufA)[i] = __ldg(src + i);
+      __syncthreads();
+      if (F.rze_w != 0 && fast_len(n)) {
+        uint8_t *d8 = P.out_payload + off;
+        bool ok;
+        if (F.rze_w == 2) {
+          if (F.delta1) ok = F.bit8 ? fast_decode_chunk<2, true, true>(bufA, size, n, bufB, d8, tmp)
+                                    : fast_decode_chunk<2, true, false>(bufA, size, n, bufB, d8, tmp);
+          else ok = F.bit8 ? fast_decode_chunk<2, false, true>(bufA, size, n, bufB, d8, tmp)
+                           : fast_decode_chunk<2, false, false>(bufA, size, n, bufB, d8, tmp);
+        } else {
+          if (F.delta1) ok = F.bit8 ? fast_decode_chunk<1, true, true>(bufA, size, n, bufB, d8, tmp)
+                                    : fast_decode_chunk<1, true, false>(bufA, size, n, bufB, d8, tmp);
+          else ok = F.bit8 ? fast_decode_chunk<1, false, true>(bufA, size, n, bufB, d8, tmp)
+                           : fast_decode_chunk<1, false, false>(bufA, size, n, bufB, d8, tmp);
+        }
+        if (!ok) {
+          if (threadIdx.x == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CORRUPT);
+          __syncthreads();
+        }
+        continue;
+      }
+      const bool ok = rze_decode(bufA, size, bufB, n, P.param[last], Bs, tmp);
       if (!ok) {
         if (threadIdx.x == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CORRUPT);
         __syncthreads();
+        continue;
       }
-      continue;
-    }
-    const bool ok = rze_decode(bufA, size, bufB, n, P.param[last], Bs, tmp);
-    if (!ok) {
-      if (threadIdx.x == 0) atomicOr(P.ctrl + kCtrlFlags, (uint32_t)KVC_FLAG_CORRUPT);
+      uint8_t *cur = bufB, *nxt = bufA;
+      for (int s = (int)last - 1; s >= 0; s--) {
+        const uint32_t k = P.kind[s], prm = P.param[s];
+        if (k == KVC_ST_TUPL) tupl_decode(cur, nxt, n, prm);
+        else if (k == KVC_ST_BIT) bit_decode(cur, nxt, n);
+        else delta_decode(cur, nxt, n, prm, tmp);
+        uint8_t *t = cur; cur = nxt; nxt = t;
+      }
+      for (uint32_t i = threadIdx.x; i < n / 16; i += LT) dst[i] = reinterpret_cast<const uint4 *>(cur)[i];
       __syncthreads();
-      continue;
     }
-    uint8_t *cur = bufB, *nxt = bufA;
-    for (int s = (int)last - 1; s >= 0; s--) {
-      const uint32_t k = P.kind[s], prm = P.param[s];
-      if (k == KVC_ST_TUPL) tupl_decode(cur, nxt, n, prm);
-      else if (k == KVC_ST_BIT) bit_decode(cur, nxt, n);
-      else delta_decode(cur, nxt, n, prm, tmp);
-      uint8_t *t = cur; cur = nxt; nxt = t;
-    }
-    for (uint32_t i = threadIdx.x; i < n / 16; i += LT) dst[i] = reinterpret_cast<const uint4 *>(cur)[i];
-    __syncthreads();
+    if (any_inpl) __syncthreads();  // s_skip is rewritten by the next batch
   }
 }
 

@@ -179,6 +179,18 @@ __device__ __forceinline__ void pack_sums32(const uint32_t (&u)[32], uint32_t (&
   }
 }
 
+// Decode with codes read in place: the address of the code unit at byte `rel` of
+// the code section (a unit never crosses a chunk boundary where this is enabled).
+__device__ __forceinline__ const uint8_t *code_unit(const QuantParams &P, size_t rel) {
+  if (P.in_lo < P.in_hi) {
+    const uint64_t o = P.codes_off + rel, c = o >> P.chunk_shift;
+    if (c >= P.in_lo && c < P.in_hi)
+      return reinterpret_cast<const uint8_t *>(__ldg(reinterpret_cast<const unsigned long long *>(P.src_of) + c)) +
+             (o & ((1ull << P.chunk_shift) - 1u));
+  }
+  return P.codes + rel;
+}
+
 // Where a value row's codes go.  Uniform width: record row R = (l T + t) H + h at
 // R * 16 BITS.  Per-(layer, head) widths: layer l's rows start at 16 T wsum[lH],
 // token t's row at + 16 t (wsum[(l+1)H] - wsum[lH]), head h at + 16 (wsum[lH+h] - wsum[lH]).
@@ -609,10 +621,11 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_dec_rows(const QuantParams P,
     constexpr uint32_t kStage = (uint32_t)dec_rows_stage_bytes(BITS);
     uint8_t *stage0 = reinterpret_cast<uint8_t *>(rows_out) + kDecRowsSmem + (size_t)warp * 2 * kStage;
     const uint32_t wpr = kHeadDim / P.group;  // metadata words per row
-    auto issue = [&](uint32_t itn, uint8_t *buf) {
+    // the codes of step itn's 16 rows: 256 BITS bytes, one unit for code_unit
+    auto codes_of = [&](uint32_t itn) { return code_unit(P, (size_t)itn * (256 * BITS)); };
+    auto issue = [&](uint32_t itn, const uint8_t *cg, uint8_t *buf) {
       const uint32_t r0 = itn * 16;
       const uint32_t nrow = NR - r0 < 16u ? NR - r0 : 16u;
-      const uint8_t *cg = P.codes + (size_t)r0 * (16 * BITS);
       for (uint32_t u = lane; u < nrow * BITS; u += 32)  // 16-byte units, BITS per row
         cp_async16_q(buf + 16 * u, cg + 16 * (size_t)u);
       const uint32_t *mg = reinterpret_cast<const uint32_t *>(P.meta) + (size_t)r0 * wpr;
@@ -624,14 +637,18 @@ __global__ void __launch_bounds__(kThreads, 2) kvc_dec_rows(const QuantParams P,
       cp_async_commit_q();
     };
     uint32_t k = 0;
-    if (it0 < n_it) issue(it0, stage0);
+    if (it0 < n_it) issue(it0, codes_of(it0), stage0);
+    // the code address of the step after the next is looked up one step early
+    const uint8_t *cg_next = it0 + it_step < n_it ? codes_of(it0 + it_step) : nullptr;
     for (uint32_t it = it0; it < n_it; it += it_step, k ^= 1u) {
       const bool valid = it * 16 + rsub < NR;
       const uint32_t l = pos.l, t = pos.b, h = pos.a;
       pos.advance(da, db, dl, na, nb);
       const uint32_t R = (l * T + t) * H + h;
-      if (it + it_step < n_it) issue(it + it_step, stage0 + (k ^ 1u) * kStage);
+      const uint8_t *cg_after = it + 2 * it_step < n_it ? codes_of(it + 2 * it_step) : nullptr;
+      if (it + it_step < n_it) issue(it + it_step, cg_next, stage0 + (k ^ 1u) * kStage);
       else cp_async_commit_q();  // an empty group keeps the wait count below uniform
+      cg_next = cg_after;
       asm volatile("cp.async.wait_group 1;" ::: "memory");
       __syncwarp();
       const uint8_t *buf = stage0 + k * kStage;
@@ -1607,11 +1624,25 @@ __device__ __forceinline__ void kdec_columns(const QuantParams &P, float *Y, flo
   }
 }
 
+// The code block of (layer, head) lh as kdec_issue addresses tile sb of it: with
+// codes read in place, shifted so that tile sb's records land where code_unit puts
+// them (the tile, 2048 BITS bytes, is one unit: the host enables this only where
+// every (layer, head) holds whole tiles).
+template <int BITS>
+__device__ __forceinline__ const uint8_t *kdec_block(const QuantParams &P, uint32_t sb, uint32_t lh) {
+  const size_t rec = P.group * BITS / 8, blk = (size_t)lh * P.n_tg * kHeadDim * rec;
+  if (P.in_lo >= P.in_hi) return P.codes + blk;
+  const size_t lead = (size_t)sb * (128u / P.group) * kHeadDim * rec;  // tile sb's first record in the block
+  return reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(code_unit(P, blk + lead)) - lead);
+}
+
 // The D-phase inputs of tile (sb, lh) for channel c: its (layer, head)'s width
-// decides the record size (a mixed-width launch dispatches per tile).
+// decides the record size (a mixed-width launch dispatches per tile).  `blk`: the
+// uniform-width launch's kdec_block for this tile.
 template <int BITS, bool MIXED>
 __device__ __forceinline__ void kdec_issue_any(const QuantParams &P, const WidthsArg<MIXED> &W, uint32_t sb,
-                                               uint32_t lh, int c, uint8_t *cbuf, uint32_t *mbuf) {
+                                               uint32_t lh, int c, uint8_t *cbuf, uint32_t *mbuf,
+                                               const uint8_t *blk) {
   if constexpr (MIXED) {
     const uint8_t *blk = P.codes + (size_t)16 * P.n_tg * P.group * W.wsum[lh];
     switch (width_of<MIXED>(W, lh)) {
@@ -1621,7 +1652,7 @@ __device__ __forceinline__ void kdec_issue_any(const QuantParams &P, const Width
       default: kdec_issue<8, BITS>(P, sb, lh, blk, c, cbuf, mbuf); break;
     }
   } else {
-    kdec_issue<BITS>(P, sb, lh, P.codes + (size_t)lh * P.n_tg * kHeadDim * (P.group * BITS / 8), c, cbuf, mbuf);
+    kdec_issue<BITS>(P, sb, lh, blk, c, cbuf, mbuf);
   }
 }
 
@@ -1649,7 +1680,8 @@ __global__ void __launch_bounds__(kKD, 3) kvc_dec_ktile(const QuantParams P, con
   cur.init(tile, n_sb, H);
   uint32_t mub = 0, anb = 0;
   int ex = 0;
-  kdec_issue_any<SB, MIXED>(P, W, cur.sb, cur.l * H + cur.h, tid, cbuf, mbuf);
+  kdec_issue_any<SB, MIXED>(P, W, cur.sb, cur.l * H + cur.h, tid, cbuf, mbuf,
+                            MIXED ? nullptr : kdec_block<SB>(P, cur.sb, cur.l * H + cur.h));
   if (smooth || DELTA) {
     const size_t cell = ((size_t)(cur.l * H + cur.h) * n_sb + cur.sb) * kHeadDim + tid;
     if (smooth) {
@@ -1663,6 +1695,9 @@ __global__ void __launch_bounds__(kKD, 3) kvc_dec_ktile(const QuantParams P, con
     const uint32_t t0 = sb * kSmoothBlock, nvalid = min((uint32_t)kSmoothBlock, T - t0);
     nxt = cur;
     nxt.advance(step_sb, step_h, step_l, n_sb, H);
+    const bool more = tile + gridDim.x < n_tiles;
+    // the next tile's code block, looked up before this tile's D phase
+    const uint8_t *blk_n = !MIXED && more ? kdec_block<SB>(P, nxt.sb, nxt.l * H + nxt.h) : nullptr;
 
     // ---- D: column tid
     cp_async_wait_all_q();
@@ -1677,8 +1712,8 @@ __global__ void __launch_bounds__(kKD, 3) kvc_dec_ktile(const QuantParams P, con
       kdec_columns<BITS, HAD, SB>(P, Y, tab, cbuf, mbuf, smooth, mub, ex);
     }
     if constexpr (DELTA) anc[tid] = elt_to_f32(anb, BF16);
-    if (tile + gridDim.x < n_tiles) {  // this thread's slots are read: the next tile's inputs go there
-      kdec_issue_any<SB, MIXED>(P, W, nxt.sb, nxt.l * H + nxt.h, tid, cbuf, mbuf);
+    if (more) {  // this thread's slots are read: the next tile's inputs go there
+      kdec_issue_any<SB, MIXED>(P, W, nxt.sb, nxt.l * H + nxt.h, tid, cbuf, mbuf, blk_n);
       if (smooth || DELTA) {
         const size_t cell = ((size_t)(nxt.l * H + nxt.h) * n_sb + nxt.sb) * kHeadDim + tid;
         if (smooth) {

@@ -26,7 +26,8 @@ EXPORTS = ["kvc_plan", "kvc_plan_destroy", "kvc_workspace_bytes", "kvc_max_strea
            "kvc_section", "kvc_num_chunks", "kvc_encode", "kvc_decode", "kvc_quantize", "kvc_lossless_encode",
            "kvc_lossless_decode", "kvc_dequantize", "kvc_query", "kvc_status_str", "kvc_launch_count",
            "kvc_timing_enable", "kvc_timing_read", "kvc_debug_lookback", "kvc_lossless_encode_noalloc",
-           "kvc_header_bytes", "kvc_debug_generic_stages", "kvc_debug_quotient_check", "kvc_fuse_value_chunks"]
+           "kvc_header_bytes", "kvc_debug_generic_stages", "kvc_debug_quotient_check", "kvc_fuse_value_chunks",
+           "kvc_decode_codes_in_place"]
 
 
 class KvcError(RuntimeError):
@@ -112,6 +113,7 @@ def load(build_if_missing: bool = True):
             "kvc_header_bytes": (sz, [P]),
             "kvc_debug_generic_stages": (st, [P, C.c_int]),
             "kvc_fuse_value_chunks": (st, [P, C.c_int]),
+            "kvc_decode_codes_in_place": (st, [P, C.c_int]),
             "kvc_debug_quotient_check": (st, [C.c_uint32, C.c_uint32, C.POINTER(C.c_ulonglong), vp]),
         }
         for name, (res, args) in sigs.items():
@@ -322,6 +324,11 @@ def kvc_timing_read(plan: Plan, max_records: int = 4096):
 def kvc_fuse_value_chunks(plan: Plan, enable: bool):
     """kvc_encode with the value encoder writing its whole code chunks into the stream."""
     _check(plan.lib.kvc_fuse_value_chunks(plan.handle, int(bool(enable))), "kvc_fuse_value_chunks")
+
+
+def kvc_decode_codes_in_place(plan: Plan, enable: bool):
+    """kvc_decode with the dequantizers reading stored code chunks from the stream (the default)."""
+    _check(plan.lib.kvc_decode_codes_in_place(plan.handle, int(bool(enable))), "kvc_decode_codes_in_place")
 
 
 def kvc_debug_generic_stages(plan: Plan, enable: bool):
