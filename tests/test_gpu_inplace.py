@@ -6,7 +6,7 @@ timings: the lossless decoder is named ..._inplace when some tensor's code chunk
 stay in the stream.  Cases: both tensors, one, none; 2-, 4- and 8-bit codes; keys
 grouped over channels; a table large enough for the separate prepare step; a
 generic stage list; compressible chunks among the in-place ones; paged output; the
-token delta; profiles that must not take the path."""
+token delta; profiles that must not take the path; corrupt chunk tables."""
 import numpy as np
 import pytest
 import torch
@@ -180,3 +180,63 @@ def test_in_place_is_on_by_default_and_lossless_decode_writes_the_payload():
     codec.query()
     Qo, _ = O.quantize(U.oracle_profile(prof), case.oracle_shape(), case.host_bits(case.k), case.host_bits(case.v))
     assert np.array_equal(U.to_np(Qg, codec.plan.payload_bytes), Qo)
+
+
+@pytest.mark.parametrize("path", ["in_decoder", "prepare"])
+def test_in_place_decode_rejects_corrupt_tables_and_writes_nothing(path):
+    """Chunk-table corruptions of a chunk whose codes are read in place (its stored
+    flag cleared, its size changed) and a truncated stream: the decoder reports
+    CORRUPT, as the oracle does, and the reconstruction kernels write nothing.  The
+    table is checked inside the decoder for small tables, by the prepare step for
+    large ones (512-byte chunks, more than 16384 of them)."""
+    if path == "in_decoder":
+        prof = dict(smooth_keys=True, hadamard=True, bits_k=4, bits_v=4, group_k=128, group_v=128, stages=LC,
+                    chunk_bytes=8192)
+        case = U.Case(L=1, T=512, H=4, dtype="bf16", dist="llama", seed=11, profile=prof).materialize()
+        assert _expected(case) == (True, True)
+    else:
+        prof = dict(smooth_keys=True, hadamard=True, bits_k=2, bits_v=2, group_k=64, group_v=64, stages=LC,
+                    chunk_bytes=512)
+        case = U.Case(L=4, T=4096, H=8, dtype="bf16", dist="llama", seed=12, profile=prof).materialize()
+        assert _expected(case) == (False, True)
+    cb = prof["chunk_bytes"]
+    codec, sg, nbytes, sg_np, so, _, _ = U.encode_both(case)
+    lay = O.layout(U.oracle_profile(prof), case.oracle_shape())
+    table = so[lay.header_bytes:lay.header_bytes + 4 * lay.n_chunks].view(np.uint32)
+    c = lay.off[2] // cb + 1  # a whole value-code chunk, stored raw
+    assert table[c] >> 31 == 1 and (table[c] & 0x7FFFFFFF) == cb
+    e = lay.header_bytes + 4 * c
+    mutations = {
+        "stored_flag": lambda s: s.__setitem__(e + 3, s[e + 3] ^ 0x80),
+        "size": lambda s: s.__setitem__(e, s[e] ^ 0x10),
+        "truncate": None,
+    }
+    for name, mut in mutations.items():
+        s = so.copy()
+        if mut is None:
+            s = s[:-32]
+        else:
+            mut(s)
+        fo = O.decode(U.oracle_profile(prof), case.oracle_shape(), s,
+                      [np.zeros_like(a) for a in case.host_bits(case.k)],
+                      [np.zeros_like(a) for a in case.host_bits(case.v)])
+        assert fo & O.FLAG_CORRUPT, name
+        dev = torch.from_numpy(np.concatenate([s, np.zeros(64, np.uint8)])).cuda()
+        ok, ov = case.empty_like_kv(fill=0x1234)
+        kvc.kvc_timing_enable(codec.plan, True)
+        codec.decode(dev, s.size, ok, ov)
+        st, _, fg = codec.query()
+        names = {n for n, _ in kvc.kvc_timing_read(codec.plan)}
+        kvc.kvc_timing_enable(codec.plan, False)
+        assert any(n.endswith("_inplace") for n in names), (name, sorted(names))
+        assert ("kvc_decode_prepare" in names) == (path == "prepare"), (name, sorted(names))
+        assert st == kvc.KVC_ERR_CORRUPT and (fg & kvc.FLAG_CORRUPT), (name, st, fg)
+        for t in ok + ov:  # nothing written
+            assert bool((t.view(torch.int16) == 0x1234).all()), name
+    # and the plan decodes the intact stream afterwards
+    gk, gv, _ = _decode(codec, case, sg, nbytes, True)
+    hk = [np.zeros_like(a) for a in case.host_bits(case.k)]
+    hv = [np.zeros_like(a) for a in case.host_bits(case.v)]
+    assert O.decode(U.oracle_profile(prof), case.oracle_shape(), so, hk, hv) == 0
+    for g, h in zip(gk + gv, hk + hv):
+        assert np.array_equal(g, h)
