@@ -152,9 +152,9 @@ void kvc_plan_destroy(kvc_plan_t *plan);
 
 /* Bytes of the caller-provided device workspace encode/decode need ("persistent
  * runtime scratch", "Beyond Compression Ratio" §4.2): a 256-byte control block
- * (status word, stream size, chunk tickets), per-chunk look-back / offset words
- * (and one word per 4096 chunks for the decode's partial sums) and, when lossless
- * stages are on, the quantized payload. */
+ * (status word, stream size, chunk tickets), per-chunk look-back / offset /
+ * chunk-address words (and one word per 4096 chunks for the decode's partial
+ * sums) and, when lossless stages are on, the quantized payload. */
 size_t kvc_workspace_bytes(const kvc_plan_t *plan);
 /* Worst-case stream size (header + chunk table + every chunk stored raw): the
  * capacity of the caller's preallocated output buffer ("Beyond Compression
@@ -192,7 +192,9 @@ kvc_status kvc_encode(kvc_plan_t *plan, const kvc_kv *in, void *d_stream, size_t
  * restoration) of a stream of stream_bytes bytes (device) into the layers of
  * *out (device, same geometry as the plan; written, never read).  The header and
  * chunk table are checked against the plan on the device; a corrupt stream sets
- * KVC_FLAG_CORRUPT and leaves *out untouched.  No host sync. */
+ * KVC_FLAG_CORRUPT and leaves *out untouched.  The stream must stay unchanged
+ * until the decode has run: by default (kvc_decode_codes_in_place) the
+ * reconstruction reads the codes of stored chunks from it.  No host sync. */
 kvc_status kvc_decode(kvc_plan_t *plan, const void *d_stream, size_t stream_bytes, const kvc_kv *out,
                       void *d_workspace, size_t workspace_bytes, kvc_stream_t stream);
 
