@@ -1,8 +1,10 @@
 """The rule for which code chunks kvc_decode reads in place, as bench.py restates
 it to count the lossless decoder's bytes, agrees with the GPU tests' restatement
 (which the GPU tests check against the library's launches) on every profile those
-tests use and on a few more; and the two execution-choice entry points reject a
-null plan.  No GPU needed: plans are host objects."""
+tests use and on a few more; every unit the in-place kernels read through one chunk
+lookup lies inside one chunk under it; and the two execution-choice entry points
+reject a null plan.  No GPU needed: plans are host objects."""
+import numpy as np
 import pytest
 
 import bench
@@ -54,3 +56,44 @@ def test_execution_choices_reject_a_null_plan():
     kvc.kvc_decode_codes_in_place(plan, True)
     kvc.kvc_fuse_value_chunks(plan, True)
     assert plan.launches == 0
+
+
+@pytest.mark.parametrize("bk,bv,gk,gv,stages,chunk,L,T,H,dtype,had,page,extra", CASES + MORE)
+def test_units_read_in_place_stay_inside_one_chunk(bk, bv, gk, gv, stages, chunk, L, T, H, dtype, had, page,
+                                                   extra):
+    """What the in-place kernels rely on: each unit they read through one chunk
+    lookup -- a key-style tile (2048 bits bytes from its first record) or a value
+    step (the codes of 16 consecutive rows) -- lies inside one chunk wherever the
+    rule reads that tensor in place.  Every unit of every accepted profile, from the
+    oracle's layout."""
+    prof = dict(smooth_keys=True, hadamard=had, bits_k=bk, bits_v=bv, group_k=gk, group_v=gv, stages=stages,
+                chunk_bytes=chunk)
+    prof.update(extra)
+    case = U.Case(L=L, T=T, H=H, dtype=dtype, page_size=page, profile=prof)
+    if page:
+        case.n_pages = -(-T // page)
+    plan = kvc.Plan(U.kvc_profile(prof), case.kvc_shape())
+    lay = O.layout(U.oracle_profile(prof), case.oracle_shape())
+    ranges = bench.in_place_ranges(plan, T)
+    for t, ok in enumerate(_expected(case)):
+        if not ok:
+            continue
+        bits = bv if t else bk
+        G = gv if t else gk
+        off, size = lay.off[2 * t], lay.size[2 * t]
+        assert (off // chunk, (off + size) // chunk) in ranges
+        if prof.get("axis_v" if t else "axis_k", 1 if t else 0) == 0:  # tiles over tokens
+            n_tg, ng, rec = -(-T // G), 128 // G, G * bits // 8
+            lh = np.arange(L * H, dtype=np.int64)[:, None]
+            sb = np.arange(-(-T // 128), dtype=np.int64)[None, :]
+            start = off + (lh * n_tg + sb * ng) * 128 * rec
+            length = np.minimum(ng, n_tg - sb * ng) * 128 * rec  # the tile's groups
+            assert (length == 2048 * bits).all()
+        else:  # value steps of 16 rows
+            NR = L * T * H
+            itn = np.arange(-(-NR // 16), dtype=np.int64)
+            start = off + itn * 256 * bits
+            length = np.minimum(16, NR - 16 * itn) * 16 * bits
+        end = start + length
+        assert (start // chunk == (end - 1) // chunk).all()
+        assert end.max() <= off + size
