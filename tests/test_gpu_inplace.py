@@ -6,7 +6,8 @@ timings: the lossless decoder is named ..._inplace when some tensor's code chunk
 stay in the stream.  Cases: both tensors, one, none; 2-, 4- and 8-bit codes; keys
 grouped over channels; a table large enough for the separate prepare step; a
 generic stage list; compressible chunks among the in-place ones; paged output; the
-token delta; profiles that must not take the path; corrupt chunk tables."""
+token delta; profiles that must not take the path; corrupt chunk tables; more chunks
+per decoder CTA than it has threads."""
 import numpy as np
 import pytest
 import torch
@@ -240,3 +241,38 @@ def test_in_place_decode_rejects_corrupt_tables_and_writes_nothing(path):
     assert O.decode(U.oracle_profile(prof), case.oracle_shape(), so, hk, hv) == 0
     for g, h in zip(gk + gv, hk + hv):
         assert np.array_equal(g, h)
+
+
+def test_in_place_decode_with_more_chunks_per_cta_than_threads():
+    """A chunk table of 405,504 entries (2-bit codes in 512-byte chunks): each CTA of
+    the lossless decoder owns more chunks than it has threads, so it settles them in
+    several batches of one chunk per thread.  The reconstruction must equal, element
+    for element, the decode that restores every chunk into the payload first (whose
+    parity with the oracle the tests above check)."""
+    prof = dict(smooth_keys=True, hadamard=True, bits_k=2, bits_v=2, group_k=32, group_v=32, stages=LC,
+                chunk_bytes=512)
+    case = U.Case(L=8, T=32768, H=8, dtype="bf16", dist="llama", seed=13, profile=prof, gen_device="cuda")
+    case.materialize()
+    assert _expected(case) == (False, True)
+    codec = U.Codec(U.kvc_profile(prof), case.kvc_shape())
+    n_ctas = torch.cuda.get_device_properties(0).multi_processor_count * 4  # at most 4 of 512 threads per SM
+    assert codec.plan.n_chunks > 512 * n_ctas
+    sg = codec.encode(case.k, case.v)
+    st, nbytes, flags = codec.query()
+    assert st == kvc.KVC_OK and flags == 0
+    outs = {}
+    for in_place in (True, False):
+        kvc.kvc_decode_codes_in_place(codec.plan, in_place)
+        ok, ov = case.empty_like_kv()
+        kvc.kvc_timing_enable(codec.plan, True)
+        codec.decode(sg, nbytes, ok, ov)
+        st, _, flags = codec.query()
+        names = {n for n, _ in kvc.kvc_timing_read(codec.plan)}
+        kvc.kvc_timing_enable(codec.plan, False)
+        assert st == kvc.KVC_OK and flags == 0, (in_place, st, flags)
+        assert "kvc_decode_prepare" in names
+        assert ("kvc_lossless_dec_inplace" in names) == in_place, sorted(names)
+        outs[in_place] = (ok, ov)
+    kvc.kvc_decode_codes_in_place(codec.plan, True)
+    for a, b in zip(outs[True][0] + outs[True][1], outs[False][0] + outs[False][1]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
